@@ -1,0 +1,252 @@
+// C ABI of libfa.so: argument validation, TMA descriptor encoding, launches,
+// the device status word, and two small diagnostic kernels.  The operations
+// and their argument conventions are documented in include/fa.h.
+#include <math.h>
+#include <mutex>
+#include <stdint.h>
+
+#include "fa.h"
+#include "fa_device.cuh"
+#include "fa_kernels.h"
+
+namespace fa {
+
+// The status word every kernel writes through a pointer (see fa_device.cuh).
+__device__ unsigned int g_status_word;
+
+namespace {
+
+int g_last_site = 0;
+
+// Device address of g_status_word for the current device, looked up once per
+// device with that device current.
+unsigned int* status_ptr() {
+  static std::mutex mu;
+  static unsigned int* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  return ptrs[dev];
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 [BH, N, d] viewed as a 3-D tensor (d, N, BH); the box is 64 columns
+// (128 bytes, one 128B-swizzle row) x 128 rows x 1 head.  Rows past N read
+// as zeros.
+bool encode_tile_map(CUtensorMap* map, const void* base, int N, int BH, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Shape checks shared by forward and backward.  Returns FA_OK, or the error,
+// with *empty set when there is nothing to compute.
+int check_shape(int B, int H, int N, int d, float scale, bool* empty) {
+  *empty = false;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) {
+    *empty = true;
+    return FA_OK;
+  }
+  const long long bh = static_cast<long long>(B) * H;
+  // grid sizes and int row indices inside the kernels
+  if (bh > (1LL << 30) || static_cast<long long>(N) * bh > (1LL << 40)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+constexpr size_t kWsAlign = 256;
+size_t round_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+__global__ void exp2_poly_eval_kernel(const float* x, float* y, long long n) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    y[i] = exp2_poly(x[i]);
+}
+
+// One mbarrier that nothing arrives on; the bounded wait must give up.
+__global__ void bounded_wait_kernel(unsigned int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t mbar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&mbar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{&abort_flag, status};
+  mbar_wait(smem_u32(&mbar), 0, ctl, 0x0F0, limit_ns);
+  __syncthreads();
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, void* stream) {
+  bool empty = false;
+  int rc = check_shape(B, H, N, d, scale, &empty);
+  if (rc != FA_OK || empty) return rc;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
+    return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+
+  FwdParams p;
+  const int BH = B * H;
+  if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
+      !encode_tile_map(&p.tm_v, v, N, BH, d))
+    return FA_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  p.N = N;
+  p.BH = BH;
+  p.n_qblk = (N + 2 * kBlockM - 1) / (2 * kBlockM);
+  p.causal = causal;
+  p.c = scale * 1.4426950408889634f;
+  p.ln2 = 0.6931471805599453f;
+  if (static_cast<long long>(p.n_qblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  return launch_fwd(p, d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  bool empty = false;
+  if (check_shape(B, H, N, d, 1.0f, &empty) != FA_OK || empty) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return round_up(rows * sizeof(float)) + round_up(rows * d * sizeof(float));
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  bool empty = false;
+  int rc = check_shape(B, H, N, d, scale, &empty);
+  if (rc != FA_OK || empty) return rc;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) != 0) return FA_ERR_WORKSPACE;
+
+  const int BH = B * H;
+  const long long rows = static_cast<long long>(BH) * N;
+  float* dsum = static_cast<float*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                           round_up(static_cast<size_t>(rows) * sizeof(float)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  BwdParams p;
+  if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
+      !encode_tile_map(&p.tm_v, v, N, BH, d) || !encode_tile_map(&p.tm_do, dout, N, BH, d))
+    return FA_ERR_CUDA;
+  p.lse = lse;
+  p.dsum = dsum;
+  p.dq_acc = dq_acc;
+  p.dk = dk;
+  p.dv = dv;
+  p.status = status_ptr();
+  if (!p.status) return FA_ERR_CUDA;
+  p.N = N;
+  p.BH = BH;
+  p.n_kblk = (N + kBlockN - 1) / kBlockN;
+  p.causal = causal;
+  p.c = scale * 1.4426950408889634f;
+  p.scale = scale;
+  p.log2e = 1.4426950408889634f;
+  if (static_cast<long long>(p.n_kblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+
+  if (launch_bwd_pre(o, dout, dsum, dq_acc, rows, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_main(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_post(dq_acc, dq, rows * d, s) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+int fa_last_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0;
+  const unsigned int zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  g_last_site = static_cast<int>((word >> 8) & 0xFFFFu);
+  const int code = static_cast<int>(word & 0xFFu);
+  return code == 0 ? FA_OK : code;
+}
+
+int fa_last_device_site(void) { return g_last_site; }
+
+int fa_exp2_poly_eval(const float* x, float* y, long long n, void* stream) {
+  if (n < 0) return FA_ERR_INVALID_ARG;
+  if (n == 0) return FA_OK;
+  if (!x || !y || !aligned4(x) || !aligned4(y)) return FA_ERR_INVALID_ARG;
+  const long long blocks = (n + 255) / 256;
+  exp2_poly_eval_kernel<<<static_cast<unsigned int>(blocks < 4096 ? blocks : 4096), 256, 0,
+                          static_cast<cudaStream_t>(stream)>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_debug_bounded_wait(unsigned long long limit_ns, void* stream) {
+  if (limit_ns < 1000000ull || limit_ns > 10000000000ull) return FA_ERR_INVALID_ARG;
+  unsigned int* status = status_ptr();
+  if (!status) return FA_ERR_CUDA;
+  bounded_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

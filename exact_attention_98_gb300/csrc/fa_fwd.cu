@@ -1,0 +1,403 @@
+// Forward exact attention for sm_103a: TMA-staged tiles, tcgen05 MMAs with
+// S and O accumulated in tensor memory, warp-specialised roles.
+//
+// What the pages ask of the forward (FlashAttention-4 abstract, items 1-3;
+// "Les capacités de Blackwell qui l'ont rendu possible" of the French page):
+//   * pipelines where the tensor cores, the exponential units and memory
+//     overlap -> one load warp, one MMA-issuing thread, two softmax
+//     warpgroups working on two query tiles in ping-pong;
+//   * accumulators and intermediates in tensor memory -> S_t, O_t and P_t
+//     (P written in place of S) for both query tiles: 2 x (128 + d) columns;
+//   * exponentials partly on the FMA pipe (exp2_poly) and partly on MUFU;
+//   * conditional rescaling: O_t and the row sum are rescaled only when a row
+//     max grows by more than kRescaleThreshold (log2 units).
+//
+// CTA = two 128-row query tiles of one (batch, head); keys and values stream
+// through a ring of shared-memory slots (K_j and V_j alternate).
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax warpgroup for query tile 0 (thread = one query row)
+//   warps 4-7  softmax warpgroup for query tile 1
+//   warp  8    TMA producer
+//   warp  9    tensor-memory allocator; lane 0 issues every MMA
+//
+// MMA order per key tile j (ping-pong: while one warpgroup computes the
+// softmax of its tile the tensor core works on the other tile):
+//   prologue: S_0(0), S_1(0)
+//   j:        [P_0(j)] O_0 += P_0(j) V_j, S_0(j+1);  [P_1(j)] O_1 += P_1(j) V_j, S_1(j+1)
+// A commit after S_t(j+1) also covers O_t += P_t(j) V_j (a thread's tcgen05
+// operations complete in issue order), so when a softmax warpgroup sees S_t(j)
+// it may read and rescale O_t.
+#include "fa_device.cuh"
+#include "fa_kernels.h"
+
+namespace fa {
+namespace {
+
+template <int D>
+struct FwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kThreads = 320;
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;
+  static constexpr int kTileBytes = kBlockM * D * 2;  // one Q, K or V tile (bf16)
+  static constexpr int kHalfBytes = kBlockM * 64 * 2;  // one 64-column swizzle block
+  static constexpr int kSlots = (D == 128) ? 4 : 6;
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+  // barriers: q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_full[2], mma_done
+  static constexpr int kBarQFull = 0;
+  static constexpr int kBarFull = 1;
+  static constexpr int kBarEmpty = 1 + kSlots;
+  static constexpr int kBarSFull = 1 + 2 * kSlots;
+  static constexpr int kBarPFull = kBarSFull + 2;
+  static constexpr int kBarOFull = kBarPFull + 2;
+  static constexpr int kBarMmaDone = kBarOFull + 2;
+  static constexpr int kNumBars = kBarMmaDone + 1;
+  static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
+  static constexpr int kAbortOff = kTmemSlotOff + 4;
+  static constexpr int kSmemUsed = kAbortOff + 4;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSCol0 = 0;    // S_t / P_t at t * 128
+  static constexpr uint32_t kOCol0 = 256;  // O_t at 256 + t * D
+  static constexpr int kPolyPerOctet = 2;  // of every 8 exponentials, this many on the FMA pipe
+};
+
+// Wait-site codes recorded on a timeout (bits 8..23 of the status word).
+enum : unsigned int {
+  kSiteEmpty = 0x101,
+  kSiteQFull = 0x102,
+  kSiteKFull = 0x103,
+  kSiteVFull = 0x104,
+  kSitePFull = 0x105,
+  kSiteSFull = 0x106,
+  kSiteOFull = 0x107,
+};
+
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
+  const WaitCtl ctl{abort_flag, p.status};
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  // Work item: heaviest query blocks first (causal blocks near the end of the
+  // sequence see the most keys).
+  const int blk = blockIdx.x;
+  const int qblk = p.n_qblk - 1 - blk / p.BH;
+  const int bh = blk % p.BH;
+  const int q0 = qblk * 2 * kBlockM;
+  const int n_ktiles = (p.N + kBlockN - 1) / kBlockN;
+  int nkv[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qs = q0 + t * kBlockM;
+    if (qs >= p.N) nkv[t] = 0;
+    else nkv[t] = p.causal ? min(n_ktiles, qs / kBlockN + 1) : n_ktiles;
+  }
+  const int nmax = max(nkv[0], nkv[1]);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(C::kBarQFull), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(bar(C::kBarFull + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarSFull + t), 1);
+      mbar_init(bar(C::kBarPFull + t), kBlockM);
+      mbar_init(bar(C::kBarOFull + t), 1);
+    }
+    mbar_init(bar(C::kBarMmaDone), 1);
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == C::kProducerWarp) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      const uint32_t q_smem = sbase + C::kQOff;
+      mbar_arrive_expect_tx(bar(C::kBarQFull), 2 * C::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(q_smem + t * C::kTileBytes + h * C::kHalfBytes, &p.tm_q, bar(C::kBarQFull),
+                      h * 64, q0 + t * kBlockM, bh);
+      int issued = 0;
+      for (int idx = 0; idx < 2 * nmax; ++idx) {
+        const int slot = idx % C::kSlots;
+        const int use = idx / C::kSlots;
+        if (use > 0 && !mbar_wait(bar(C::kBarEmpty + slot), (use - 1) & 1, ctl, kSiteEmpty)) break;
+        const CUtensorMap* map = (idx & 1) ? &p.tm_v : &p.tm_k;
+        const int j = idx >> 1;
+        const uint32_t dst = sbase + C::kRingOff + slot * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(dst + h * C::kHalfBytes, map, bar(C::kBarFull + slot), h * 64, j * kBlockN, bh);
+        issued = idx + 1;
+      }
+      // Let every copy this CTA started land before shared memory is released
+      // (only waits on the give-up path; on the normal path all have landed).
+      mbar_wait_drain(bar(C::kBarQFull), 0);
+      for (int idx = max(0, issued - C::kSlots); idx < issued; ++idx)
+        mbar_wait_drain(bar(C::kBarFull + idx % C::kSlots), (idx / C::kSlots) & 1);
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
+      const uint32_t q_smem = sbase + C::kQOff;
+      const uint32_t ring = sbase + C::kRingOff;
+      auto slot_of = [](int idx) { return idx % C::kSlots; };
+      auto parity_of = [](int idx) { return static_cast<uint32_t>((idx / C::kSlots) & 1); };
+
+      // S_t = Q_t K^T : M = 128 query rows, N = 128 keys, K = d (16 per MMA).
+      // Both operands K-major, 128B-swizzled: 64 columns per 16 KB block.
+      auto issue_s = [&](int t, int kslot) {
+        const uint32_t a0 = q_smem + t * C::kTileBytes;
+        const uint32_t b0 = ring + kslot * C::kTileBytes;
+        const uint32_t dcol = tmem_base + C::kSCol0 + t * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+          mma_ss(dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), kIdescS,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V : M = 128, N = d, K = 128 keys.  P_t (bf16, two per
+      // 32-bit column) sits in tensor memory over S_t; V is MN-major in shared
+      // memory (d contiguous), 8-key groups 1024 B apart, 64-wide d blocks
+      // kHalfBytes apart.
+      auto issue_pv = [&](int t, int vslot, bool accumulate) {
+        const uint32_t b0 = ring + vslot * C::kTileBytes;
+        const uint32_t acol = tmem_base + C::kSCol0 + t * 128;
+        const uint32_t dcol = tmem_base + C::kOCol0 + t * D;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          mma_ts(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024), kIdescPV,
+                 (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      bool ok = mbar_wait(bar(C::kBarQFull), 0, ctl, kSiteQFull);
+      if (ok) ok = mbar_wait(bar(C::kBarFull + slot_of(0)), parity_of(0), ctl, kSiteKFull);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (nkv[t] > 0) {
+            issue_s(t, slot_of(0));
+            mma_commit(bar(C::kBarSFull + t));
+          }
+        mma_commit(bar(C::kBarEmpty + slot_of(0)));
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int vidx = 2 * j + 1, kidx = 2 * j + 2;
+        ok = mbar_wait(bar(C::kBarFull + slot_of(vidx)), parity_of(vidx), ctl, kSiteVFull);
+        if (!ok) break;
+        tc_fence_after();
+        bool k_next_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nkv[t]) continue;
+          ok = mbar_wait(bar(C::kBarPFull + t), j & 1, ctl, kSitePFull);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, slot_of(vidx), j > 0);
+          if (j == nkv[t] - 1) {
+            mma_commit(bar(C::kBarOFull + t));
+          } else {
+            if (!k_next_ready) {
+              ok = mbar_wait(bar(C::kBarFull + slot_of(kidx)), parity_of(kidx), ctl, kSiteKFull);
+              if (!ok) break;
+              tc_fence_after();
+              k_next_ready = true;
+            }
+            issue_s(t, slot_of(kidx));
+            mma_commit(bar(C::kBarSFull + t));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(C::kBarEmpty + slot_of(vidx)));
+        if (k_next_ready) mma_commit(bar(C::kBarEmpty + slot_of(kidx)));
+      }
+      // Every MMA this thread issued must finish before tensor memory is freed.
+      mma_commit(bar(C::kBarMmaDone));
+      mbar_wait_drain(bar(C::kBarMmaDone), 0);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int t = warp >> 2;             // query tile of this warpgroup
+    const int quarter = warp & 3;        // tensor-memory lane quarter
+    const int row = quarter * 32 + lane;  // row within the query tile
+    const int qpos = q0 + t * kBlockM + row;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t t_s = lane_base + C::kSCol0 + t * 128;
+    const uint32_t t_o = lane_base + C::kOCol0 + t * D;
+    const float c = p.c;
+    const bool ragged = (p.N % kBlockN) != 0;
+
+    float m_used = -INFINITY;  // running row max in log2 units (scores * c)
+    float l = 0.0f;            // running row sum of exp2(x - m_used)
+    bool ok = true;
+    for (int j = 0; j < nkv[t]; ++j) {
+      ok = mbar_wait(bar(C::kBarSFull + t), j & 1, ctl, kSiteSFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int kbase = j * kBlockN;
+      const bool edge = (p.causal && j == nkv[t] - 1) || (ragged && j == n_ktiles - 1);
+      auto valid = [&](int col) {
+        const int kpos = kbase + col;
+        return kpos < p.N && (!p.causal || kpos <= qpos);
+      };
+
+      // pass 1: row max of this tile
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int ch = 0; ch < kBlockN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(t_s + ch * 32, r);
+        tmem_ld_wait(r);
+        if (edge) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (valid(ch * 32 + e)) mx = fmaxf(mx, __uint_as_float(r[e]) * c);
+        } else {
+          float m2 = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) m2 = fmaxf(m2, __uint_as_float(r[e]));
+          mx = fmaxf(mx, m2 * c);
+        }
+      }
+      // Conditional rescale: move the reference max only when it grows by
+      // more than the threshold (always on the first tile, m_used = -inf).
+      const float m_new = fmaxf(m_used, mx);
+      const bool need = (m_new - m_used) > kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2_mufu(m_used - m_new) : 1.0f;
+        if (j > 0) {
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld32(t_o + ch * 32, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(t_o + ch * 32, r);
+          }
+          tmem_st_wait();
+        }
+        if (need) {
+          l *= alpha;
+          m_used = m_new;
+        }
+      }
+
+      // pass 2: P = exp2(x - m_used) -> bf16 into tensor memory over S
+      const float neg_m = -m_used;
+#pragma unroll 1
+      for (int ch = 0; ch < kBlockN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(t_s + ch * 32, r);
+        tmem_ld_wait(r);
+        float pv[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float x = fmaf(__uint_as_float(r[e]), c, neg_m);
+          pv[e] = ((e & 7) < C::kPolyPerOctet) ? exp2_poly(x) : ex2_mufu(x);
+        }
+        if (edge) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (!valid(ch * 32 + e)) pv[e] = 0.0f;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          l += pv[2 * e] + pv[2 * e + 1];
+          w[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+        }
+        tmem_st16(t_s + ch * 16, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPFull + t));
+    }
+
+    // epilogue: O / l -> bf16, LSE = ln(2) * m_used + ln(l)
+    if (ok && nkv[t] > 0) {
+      ok = mbar_wait(bar(C::kBarOFull + t), 0, ctl, kSiteOFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l;
+        const bool in_range = qpos < p.N;
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(t_o + ch * 32, r);
+          tmem_ld_wait(r);
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+          if (in_range) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          }
+        }
+        if (in_range) p.lse[static_cast<size_t>(bh) * p.N + qpos] = m_used * p.ln2 + logf(l);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  cudaError_t err = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const long long blocks = static_cast<long long>(p.n_qblk) * p.BH;
+  fa_fwd_kernel<D><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
+  if (d == 128) return launch_fwd_d<128>(p, stream);
+  if (d == 64) return launch_fwd_d<64>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

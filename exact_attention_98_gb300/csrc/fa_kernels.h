@@ -1,0 +1,68 @@
+// Parameter blocks and launchers shared between the C-ABI layer (fa_api.cu)
+// and the kernel translation units (fa_fwd.cu, fa_bwd.cu).  Host code only
+// sees these declarations; the kernels are internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Tile shape shared by the forward and backward kernels: 128 query rows x 128
+// key rows per step, the tcgen05 M = 128 single-CTA shape.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+// Conditional-rescale threshold, in log2 units of the scaled scores: O and the
+// row sum are rescaled only when a row max grows by more than 2^8.  Any value
+// gives the same result (the final division uses the same stale max); it only
+// bounds the fp32 range of the unnormalised values, which stay <= 2^8.
+constexpr float kRescaleThreshold = 8.0f;
+
+struct FwdParams {
+  CUtensorMap tm_q;  // bf16 [BH, N, d], box {64, 128, 1}, 128B swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  void* o;               // bf16 [BH, N, d]
+  float* lse;            // fp32 [BH, N]
+  unsigned int* status;  // device status word
+  int N;
+  int BH;
+  int n_qblk;  // ceil(N / 256): each CTA takes two 128-row query tiles
+  int causal;
+  float c;          // scale * log2(e): scores enter exp2 in these units
+  float ln2;        // ln(2), to turn the log2-unit row max into LSE
+};
+
+struct BwdParams {
+  CUtensorMap tm_q;   // bf16 [BH, N, d]
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const float* lse;   // fp32 [BH, N]
+  const float* dsum;  // fp32 [BH, N]: D = rowsum(dO * O)
+  float* dq_acc;      // fp32 [BH, N, d], zeroed before the main kernel
+  void* dk;           // bf16 [BH, N, d]
+  void* dv;           // bf16 [BH, N, d]
+  unsigned int* status;
+  int N;
+  int BH;
+  int n_kblk;  // ceil(N / 128)
+  int causal;
+  float c;      // scale * log2(e)
+  float scale;  // folded into dS so that dQ and dK come out scaled
+  float log2e;
+};
+
+// Forward: one launch of the tcgen05 kernel for head dim d (64 or 128).
+cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
+
+// Backward: D = rowsum(dO * O) and dQ accumulator zeroing.
+cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* dq_acc,
+                           long long rows, int d, cudaStream_t stream);
+// Backward main kernel (key/value stationary).
+cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
+// dQ = dQ accumulator -> bf16.
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, cudaStream_t stream);
+
+}  // namespace fa

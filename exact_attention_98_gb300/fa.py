@@ -1,0 +1,195 @@
+"""Python binding of libfa.so (include/fa.h), argument marshalling only.
+
+The functions with the C names (``fa_fwd``, ``fa_bwd``, ...) take torch CUDA
+tensors that the caller allocated and pass their device pointers, sizes and the
+current CUDA stream straight to the C ABI; every step of the computation runs
+in the library's kernels.  ``forward`` / ``backward`` are conveniences that
+allocate the outputs with torch and then call those.
+
+There is no fallback: if libfa.so is missing or cannot be loaded, importing
+this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "fa.h")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_WORKSPACE = 5
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where} failed: {status_string(code)} ({code})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -m exact_attention_98_gb300.build` "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_bwd_workspace_bytes.restype = sz
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_last_device_status.argtypes = [vp]
+    lib.fa_last_device_status.restype = i
+    lib.fa_last_device_site.argtypes = []
+    lib.fa_last_device_site.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_exp2_poly_eval.argtypes = [vp, vp, ctypes.c_longlong, vp]
+    lib.fa_exp2_poly_eval.restype = i
+    lib.fa_debug_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
+    lib.fa_debug_bounded_wait.restype = i
+    return lib
+
+
+lib = _load()
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions include/fa.h declares."""
+    text = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(fa_\w+)\s*\(", text, re.M)))
+
+
+def status_string(code: int) -> str:
+    return lib.fa_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != FA_OK:
+        raise FAError(code, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d]")
+    return tuple(int(x) for x in q.shape)
+
+
+def _check_tensor(t, name, dtype, shape):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# --- the C entry points --------------------------------------------------------
+
+
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
+    B, H, N, d = _shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
+    _check_tensor(lse, "lse", torch.float32, (B, H, N))
+    _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+                      int(bool(causal)), _stream(stream)), "fa_fwd")
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib.fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool, workspace,
+           stream=None) -> None:
+    B, H, N, d = _shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
+    _check_tensor(lse, "lse", torch.float32, (B, H, N))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                      _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                      _ptr(workspace), ws_bytes, _stream(stream)), "fa_bwd")
+
+
+def fa_last_device_status(stream=None) -> int:
+    return int(lib.fa_last_device_status(_stream(stream)))
+
+
+def fa_last_device_site() -> int:
+    return int(lib.fa_last_device_site())
+
+
+def fa_status_string(code: int) -> str:
+    return status_string(code)
+
+
+def fa_exp2_poly_eval(x, y, stream=None) -> None:
+    _check_tensor(x, "x", torch.float32, x.shape)
+    _check_tensor(y, "y", torch.float32, x.shape)
+    _check(lib.fa_exp2_poly_eval(_ptr(x), _ptr(y), x.numel(), _stream(stream)),
+           "fa_exp2_poly_eval")
+
+
+def fa_debug_bounded_wait(limit_ns: int, stream=None) -> None:
+    _check(lib.fa_debug_bounded_wait(int(limit_ns), _stream(stream)), "fa_debug_bounded_wait")
+
+
+# --- conveniences ----------------------------------------------------------------
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Returns (o, lse) freshly allocated on q's device."""
+    B, H, N, d = _shape(q)
+    scale = default_scale(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def workspace_for(q):
+    B, H, N, d = _shape(q)
+    n = fa_bwd_workspace_bytes(B, H, N, d)
+    # torch's caching allocator hands out 512-byte aligned blocks
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+             workspace=None, stream=None):
+    """Returns (dq, dk, dv) freshly allocated on q's device."""
+    B, H, N, d = _shape(q)
+    scale = default_scale(d) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    if workspace is None:
+        workspace = workspace_for(q)
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale, causal, workspace, stream)
+    return dq, dk, dv

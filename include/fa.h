@@ -1,0 +1,128 @@
+/*
+ * fa.h -- C ABI of the exact-attention library (libfa.so), sm_103a (GB300).
+ *
+ * The library computes exact scaled-dot-product attention, forward and
+ * backward, tile by tile with an online softmax.  What it computes is the
+ * plain definition: S = scale * Q K^T (optionally causal: key j <= query i),
+ * P = softmax over each row of S, O = P V, LSE = ln sum_j exp(S_ij) -- the
+ * two matrix products and softmax of "FlashAttention-4 : comment Together AI a
+ * accéléré l'attention sur GPU Blackwell", section "Pourquoi l'approche
+ * standard ne fonctionne plus"; the pages state that the tiled schedules leave
+ * the mechanism unchanged ("FlashAttention-3 и FlashAttention-4", section
+ * "Ключевая идея FlashAttention-3").  The backward pass is the chain rule of
+ * the loss sum(O * dO): D = rowsum(dO * O), dP = dO V^T, dS = P * (dP - D),
+ * dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors Q, K, V, O, dO, dQ, dK, dV are bf16, contiguous [B, H, N, d]
+ *     (d fastest), device pointers, 16-byte aligned.  LSE is fp32 [B, H, N].
+ *   - d must be 64 or 128.  Any N >= 0 is accepted; a ragged last tile is
+ *     masked.  B, H, N of 0 are a no-op that returns FA_OK.
+ *   - Queries and keys have the same length N, so "causal" is unambiguous.
+ *   - The caller owns every buffer; the library allocates no device memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  The return value reports argument validation and
+ *     launch errors only.  A kernel that gives up on a bounded wait records
+ *     FA_ERR_TIMEOUT in a device status word instead of hanging; read it
+ *     with fa_last_device_status().
+ *   - Input and output buffers must not overlap.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misaligned buffer   */
+  FA_ERR_UNSUPPORTED = 2, /* a shape the kernels do not handle (d not 64/128)  */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed      */
+  FA_ERR_TIMEOUT = 4,     /* a kernel's bounded wait expired (device status)    */
+  FA_ERR_WORKSPACE = 5    /* the backward workspace is missing or too small     */
+} fa_status;
+
+/*
+ * Forward.  O = softmax(scale * Q K^T [masked]) V and, per row,
+ * LSE = ln sum_j exp(scale * q_i . k_j) over the allowed keys (natural log of
+ * the scaled scores).
+ *   q, k, v : in,  bf16 [B, H, N, d]
+ *   o       : out, bf16 [B, H, N, d]
+ *   lse     : out, fp32 [B, H, N]
+ *   scale   : the factor on Q K^T (usually 1/sqrt(d)); must be finite and > 0
+ *   causal  : 0 = every key, 1 = key j <= query i
+ * Kernels: TMA-staged Q/K/V tiles, tcgen05 MMAs accumulating S and O in
+ * tensor memory, warp-specialised load / MMA / softmax roles, polynomial exp2
+ * mixed with the MUFU unit, O rescaled only when a row max grows past a
+ * threshold (FlashAttention-4 abstract, items 1-3).
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+           int N, int d, float scale, int causal, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: fp32 D = rowsum(dO * O) [B, H, N]
+ * and the fp32 dQ accumulator [B, H, N, d], each 256-byte aligned.
+ * Returns 0 for empty or unsupported shapes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward of the loss sum(O * dO).
+ *   q, k, v   : in,  bf16 [B, H, N, d]  (the forward's inputs)
+ *   o, lse    : in,  the forward's outputs (bf16 [B,H,N,d], fp32 [B,H,N])
+ *   dout      : in,  bf16 [B, H, N, d]
+ *   dq, dk, dv: out, bf16 [B, H, N, d]
+ *   workspace : device scratch of at least fa_bwd_workspace_bytes(B,H,N,d)
+ *               bytes, 256-byte aligned, owned by the caller; its contents on
+ *               entry do not matter and are overwritten.
+ * Three kernels run in stream order: D and dQ-accumulator zeroing; the
+ * key/value-stationary main kernel (S and dP recomputed in tensor memory, dK
+ * and dV accumulated there, dQ added with fp32 atomics -- the backward's
+ * "reductions and atomic updates" of "FlashAttention-3 и FlashAttention-4",
+ * section "Режим 2-CTA MMA"); and dQ conversion to bf16.
+ * Returns FA_ERR_WORKSPACE when workspace is NULL or workspace_bytes is short.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word:
+ * FA_OK, or FA_ERR_TIMEOUT when a kernel gave up on a bounded wait since the
+ * last call, or FA_ERR_CUDA when the synchronisation itself failed.
+ */
+int fa_last_device_status(void* stream);
+
+/* Extra detail about the last device status: the code of the wait site that
+ * timed out (0 if none).  Valid after fa_last_device_status(). */
+int fa_last_device_site(void);
+
+/* Human-readable name of a fa_status value (static string). */
+const char* fa_status_string(int status);
+
+/*
+ * Diagnostic: evaluates the kernels' polynomial exp2 (the software-emulated
+ * exponential on the FMA pipe, FlashAttention-4 abstract item 2; "Программная
+ * эмуляция экспоненты" of "FlashAttention-3 и FlashAttention-4") on n fp32
+ * values.  x, y are device pointers; the input is clamped to the kernels'
+ * domain [-125, 127] first.  For testing the approximation only.
+ */
+int fa_exp2_poly_eval(const float* x, float* y, long long n, void* stream);
+
+/*
+ * Diagnostic: runs one kernel whose only work is an mbarrier wait that nothing
+ * ever completes, bounded by limit_ns nanoseconds (1 ms .. 10 s).  It returns
+ * through the same give-up path as the attention kernels, so a following
+ * fa_last_device_status() must report FA_ERR_TIMEOUT and the CUDA context
+ * stays usable.  For testing the bounded-wait machinery without a fault.
+ */
+int fa_debug_bounded_wait(unsigned long long limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

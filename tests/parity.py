@@ -1,0 +1,92 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path, run the oracle on
+the same bf16 values (upcast exactly to fp64), and compare.
+
+Tolerances (the bounds the library is held to):
+  * O:   max |O - O_ref| <= 1e-2, where elements with |O_ref| >= 2 may also use
+         half a bf16 ulp of O_ref (the output is bf16: its rounding alone is
+         2^-7 there);
+  * LSE: max |LSE - LSE_ref| <= 1e-3;
+  * dQ, dK, dV: ||X - X_ref||_F / ||X_ref||_F <= 2e-2 over the compared rows.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from exact_attention_98_gb300.inputs import attention_inputs, sampled_rows
+
+O_ATOL = 1e-2
+LSE_ATOL = 1e-3
+GRAD_RTOL = 2e-2
+
+
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.maximum(ax, 1e-30)))
+    return np.where(ax > 0, np.exp2(e - 8), 0.0)
+
+
+def check_o(o_gpu: np.ndarray, o_ref: np.ndarray, what: str) -> float:
+    err = np.abs(o_gpu - o_ref)
+    bound = O_ATOL + np.where(np.abs(o_ref) >= 2.0, half_ulp_bf16(o_ref), 0.0)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: O max abs err {err.max():.3e}; {int(bad.sum())} elements "
+                           f"over the bound, worst at |O_ref| = {np.abs(o_ref[bad]).max():.3f}")
+    return float(err.max())
+
+
+def check_lse(lse_gpu: np.ndarray, lse_ref: np.ndarray, what: str) -> float:
+    err = float(np.abs(lse_gpu - lse_ref).max())
+    assert err <= LSE_ATOL, f"{what}: LSE max abs err {err:.3e}"
+    return err
+
+
+def rel_fro(x: np.ndarray, ref: np.ndarray) -> float:
+    den = float(np.linalg.norm(ref))
+    return float(np.linalg.norm(x - ref)) / max(den, 1e-30)
+
+
+def check_grad(x: np.ndarray, ref: np.ndarray, what: str) -> float:
+    err = rel_fro(x, ref)
+    assert err <= GRAD_RTOL, f"{what}: relative Frobenius error {err:.3e}"
+    return err
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def run_fwd(B, H, N, d, causal, seed=0, stress=False, scale=None):
+    from exact_attention_98_gb300 import fa
+
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    q, k, v, _ = attention_inputs(B, H, N, d, seed=seed, stress=stress, with_dout=False)
+    dev = torch.device("cuda")
+    o, lse = fa.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale)
+    status = fa.fa_last_device_status()
+    assert status == fa.FA_OK, fa.status_string(status)
+    return (q, k, v), to64(o), to64(lse), scale
+
+
+def compare_fwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_per_head=None):
+    """Forward parity.  full_heads: number of leading (b, h) slices compared on
+    every row (None = all); the others on sampled rows."""
+    (q, k, v), o, lse, scale = run_fwd(B, H, N, d, causal, seed, stress)
+    q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
+    worst_o = worst_l = 0.0
+    for b in range(B):
+        for h in range(H):
+            idx = b * H + h
+            if full_heads is None or idx < full_heads:
+                rows = None
+            else:
+                rows = sampled_rows(N, rows_per_head, b, h, H)
+            o_ref, l_ref = oracle.fwd_head(q64[b, h], k64[b, h], v64[b, h], scale, causal, rows=rows)
+            sel = slice(None) if rows is None else rows
+            what = f"B{B} H{H} N{N} d{d} causal={causal} stress={stress} head ({b},{h})"
+            worst_o = max(worst_o, check_o(o[b, h][sel], o_ref, what))
+            worst_l = max(worst_l, check_lse(lse[b, h][sel], l_ref, what))
+    return worst_o, worst_l

@@ -1,0 +1,109 @@
+"""The C ABI: the library loads, exports every function include/fa.h declares,
+and rejects bad arguments on the host (no GPU needed: these calls return
+before any CUDA work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_98_gb300 import build
+
+    build.build()
+    from exact_attention_98_gb300 import fa
+
+    return fa
+
+
+def declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(fa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared()
+    for must in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_last_device_status",
+                 "fa_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    assert lib.status_string(0) == "FA_OK"
+    assert lib.status_string(4) == "FA_ERR_TIMEOUT"
+    assert lib.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    ws = lib.fa_bwd_workspace_bytes
+    B, H, N, d = 2, 16, 8192, 128
+    rows = B * H * N
+    up = lambda x: (x + 255) // 256 * 256
+    assert ws(B, H, N, d) == up(4 * rows) + up(4 * rows * d)
+    assert ws(1, 1, 1, 64) == 256 + 256
+    assert ws(0, 1, 1, 64) == 0
+    assert ws(1, 1, 1, 96) == 0  # unsupported head dim
+
+
+P = ctypes.c_void_p
+
+
+def fwd(lib, q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, B=1, H=1, N=128, d=64,
+        scale=0.125, causal=0):
+    return lib.lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, causal, None)
+
+
+def test_fwd_validation(lib):
+    assert fwd(lib, B=-1) == lib.FA_ERR_INVALID_ARG
+    assert fwd(lib, N=-5) == lib.FA_ERR_INVALID_ARG
+    assert fwd(lib, d=96) == lib.FA_ERR_UNSUPPORTED
+    assert fwd(lib, d=256) == lib.FA_ERR_UNSUPPORTED
+    assert fwd(lib, scale=0.0) == lib.FA_ERR_INVALID_ARG
+    assert fwd(lib, scale=float("nan")) == lib.FA_ERR_INVALID_ARG
+    assert fwd(lib, scale=float("inf")) == lib.FA_ERR_INVALID_ARG
+    assert fwd(lib, q=0) == lib.FA_ERR_INVALID_ARG
+    assert fwd(lib, lse=0) == lib.FA_ERR_INVALID_ARG
+    assert fwd(lib, k=0x1008) == lib.FA_ERR_INVALID_ARG  # not 16-byte aligned
+    assert fwd(lib, lse=0x1002) == lib.FA_ERR_INVALID_ARG
+    assert fwd(lib, causal=2) == lib.FA_ERR_INVALID_ARG
+    # empty problems are a no-op even with null pointers
+    assert fwd(lib, q=0, k=0, v=0, o=0, lse=0, N=0) == lib.FA_OK
+    assert fwd(lib, q=0, k=0, v=0, o=0, lse=0, B=0) == lib.FA_OK
+
+
+def bwd(lib, ws=0x10000, ws_bytes=1 << 30, d=64, N=128, dq=0x1000, scale=0.125):
+    a = P(0x1000)
+    return lib.lib.fa_bwd(a, a, a, a, a, a, P(dq), a, a, 1, 1, N, d, scale, 0, P(ws), ws_bytes, None)
+
+
+def test_bwd_validation(lib):
+    need = lib.fa_bwd_workspace_bytes(1, 1, 128, 64)
+    assert bwd(lib, ws=0) == lib.FA_ERR_WORKSPACE
+    assert bwd(lib, ws_bytes=need - 1) == lib.FA_ERR_WORKSPACE
+    assert bwd(lib, ws=0x10010) == lib.FA_ERR_WORKSPACE  # not 256-byte aligned
+    assert bwd(lib, d=32) == lib.FA_ERR_UNSUPPORTED
+    assert bwd(lib, dq=0) == lib.FA_ERR_INVALID_ARG
+    assert bwd(lib, scale=-1.0) == lib.FA_ERR_INVALID_ARG
+    assert bwd(lib, N=0, dq=0, ws=0) == lib.FA_OK
+
+
+def test_diagnostics_validation(lib):
+    assert lib.lib.fa_exp2_poly_eval(P(0), P(0), -1, None) == lib.FA_ERR_INVALID_ARG
+    assert lib.lib.fa_exp2_poly_eval(P(0), P(0), 0, None) == lib.FA_OK
+    assert lib.lib.fa_debug_bounded_wait(10, None) == lib.FA_ERR_INVALID_ARG
+
+
+def test_binding_exposes_c_names(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
