@@ -329,11 +329,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (!valid(ch * 32 + e)) pv[e] = 0.0f;
         }
+        // The row sum takes the bf16-rounded P, the very weights the P V MMA
+        // uses: O is then an exact convex combination of V rows, and the
+        // rounding of a dominant weight (a stale reference max makes it
+        // anything in [1, 2^8]) cancels in O / l.
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          l += pv[2 * e] + pv[2 * e + 1];
           w[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+          l += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
         }
         tmem_st16(t_s + ch * 16, w);
       }
