@@ -1,12 +1,462 @@
-// Backward main kernel (key/value stationary), sm_103a.
+// Backward exact attention for sm_103a: key/value-stationary CTAs, all five
+// GEMMs of a tile on tcgen05 with their accumulators in tensor memory, dQ
+// accumulated with fp32 vector atomics.
+//
+// The pages single out the backward pass as limited by shared-memory traffic
+// and by its reductions and atomic updates ("Pourquoi l'approche standard ne
+// fonctionne plus" of the French page; "Режим 2-CTA MMA" of "FlashAttention-3
+// и FlashAttention-4"; FlashAttention-4 abstract item 3).  This kernel keeps
+// every intermediate it can in tensor memory so that shared memory carries
+// only operands:
+//
+//   tensor memory (512 columns x 128 lanes, lane = key row of the tile)
+//     [  0,128)  S^T = K Q_i^T (fp32) -> P^T (bf16) -> later dQ_i
+//     [128,256)  dP^T = V dO_i^T (fp32) -> dS^T (bf16)
+//     [256,256+d)      dV accumulator
+//     [256+d,256+2d)   dK accumulator
+//   Each compute warpgroup owns 64 query columns of S^T and dP^T and packs
+//   its bf16 P^T / dS^T into the first 32 of them, so neither warpgroup
+//   overwrites fp32 values the other has not read yet.
+//   (dQ_i = dS K has the query as its row, so it is the one product whose
+//    A operand must come from shared memory: at d = 128 dS is written over
+//    the dO_i tile once dV has consumed it; at d = 64 it has its own buffer.
+//    dQ_i lands in the S^T columns.)
+//
+// Per query tile i (MMA issue order):
+//   dP^T = V dO_i^T ; [dQ_{i-1} drained] S^T = K Q_i^T ;
+//   [P^T ready] dV += P^T dO_i ; [dS ready] dK += dS^T Q_i ; dQ_i = dS K
+// with P^T = exp2(S^T c - LSE_i log2 e) and dS = scale * P (dP - D_i): the
+// softmax scale is folded into dS, so dK and dQ come out scaled.
+//
+// Warp roles (448 threads):
+//   warps 0-7   compute: two warpgroups, thread = key row, warpgroup w takes
+//               query columns [64w, 64w + 64); at the end warpgroup 0 writes
+//               dV, warpgroup 1 dK
+//   warps 8-11  dQ drain: thread = query row, tensor memory -> fp32 atomics
+//   warp  12    loads: K, V once; Q_i, dO_i by TMA; LSE_i, D_i by plain loads
+//   warp  13    tensor-memory allocator; lane 0 issues every MMA
 #include "fa_device.cuh"
 #include "fa_kernels.h"
 
 namespace fa {
+namespace {
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kThreads = 448;
+  static constexpr int kDrainWarp0 = 8;
+  static constexpr int kProducerWarp = 12;
+  static constexpr int kMmaWarp = 13;
+  static constexpr int kTileBytes = kBlockM * D * 2;
+  static constexpr int kHalfBytes = kBlockM * 64 * 2;
+  static constexpr int kStages = 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQOff = 2 * kTileBytes;                     // kStages tiles
+  static constexpr int kDOOff = kQOff + kStages * kTileBytes;      // kStages tiles
+  static constexpr int kLseOff = kDOOff + kStages * kTileBytes;    // kStages x 128 fp32
+  static constexpr int kDsumOff = kLseOff + kStages * kBlockM * 4;  // kStages x 128 fp32
+  static constexpr int kDsTileBytes = kBlockN * kBlockM * 2;  // dS is 128 x 128 for any d
+  // At d = 128 the dS tile reuses the dO_i buffer; at d = 64 that buffer is
+  // too small and dS gets one buffer per stage.
+  static constexpr int kDsOff = kDsumOff + kStages * kBlockM * 4;
+  static constexpr int kDsBytes = (D == 128) ? 0 : kStages * kDsTileBytes;
+  static constexpr int kBarOff = kDsOff + kDsBytes;
+  static constexpr int kBarKV = 0;
+  static constexpr int kBarStFull = 1;
+  static constexpr int kBarStEmpty = kBarStFull + kStages;
+  static constexpr int kBarSFull = kBarStEmpty + kStages;
+  static constexpr int kBarDPFull = kBarSFull + 1;
+  static constexpr int kBarPFull = kBarDPFull + 1;
+  static constexpr int kBarDVDone = kBarPFull + 1;
+  static constexpr int kBarDSFull = kBarDVDone + 1;
+  static constexpr int kBarDQFull = kBarDSFull + 1;
+  static constexpr int kBarDQEmpty = kBarDQFull + 1;
+  static constexpr int kBarMmaDone = kBarDQEmpty + 1;
+  static constexpr int kNumBars = kBarMmaDone + 1;
+  static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
+  static constexpr int kAbortOff = kTmemSlotOff + 4;
+  static constexpr int kSmemBytes = kAbortOff + 4 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = 128;
+  static constexpr uint32_t kColDV = 256;
+  static constexpr uint32_t kColDK = 256 + D;
+  // Shared-memory offset of stage s's dS tile.
+  static __device__ __forceinline__ int ds_off(int s) {
+    return (D == 128) ? kDOOff + s * kTileBytes : kDsOff + s * kDsTileBytes;
+  }
+  // Tensor-memory column (relative to the S^T or dP^T region) of the packed
+  // bf16 pair for query columns 16*kk.. of the tile: warpgroup kk/4 owns
+  // columns [64*(kk/4), +64) and packs into the first 32.
+  static __device__ __forceinline__ uint32_t packed_col(int kk) {
+    return static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8);
+  }
+};
+
+enum : unsigned int {
+  kSiteKV = 0x201,
+  kSiteStFull = 0x202,
+  kSiteStEmpty = 0x203,
+  kSiteSFull = 0x204,
+  kSiteDPFull = 0x205,
+  kSitePFull = 0x206,
+  kSiteDVDone = 0x207,
+  kSiteDSFull = 0x208,
+  kSiteDQFull = 0x209,
+  kSiteDQEmpty = 0x20A,
+  kSiteMmaDone = 0x20B,
+};
+
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
+  float* lse_s = reinterpret_cast<float*>(smem + C::kLseOff);
+  float* dsum_s = reinterpret_cast<float*>(smem + C::kDsumOff);
+  const WaitCtl ctl{abort_flag, p.status};
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  // Work item: key tile j of head bh; causal tiles with small j see the most
+  // query tiles, so they go first.
+  const int blk = blockIdx.x;
+  const int kt = blk / p.BH;
+  const int bh = blk % p.BH;
+  const int k0 = kt * kBlockN;
+  const int n_qtiles = (p.N + kBlockM - 1) / kBlockM;
+  const int i_first = p.causal ? kt : 0;
+  const int n_iter = n_qtiles - i_first;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(C::kBarKV), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarStFull + s), 2);
+      mbar_init(bar(C::kBarStEmpty + s), 1);
+    }
+    mbar_init(bar(C::kBarSFull), 1);
+    mbar_init(bar(C::kBarDPFull), 1);
+    mbar_init(bar(C::kBarPFull), 2 * kBlockM);
+    mbar_init(bar(C::kBarDVDone), 1);
+    mbar_init(bar(C::kBarDSFull), 2 * kBlockM);
+    mbar_init(bar(C::kBarDQFull), 1);
+    mbar_init(bar(C::kBarDQEmpty), kBlockM);
+    mbar_init(bar(C::kBarMmaDone), 1);
+    fence_mbar_init();
+  }
+  if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == C::kProducerWarp) {
+    // ------------------------------------------------------------- loads
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      tma_prefetch_desc(&p.tm_do);
+      mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTileBytes);
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_3d(sbase + C::kKOff + h * C::kHalfBytes, &p.tm_k, bar(C::kBarKV), h * 64, k0, bh);
+        tma_load_3d(sbase + C::kVOff + h * C::kHalfBytes, &p.tm_v, bar(C::kBarKV), h * 64, k0, bh);
+      }
+    }
+    int issued = 0;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % C::kStages;
+      const int use = it / C::kStages;
+      if (use > 0) {
+        bool ok = mbar_wait(bar(C::kBarStEmpty + s), (use - 1) & 1, ctl, kSiteStEmpty);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      const int q0 = (i_first + it) * kBlockM;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(C::kBarStFull + s), 2 * C::kTileBytes);
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_3d(sbase + C::kQOff + s * C::kTileBytes + h * C::kHalfBytes, &p.tm_q,
+                      bar(C::kBarStFull + s), h * 64, q0, bh);
+          tma_load_3d(sbase + C::kDOOff + s * C::kTileBytes + h * C::kHalfBytes, &p.tm_do,
+                      bar(C::kBarStFull + s), h * 64, q0, bh);
+        }
+      }
+      // LSE in log2 units and D for the 128 rows; rows past N get LSE = +inf
+      // (so P = 0) and D = 0.
+#pragma unroll
+      for (int r4 = 0; r4 < 4; ++r4) {
+        const int r = lane * 4 + r4;
+        const int q = q0 + r;
+        const size_t gi = static_cast<size_t>(bh) * p.N + q;
+        lse_s[s * kBlockM + r] = (q < p.N) ? p.lse[gi] * p.log2e : INFINITY;
+        dsum_s[s * kBlockM + r] = (q < p.N) ? p.dsum[gi] : 0.0f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kBarStFull + s));
+      issued = it + 1;
+    }
+    if (lane == 0) {
+      mbar_wait_drain(bar(C::kBarKV), 0);
+      for (int it = max(0, issued - C::kStages); it < issued; ++it)
+        mbar_wait_drain(bar(C::kBarStFull + it % C::kStages), (it / C::kStages) & 1);
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t kIdescSq = idesc_bf16_f32(kBlockN, kBlockM, false, false);  // S^T, dP^T
+      constexpr uint32_t kIdescKV = idesc_bf16_f32(kBlockN, D, false, true);          // dV, dK
+      constexpr uint32_t kIdescQ = idesc_bf16_f32(kBlockM, D, true, true);            // dQ
+      const uint32_t k_smem = sbase + C::kKOff;
+      const uint32_t v_smem = sbase + C::kVOff;
+      // X^T = A B^T with A = K or V (key rows, K-major over d) and
+      // B = Q_i or dO_i (query rows, K-major over d): M = keys, N = queries.
+      auto issue_nt = [&](uint32_t a0, uint32_t b0, uint32_t dcol) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+          mma_ss(tmem_base + dcol, sdesc_sw128(a0 + off, 16, 1024),
+                 sdesc_sw128(b0 + off, 16, 1024), kIdescSq, kk > 0 ? 1u : 0u);
+        }
+      };
+      // acc += X^T Y with X^T (keys x queries, bf16) in tensor memory and Y =
+      // dO_i or Q_i in shared memory as an MN-major B (d contiguous).
+      auto issue_tn = [&](uint32_t acol, uint32_t b0, uint32_t dcol, bool accumulate) {
+#pragma unroll
+        for (int kk = 0; kk < kBlockM / 16; ++kk)
+          mma_ts(tmem_base + dcol, tmem_base + acol + C::packed_col(kk),
+                 sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024), kIdescKV,
+                 (accumulate || kk > 0) ? 1u : 0u);
+      };
+      // dQ_i = dS K: A = dS (queries x keys) MN-major in the dO_i buffer
+      // (64-query blocks 16 KB apart, 8-key groups 1024 B apart); B = K as an
+      // MN-major operand (d contiguous).
+      auto issue_dq = [&](uint32_t ds0) {
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ss(tmem_base + C::kColS, sdesc_sw128(ds0 + kk * 2048, kBlockN * 128, 1024),
+                 sdesc_sw128(k_smem + kk * 2048, C::kHalfBytes, 1024), kIdescQ, kk > 0 ? 1u : 0u);
+      };
+
+      bool ok = mbar_wait(bar(C::kBarKV), 0, ctl, kSiteKV);
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int s = it % C::kStages;
+        const uint32_t q_s = sbase + C::kQOff + s * C::kTileBytes;
+        const uint32_t do_s = sbase + C::kDOOff + s * C::kTileBytes;
+        if (!(ok = mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull))) break;
+        tc_fence_after();
+        issue_nt(v_smem, do_s, C::kColDP);
+        mma_commit(bar(C::kBarDPFull));
+        if (it > 0) {
+          if (!(ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl, kSiteDQEmpty))) break;
+          tc_fence_after();
+        }
+        issue_nt(k_smem, q_s, C::kColS);
+        mma_commit(bar(C::kBarSFull));
+        if (!(ok = mbar_wait(bar(C::kBarPFull), it & 1, ctl, kSitePFull))) break;
+        tc_fence_after();
+        issue_tn(C::kColS, do_s, C::kColDV, it > 0);
+        mma_commit(bar(C::kBarDVDone));
+        if (!(ok = mbar_wait(bar(C::kBarDSFull), it & 1, ctl, kSiteDSFull))) break;
+        tc_fence_after();
+        issue_tn(C::kColDP, q_s, C::kColDK, it > 0);
+        issue_dq(sbase + C::ds_off(s));
+        mma_commit(bar(C::kBarDQFull));
+        mma_commit(bar(C::kBarStEmpty + s));
+      }
+      mma_commit(bar(C::kBarMmaDone));
+      if (!ok) mbar_wait_drain(bar(C::kBarMmaDone), 0);
+    }
+  } else if (warp >= C::kDrainWarp0) {
+    // ------------------------------------------------------------- dQ drain
+    const int quarter = warp & 3;
+    const int qr = quarter * 32 + lane;
+    const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColS;
+    for (int it = 0; it < n_iter; ++it) {
+      bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int q = (i_first + it) * kBlockM + qr;
+      float4* dst = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.N + q) * D);
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(t_dq + ch * 32, r);
+        tmem_ld_wait(r);
+        if (q < p.N) {
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            atomicAdd(dst + ch * 8 + v4,
+                      make_float4(__uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
+                                  __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarDQEmpty));
+    }
+  } else {
+    // ------------------------------------------------------------- compute
+    const int wg = warp >> 2;  // query-column half
+    const int quarter = warp & 3;
+    const int kr = quarter * 32 + lane;  // key row within the tile
+    const int kpos = k0 + kr;
+    const bool row_valid = kpos < p.N;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c = p.c;
+    const float scale = p.scale;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % C::kStages;
+      const int i = i_first + it;
+      const bool diag = p.causal && i == kt;
+      ok = mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull);
+      ok = ok && mbar_wait(bar(C::kBarSFull), it & 1, ctl, kSiteSFull);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const float* lse2 = lse_s + s * kBlockM;
+      const float* dsm = dsum_s + s * kBlockM;
+
+      // P^T = exp2(S^T c - LSE log2 e); masked entries (query < key on the
+      // diagonal tile, keys past N) are 0.
+      float pf[64];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int col0 = wg * 64 + ch * 32;
+        uint32_t r[32];
+        tmem_ld32(lane_base + C::kColS + col0, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + col0 + 4 * e4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = col0 + 4 * e4 + e;
+            float pv = ex2_mufu(fmaf(__uint_as_float(r[4 * e4 + e]), c, -lv[e]));
+            if (!row_valid || (diag && col < kr)) pv = 0.0f;
+            pf[ch * 32 + 4 * e4 + e] = pv;
+          }
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]);
+        tmem_st16(lane_base + C::kColS + wg * 64 + ch * 16, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPFull));
+
+      // dS = scale * P (dP - D): to tensor memory (for dK) and, once dV has
+      // finished reading dO_i, into the dO_i buffer (for dQ).
+      ok = mbar_wait(bar(C::kBarDPFull), it & 1, ctl, kSiteDPFull);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t dsw[32];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int col0 = wg * 64 + ch * 32;
+        uint32_t r[32];
+        tmem_ld32(lane_base + C::kColDP + col0, r);
+        tmem_ld_wait(r);
+        float dsv[32];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(dsm + col0 + 4 * e4);
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dsv[4 * e4 + e] =
+                scale * pf[ch * 32 + 4 * e4 + e] * (__uint_as_float(r[4 * e4 + e]) - dv[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dsw[ch * 16 + e] = pack_bf16x2(dsv[2 * e], dsv[2 * e + 1]);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = dsw[ch * 16 + e];
+        tmem_st16(lane_base + C::kColDP + wg * 64 + ch * 16, w);
+      }
+      ok = mbar_wait(bar(C::kBarDVDone), it & 1, ctl, kSiteDVDone);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      // dS tile laid out as an MN-major operand with 128B swizzle:
+      // [query half][key row][64 queries], 16-byte chunk index XOR (key row
+      // mod 8).
+      uint8_t* ds_tile = smem + C::ds_off(s);
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        const int q = wg * 64 + c8 * 8;  // first query of this 16-byte chunk
+        const int half = q >> 6;
+        const int chunk = (q & 63) >> 3;
+        uint4* dst = reinterpret_cast<uint4*>(ds_tile + half * (kBlockN * 128) + kr * 128 +
+                                              ((chunk ^ (kr & 7)) << 4));
+        *dst = make_uint4(dsw[4 * c8], dsw[4 * c8 + 1], dsw[4 * c8 + 2], dsw[4 * c8 + 3]);
+      }
+      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarDSFull));
+    }
+
+    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (already scaled)
+    if (ok) {
+      ok = mbar_wait(bar(C::kBarMmaDone), 0, ctl, kSiteMmaDone);
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(wg == 0 ? p.dv : p.dk) +
+                             (static_cast<size_t>(bh) * p.N + kpos) * D;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + col + ch * 32, r);
+          tmem_ld_wait(r);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * v4]), __uint_as_float(r[8 * v4 + 1])),
+                                   pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3])),
+                                   pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5])),
+                                   pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7])));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  cudaError_t err = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const long long blocks = static_cast<long long>(p.n_kblk) * p.BH;
+  fa_bwd_kernel<D><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream) {
-  (void)p; (void)d; (void)stream;
-  return cudaErrorNotSupported;
+  if (d == 128) return launch_bwd_d<128>(p, stream);
+  if (d == 64) return launch_bwd_d<64>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

@@ -91,3 +91,47 @@ def compare_fwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_
             worst_o = max(worst_o, check_o(o[b, h][sel], o_ref, what))
             worst_l = max(worst_l, check_lse(lse[b, h][sel], l_ref, what))
     return worst_o, worst_l
+
+
+def run_bwd(B, H, N, d, causal, seed=0, stress=False, scale=None):
+    """GPU forward then backward; O and LSE come from this library's forward."""
+    from exact_attention_98_gb300 import fa
+
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    q, k, v, do = attention_inputs(B, H, N, d, seed=seed, stress=stress)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    status = fa.fa_last_device_status()
+    assert status == fa.FA_OK, fa.status_string(status)
+    return (q, k, v, do), (to64(dq), to64(dk), to64(dv)), scale
+
+
+def compare_bwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_per_head=None,
+                kv_heads=()):
+    """Backward parity.  Heads with index < full_heads (None = all) compare
+    every row of dQ, dK, dV; other heads compare sampled dQ rows, and the
+    heads listed in kv_heads also sampled dK/dV rows."""
+    inputs, grads, scale = run_bwd(B, H, N, d, causal, seed, stress)
+    q64, k64, v64, do64 = (t.double().numpy() for t in inputs)
+    dq, dk, dv = grads
+    worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
+    for b in range(B):
+        for h in range(H):
+            idx = b * H + h
+            what = f"B{B} H{H} N{N} d{d} causal={causal} stress={stress} head ({b},{h})"
+            if full_heads is None or idx < full_heads:
+                qrows = krows = None
+            else:
+                qrows = sampled_rows(N, rows_per_head, b, h, H)
+                krows = qrows if idx in kv_heads else []
+            r = oracle.bwd_head(q64[b, h], k64[b, h], v64[b, h], do64[b, h], scale, causal,
+                                qrows=qrows, krows=krows)
+            qs = slice(None) if qrows is None else qrows
+            worst["dq"] = max(worst["dq"], check_grad(dq[b, h][qs], r[0], what + " dQ"))
+            if krows is None or len(krows):
+                ks = slice(None) if krows is None else krows
+                worst["dk"] = max(worst["dk"], check_grad(dk[b, h][ks], r[1], what + " dK"))
+                worst["dv"] = max(worst["dv"], check_grad(dv[b, h][ks], r[2], what + " dV"))
+    return worst, grads, inputs
