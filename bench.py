@@ -1,0 +1,379 @@
+"""Benchmark of the exact-attention hot path: one step = forward + backward
+over one batch of synthetic bf16 inputs, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Default workload: B=2, H=16, N=4096, d=128, bf16, non-causal, scale 1/sqrt(d)
+(the B2 H16 N4096 d128 configuration; the causal variant is reported as an
+extra).  Algorithmic FLOPs: forward 4*B*H*N^2*d (halved when causal),
+backward 2.5x that.
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its
+own replica on its own GPU (independent batches, no collective on the data
+path: weak scaling); the step time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, each step
+a bounded sample of the same workload (forward and backward rows of one head).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PAGES_PEAK_TFLOPS = 2250.0  # dense BF16 peak the pages quote for the GPU generation
+METRIC = "attention fwd/bwd TFLOPs/s (bf16, d=128) and % of 2.25 PF dense BF16 peak"
+WORKLOAD = dict(B=2, H=16, N=4096, d=128)
+
+
+def flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    if causal:
+        f *= 0.5
+    return f, 2.5 * f
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (for profiler runs)")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+
+def oracle_sample(seconds_target: float, steps: int = 1):
+    """Times the fp64 oracle on a bounded sample of the workload: forward and
+    dQ/dK/dV-backward of R query rows of head 0 (R sized so one sample takes
+    about `seconds_target`).  Returns (TFLOP/s, threads, description)."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    B, H, N, d = WORKLOAD["B"], WORKLOAD["H"], WORKLOAD["N"], WORKLOAD["d"]
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = attention_inputs(1, 1, N, d, seed=0)
+    q, k, v, do = (t.double().numpy()[0, 0] for t in (q, k, v, do))
+
+    def run(rows):
+        oracle.fwd_head(q, k, v, scale, False, rows=rows)
+        oracle.bwd_head(q, k, v, do, scale, False, qrows=rows, krows=[])
+        return len(rows)
+
+    # warm up, calibrate on a few rows, then size the sample
+    run(list(range(4)))
+    t0 = time.perf_counter()
+    run(list(range(32)))
+    per_row = (time.perf_counter() - t0) / 32
+    R = int(max(16, min(N, seconds_target / max(per_row, 1e-9))))
+    rows = list(range(R))
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        run(rows)
+        times.append(time.perf_counter() - t0)
+    # algorithmic FLOPs of the sample, same convention as the GPU figure:
+    # forward 4*R*N*d; of the backward only the dQ rows are computed, whose
+    # share is S, dP and dS K for those rows: 6*R*N*d
+    f = 10.0 * R * N * d
+    tf = f / statistics.median(times) / 1e12
+    desc = (f"forward + dQ rows of the backward for {R} of {N} query rows of one head "
+            f"(B2 H16 N{N} d{d} non-causal workload), fp64, {oracle.num_threads()} threads")
+    return tf, oracle.num_threads(), desc, times, f
+
+
+def reference_arm(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    per_step = 4.0  # seconds of oracle work per step
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state; calibration runs inside oracle_sample
+    tf, threads, desc, times, f = oracle_sample(per_step, steps=args.steps)
+    ms = statistics.median(times) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "attention fwd+bwd B2 H16 N4096 d128 non-causal bf16 inputs",
+                   "sample": desc},
+        "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def native_arm(args):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    from exact_attention_98_gb300 import fa
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    B, H, N, d = WORKLOAD["B"], WORKLOAD["H"], WORKLOAD["N"], WORKLOAD["d"]
+    scale = 1.0 / math.sqrt(d)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+            torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    # each rank: its own replica batch (different seed per rank)
+    q, k, v, do = attention_inputs(B, H, N, d, seed=rank)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
+    ws = fa.workspace_for(qd)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    stream = torch.cuda.current_stream()
+
+    def step(causal):
+        fa.fa_fwd(qd, kd, vd, o, lse, scale, causal)
+        fa.fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, scale, causal, ws)
+
+    def timed(causal, steps, warmup, kernel_times=False):
+        for _ in range(warmup):
+            step(causal)
+        if fa.fa_last_device_status() != fa.FA_OK:
+            raise RuntimeError("device status after warm-up")
+        fa.fa_timing_enable(kernel_times)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        fwd_ms, bwd_ms = [], []
+        barrier()
+        wall0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()  # L2 flush between steps, outside the step's events
+            starts[i].record(stream)
+            step(causal)
+            ends[i].record(stream)
+            if kernel_times:
+                fwd_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
+                bwd_ms.append(fa.fa_timing_last_ms(fa.KERNEL_BWD_MAIN))
+        barrier()
+        wall = time.perf_counter() - wall0
+        fa.fa_timing_enable(False)
+        status = fa.fa_last_device_status()
+        if status != fa.FA_OK:
+            raise RuntimeError(f"device status {fa.status_string(status)}")
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return step_ms, fwd_ms, bwd_ms, wall
+
+    # headline: non-causal, with per-kernel events and clocks sampled meanwhile
+    with ClockSampler(local) as clocks:
+        step_ms, fwd_ms, bwd_ms, wall = timed(False, args.steps, args.warmup, kernel_times=True)
+    clk = clocks.summary()
+    mean_ms = max_over_ranks(statistics.mean(step_ms))
+    f_fwd, f_bwd = flops(B, H, N, d, False)
+    value = world * (f_fwd + f_bwd) / (mean_ms * 1e-3) / 1e12
+    fwd_med, bwd_med = statistics.median(fwd_ms), statistics.median(bwd_ms)
+    fwd_tf = f_fwd / (fwd_med * 1e-3) / 1e12
+    bwd_main_tf = f_bwd / (bwd_med * 1e-3) / 1e12
+
+    # causal variant (extra)
+    c_ms, c_fwd, c_bwd, _ = timed(True, max(3, args.steps // 2), 2, kernel_times=True)
+    cf_fwd, cf_bwd = flops(B, H, N, d, True)
+    causal_extra = {
+        "step_tflops": (cf_fwd + cf_bwd) / (statistics.mean(c_ms) * 1e-3) / 1e12,
+        "fwd_tflops": cf_fwd / (statistics.median(c_fwd) * 1e-3) / 1e12,
+        "bwd_main_tflops": cf_bwd / (statistics.median(c_bwd) * 1e-3) / 1e12,
+    }
+
+    # end to end through the public API with pinned host buffers: H2D of
+    # q, k, v, dO, forward, backward, D2H of dQ, dK, dV every step
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (q, q, q))
+    e2e_steps = max(3, args.steps // 2)
+
+    def e2e_step():
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        dod.copy_(hdo, non_blocking=True)
+        step(False)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
+    e2e_value = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+    tensor_bytes = q.numel() * q.element_size()
+
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    peak = peaks.get("bf16_tflops")
+    peak_note = "measured burst cuBLAS bf16 (MEASURED_PEAKS.json bf16_tflops)"
+    if peak is None:
+        peak, peak_note = 1900.0, "fallback 1.9 PFLOP/s bf16"
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": mean_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "attention fwd+bwd B2 H16 N4096 d128 non-causal", "B": B, "H": H,
+                   "N": N, "d": d, "causal": False, "global_batch": B * world, "seq_len": N,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between steps (256 MiB write outside the step events)"},
+        "pct_of_2250_tflops": 100.0 * value / PAGES_PEAK_TFLOPS,
+        "fwd_tflops": fwd_tf,
+        "bwd_main_tflops": bwd_main_tf,
+        "fwd_ms": fwd_med,
+        "bwd_main_ms": bwd_med,
+        "causal": causal_extra,
+        "roofline": {
+            "kernel": "fa_bwd_kernel<128>",
+            "bound": "tensor",
+            "achieved": bwd_main_tf,
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": bwd_main_tf / peak,
+            "peak_source": peak_note,
+            "traffic": None,
+        },
+        "roofline_fwd": {"kernel": "fa_fwd_kernel<128>", "bound": "tensor", "achieved": fwd_tf,
+                         "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": 4 * tensor_bytes, "d2h_bytes_per_step": 3 * tensor_bytes},
+        "gpu_launches": 4 * args.steps,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, threads, desc, _, _ = oracle_sample(12.0, steps=1)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        native_arm(args)
+
+
+if __name__ == "__main__":
+    main()

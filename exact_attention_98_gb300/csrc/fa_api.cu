@@ -18,6 +18,34 @@ namespace {
 
 int g_last_site = 0;
 
+// Optional event pairs around the main kernels (kernel 0 = forward, 1 =
+// backward main), recorded on the launch stream when timing is enabled.
+struct KernelTiming {
+  std::mutex mu;
+  bool enabled = false;
+  cudaEvent_t start[2] = {nullptr, nullptr};
+  cudaEvent_t stop[2] = {nullptr, nullptr};
+  bool recorded[2] = {false, false};
+};
+KernelTiming g_timing;
+
+bool timing_on() {
+  std::lock_guard<std::mutex> lock(g_timing.mu);
+  return g_timing.enabled;
+}
+
+cudaError_t timing_record(int kernel, bool at_start, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_timing.mu);
+  if (!g_timing.enabled) return cudaSuccess;
+  cudaEvent_t& ev = at_start ? g_timing.start[kernel] : g_timing.stop[kernel];
+  if (!ev) {
+    cudaError_t e = cudaEventCreate(&ev);
+    if (e != cudaSuccess) return e;
+  }
+  if (!at_start) g_timing.recorded[kernel] = true;
+  return cudaEventRecord(ev, s);
+}
+
 // Device address of g_status_word for the current device, looked up once per
 // device with that device current.
 unsigned int* status_ptr() {
@@ -160,7 +188,11 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.c = scale * 1.4426950408889634f;
   p.ln2 = 0.6931471805599453f;
   if (static_cast<long long>(p.n_qblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  return launch_fwd(p, d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (timing_record(0, true, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_fwd(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (timing_record(0, false, s) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
@@ -213,7 +245,9 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (static_cast<long long>(p.n_kblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
 
   if (launch_bwd_pre(o, dout, dsum, dq_acc, rows, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (timing_record(1, true, s) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_bwd_main(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_bwd_post(dq_acc, dq, rows * d, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -230,6 +264,25 @@ int fa_last_device_status(void* stream) {
 }
 
 int fa_last_device_site(void) { return g_last_site; }
+
+int fa_timing_enable(int enable) {
+  std::lock_guard<std::mutex> lock(g_timing.mu);
+  g_timing.enabled = enable != 0;
+  return FA_OK;
+}
+
+int fa_timing_last_ms(int kernel, float* ms) {
+  if (kernel < 0 || kernel > 1 || !ms) return FA_ERR_INVALID_ARG;
+  cudaEvent_t start, stop;
+  {
+    std::lock_guard<std::mutex> lock(g_timing.mu);
+    if (!g_timing.recorded[kernel]) return FA_ERR_INVALID_ARG;
+    start = g_timing.start[kernel];
+    stop = g_timing.stop[kernel];
+  }
+  if (cudaEventSynchronize(stop) != cudaSuccess) return FA_ERR_CUDA;
+  return cudaEventElapsedTime(ms, start, stop) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 int fa_exp2_poly_eval(const float* x, float* y, long long n, void* stream) {
   if (n < 0) return FA_ERR_INVALID_ARG;

@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const bool ragged = (p.N % kBlockN) != 0;
 
     float m_used = -INFINITY;  // running row max in log2 units (scores * c)
-    float l = 0.0f;            // running row sum of exp2(x - m_used)
+    float l = 0.0f;            // row sum of exp2(x - m_used), unrounded: gives LSE
+    float l_bf = 0.0f;         // row sum of the bf16-rounded P: normalises O
     bool ok = true;
     for (int j = 0; j < nkv[t]; ++j) {
       ok = mbar_wait(bar(C::kBarSFull + t), j & 1, ctl, kSiteSFull);
@@ -307,6 +308,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         if (need) {
           l *= alpha;
+          l_bf *= alpha;
           m_used = m_new;
         }
       }
@@ -329,15 +331,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (!valid(ch * 32 + e)) pv[e] = 0.0f;
         }
-        // The row sum takes the bf16-rounded P, the very weights the P V MMA
-        // uses: O is then an exact convex combination of V rows, and the
-        // rounding of a dominant weight (a stale reference max makes it
-        // anything in [1, 2^8]) cancels in O / l.
+        // O is normalised by the sum of the bf16-rounded P, the very weights
+        // the P V MMA uses: O is then an exact convex combination of V rows,
+        // and the rounding of a dominant weight (a stale reference max makes
+        // it anything in [1, 2^8]) cancels in O / l_bf.  LSE keeps the
+        // unrounded sum.
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           w[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-          l += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
+          l += pv[2 * e] + pv[2 * e + 1];
+          l_bf += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
         }
         tmem_st16(t_s + ch * 16, w);
       }
@@ -346,13 +350,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_arrive(bar(C::kBarPFull + t));
     }
 
-    // epilogue: O / l -> bf16, LSE = ln(2) * m_used + ln(l)
+    // epilogue: O / l_bf -> bf16, LSE = ln(2) * m_used + ln(l)
     if (ok && nkv[t] > 0) {
       ok = mbar_wait(bar(C::kBarOFull + t), 0, ctl, kSiteOFull);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        const float inv_l = 1.0f / l;
+        const float inv_l = 1.0f / l_bf;
         const bool in_range = qpos < p.N;
         __nv_bfloat16* orow =
             static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;

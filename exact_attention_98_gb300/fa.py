@@ -59,6 +59,10 @@ def _load() -> ctypes.CDLL:
     lib.fa_exp2_poly_eval.restype = i
     lib.fa_debug_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
     lib.fa_debug_bounded_wait.restype = i
+    lib.fa_timing_enable.argtypes = [i]
+    lib.fa_timing_enable.restype = i
+    lib.fa_timing_last_ms.argtypes = [i, ctypes.POINTER(ctypes.c_float)]
+    lib.fa_timing_last_ms.restype = i
     return lib
 
 
@@ -157,6 +161,20 @@ def fa_exp2_poly_eval(x, y, stream=None) -> None:
 
 def fa_debug_bounded_wait(limit_ns: int, stream=None) -> None:
     _check(lib.fa_debug_bounded_wait(int(limit_ns), _stream(stream)), "fa_debug_bounded_wait")
+
+
+KERNEL_FWD = 0
+KERNEL_BWD_MAIN = 1
+
+
+def fa_timing_enable(enable: bool) -> None:
+    _check(lib.fa_timing_enable(int(bool(enable))), "fa_timing_enable")
+
+
+def fa_timing_last_ms(kernel: int) -> float:
+    ms = ctypes.c_float(0.0)
+    _check(lib.fa_timing_last_ms(int(kernel), ctypes.byref(ms)), "fa_timing_last_ms")
+    return float(ms.value)
 
 
 # --- conveniences ----------------------------------------------------------------

@@ -121,6 +121,19 @@ int fa_exp2_poly_eval(const float* x, float* y, long long n, void* stream);
  */
 int fa_debug_bounded_wait(unsigned long long limit_ns, void* stream);
 
+/*
+ * Timing of the main kernels.  fa_timing_enable(1) makes every later fa_fwd /
+ * fa_bwd record a pair of CUDA events on its stream around its main kernel
+ * (the forward kernel; the backward main kernel, between the pre- and
+ * post-processing kernels); fa_timing_enable(0) stops it.  The events belong
+ * to the library (created on first use on the current device).
+ * fa_timing_last_ms(kernel, &ms) waits for the last recorded pair of that
+ * kernel (0 = forward, 1 = backward main) and returns its elapsed time in
+ * milliseconds; FA_ERR_INVALID_ARG if none was recorded.
+ */
+int fa_timing_enable(int enable);
+int fa_timing_last_ms(int kernel, float* ms);
+
 #ifdef __cplusplus
 }
 #endif
