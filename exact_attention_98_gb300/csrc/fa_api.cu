@@ -143,6 +143,28 @@ __global__ void bounded_wait_kernel(unsigned int* status, unsigned long long lim
   __syncthreads();
 }
 
+// Scratch of fa_bwd_noalloc: the backward's D and dQ accumulator for callers
+// that cannot allocate.  Fixed size, one per device, shared by every call.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch for the current device.  Host code may
+// not pass the array's name to a kernel (on the host it names a host-side
+// stand-in), so the address is looked up once per device, with that device
+// current, and cached.
+void* noalloc_scratch_ptr() {
+  static std::mutex mu;
+  static void* ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -158,6 +180,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
     case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_TOO_LARGE: return "FA_ERR_TOO_LARGE";
     default: return "FA_ERR_UNKNOWN";
   }
 }
@@ -250,6 +273,22 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_bwd_post(dq_acc, dq, rows * d, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
+}
+
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   float scale, int causal, void* stream) {
+  bool empty = false;
+  int rc = check_shape(B, H, N, d, scale, &empty);
+  if (rc != FA_OK || empty) return rc;
+  if (fa_bwd_workspace_bytes(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_TOO_LARGE;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  void* scratch = noalloc_scratch_ptr();
+  if (!scratch) return FA_ERR_CUDA;
+  // fa_bwd's first kernel zeroes the dQ accumulator and overwrites D, so the
+  // previous call's contents of the scratch do not matter.
+  return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, scratch,
+                FA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 int fa_last_device_status(void* stream) {

@@ -28,6 +28,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_WORKSPACE = 5
+FA_ERR_TOO_LARGE = 6
 
 
 class FAError(RuntimeError):
@@ -59,6 +60,8 @@ def _load() -> ctypes.CDLL:
     lib.fa_exp2_poly_eval.restype = i
     lib.fa_debug_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
     lib.fa_debug_bounded_wait.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_bwd_noalloc.restype = i
     lib.fa_timing_enable.argtypes = [i]
     lib.fa_timing_enable.restype = i
     lib.fa_timing_last_ms.argtypes = [i, ctypes.POINTER(ctypes.c_float)]
@@ -138,6 +141,20 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool, worksp
     _check(lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                       _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                       _ptr(workspace), ws_bytes, _stream(stream)), "fa_bwd")
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool,
+                   stream=None) -> None:
+    """fa_bwd with the library's fixed scratch array instead of a caller
+    workspace: for callers that cannot allocate device memory."""
+    B, H, N, d = _shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
+    _check_tensor(lse, "lse", torch.float32, (B, H, N))
+    _check(lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                              _stream(stream)), "fa_bwd_noalloc")
 
 
 def fa_last_device_status(stream=None) -> int:

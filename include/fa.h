@@ -42,7 +42,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2, /* a shape the kernels do not handle (d not 64/128)  */
   FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a launch failed      */
   FA_ERR_TIMEOUT = 4,     /* a kernel's bounded wait expired (device status)    */
-  FA_ERR_WORKSPACE = 5    /* the backward workspace is missing or too small     */
+  FA_ERR_WORKSPACE = 5,   /* the backward workspace is missing or too small     */
+  FA_ERR_TOO_LARGE = 6    /* problem exceeds fa_bwd_noalloc's fixed scratch      */
 } fa_status;
 
 /*
@@ -88,6 +89,32 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
            float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward without any allocation, for callers that cannot allocate device
+ * memory: plugin hosts that hand a library its input and output buffers but
+ * no allocator and no workspace, and latency-critical loops where a
+ * cudaMalloc/cudaFree would synchronise the device.  The pages describe no
+ * such entry point; it has no counterpart there.
+ *
+ * Same arguments and results as fa_bwd, minus the workspace: the scratch
+ * (D and the fp32 dQ accumulator) lives in one fixed array of
+ * FA_NOALLOC_SCRATCH_BYTES (96 MiB) of device memory inside the library,
+ * which every GPU that loads the library keeps until the process exits.
+ * Problems whose fa_bwd_workspace_bytes() exceeds it (at d = 128 roughly
+ * B*H*N > 195,000 rows, at d = 64 > 380,000) return FA_ERR_TOO_LARGE.
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.  Its first call on a device looks up that device's address of the
+ * array (with that device current); make that first call before any stream
+ * capture.  The array keeps the last call's contents; the call itself
+ * zeroes the part that must start at zero.  All calls share the one array,
+ * so calls that overlap on the GPU (on different streams, or from several
+ * threads) race and give wrong results: serialise them.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (96ull << 20)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   float scale, int causal, void* stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word:
