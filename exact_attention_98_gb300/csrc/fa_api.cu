@@ -2,6 +2,7 @@
 // the device status word, and two small diagnostic kernels.  The operations
 // and their argument conventions are documented in include/fa.h.
 #include <math.h>
+#include <stdlib.h>
 #include <mutex>
 #include <stdint.h>
 
@@ -95,6 +96,35 @@ bool encode_tile_map(CUtensorMap* map, const void* base, int N, int BH, int d) {
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Share of the forward's exponentials on the FMA pipe, per 8 (env override).
+int poly_per_octet() {
+  static std::once_flag once;
+  static int value = kDefaultPolyPerOctet;
+  std::call_once(once, [] {
+    const char* e = getenv("FA_FWD_POLY_PER_OCTET");
+    if (e && e[0] >= '0' && e[0] <= '3' && e[1] == '\0') value = e[0] - '0';
+  });
+  return value;
+}
+
+// fp32 dQ accumulator [BH, N, d] viewed as (d, N, BH); box 16 columns (64
+// bytes) x 128 rows x 1 head with 64-byte swizzle, for bulk reduce-adds.
+// Rows past N are dropped by the TMA unit.
+bool encode_dq_map(CUtensorMap* map, const float* base, int N, int BH, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 4};
+  const cuuint32_t box[3] = {16, 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+            elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -210,6 +240,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.causal = causal;
   p.c = scale * 1.4426950408889634f;
   p.ln2 = 0.6931471805599453f;
+  p.poly_per_octet = poly_per_octet();
   if (static_cast<long long>(p.n_qblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (timing_record(0, true, s) != cudaSuccess) return FA_ERR_CUDA;
@@ -249,7 +280,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
 
   BwdParams p;
   if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
-      !encode_tile_map(&p.tm_v, v, N, BH, d) || !encode_tile_map(&p.tm_do, dout, N, BH, d))
+      !encode_tile_map(&p.tm_v, v, N, BH, d) || !encode_tile_map(&p.tm_do, dout, N, BH, d) ||
+      !encode_dq_map(&p.tm_dq, dq_acc, N, BH, d))
     return FA_ERR_CUDA;
   p.lse = lse;
   p.dsum = dsum;

@@ -1,40 +1,46 @@
 // Backward exact attention for sm_103a: key/value-stationary CTAs, all five
 // GEMMs of a tile on tcgen05 with their accumulators in tensor memory, dQ
-// accumulated with fp32 vector atomics.
+// added into an fp32 accumulator by bulk TMA reductions.
 //
 // The pages single out the backward pass as limited by shared-memory traffic
 // and by its reductions and atomic updates ("Pourquoi l'approche standard ne
 // fonctionne plus" of the French page; "Режим 2-CTA MMA" of "FlashAttention-3
 // и FlashAttention-4"; FlashAttention-4 abstract item 3).  This kernel keeps
 // every intermediate it can in tensor memory so that shared memory carries
-// only operands:
+// only operands, and adds dQ tile by tile with bulk reductions instead of one
+// atomic per element:
 //
-//   tensor memory (512 columns x 128 lanes, lane = key row of the tile)
-//     [  0,128)  S^T = K Q_i^T (fp32) -> P^T (bf16) -> later dQ_i
-//     [128,256)  dP^T = V dO_i^T (fp32) -> dS^T (bf16)
-//     [256,256+d)      dV accumulator
-//     [256+d,256+2d)   dK accumulator
+//   tensor memory (512 columns x 128 lanes)
+//     [  0,128)  S^T = K Q_i^T (fp32, lane = key) -> P^T (bf16)
+//     [128,256)  dP^T = V dO_i^T (fp32, lane = key) -> dS^T (bf16)
+//                -> then dQ_i = dS K (fp32, lane = query, d columns)
+//     [256,256+d)      dV accumulator (lane = key)
+//     [256+d,256+2d)   dK accumulator (lane = key)
 //   Each compute warpgroup owns 64 query columns of S^T and dP^T and packs
 //   its bf16 P^T / dS^T into the first 32 of them, so neither warpgroup
-//   overwrites fp32 values the other has not read yet.
-//   (dQ_i = dS K has the query as its row, so it is the one product whose
-//    A operand must come from shared memory: at d = 128 dS is written over
-//    the dO_i tile once dV has consumed it; at d = 64 it has its own buffer.
-//    dQ_i lands in the S^T columns.)
+//   overwrites fp32 values the other has not read yet.  dQ_i = dS K has the
+//   query as its row, so its A operand is dS in shared memory (at d = 128
+//   written over the dO_i tile once dV has consumed it; at d = 64 in its own
+//   buffer).  dQ_i lands in the dP^T columns, so draining it overlaps the next
+//   tile's S^T product and softmax.
 //
 // Per query tile i (MMA issue order):
-//   dP^T = V dO_i^T ; [dQ_{i-1} drained] S^T = K Q_i^T ;
+//   S^T = K Q_i^T ; [dQ_{i-1} drained] dP^T = V dO_i^T ;
 //   [P^T ready] dV += P^T dO_i ; [dS ready] dK += dS^T Q_i ; dQ_i = dS K
 // with P^T = exp2(S^T c - LSE_i log2 e) and dS = scale * P (dP - D_i): the
 // softmax scale is folded into dS, so dK and dQ come out scaled.
 //
-// Warp roles (448 threads):
+// Warp roles (512 threads = four warpgroups):
 //   warps 0-7   compute: two warpgroups, thread = key row, warpgroup w takes
 //               query columns [64w, 64w + 64); at the end warpgroup 0 writes
 //               dV, warpgroup 1 dK
-//   warps 8-11  dQ drain: thread = query row, tensor memory -> fp32 atomics
+//   warps 8-11  dQ drain: thread = query row; tensor memory -> swizzled
+//               shared-memory chunks of 16 columns -> TMA reduce-add
 //   warp  12    loads: K, V once; Q_i, dO_i by TMA; LSE_i, D_i by plain loads
 //   warp  13    tensor-memory allocator; lane 0 issues every MMA
+//   warps 14-15 idle
+// Launched with 128 registers per thread; the warpgroups then re-split them
+// (compute 176, drain 80, load/MMA 72).
 #include "fa_device.cuh"
 #include "fa_kernels.h"
 
@@ -44,7 +50,14 @@ namespace {
 template <int D>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kThreads = 448;
+  static constexpr int kThreads = 512;
+  static constexpr int kLaunchRegs = 128;
+  static constexpr int kComputeRegs = 176;  // 2 x 128 threads
+  static constexpr int kDrainRegs = 80;     // 128 threads
+  static constexpr int kOtherRegs = 72;     // 128 threads
+  static_assert(2 * 128 * kComputeRegs + 128 * kDrainRegs + 128 * kOtherRegs <=
+                    kThreads * kLaunchRegs,
+                "register split exceeds the launch allocation");
   static constexpr int kDrainWarp0 = 8;
   static constexpr int kProducerWarp = 12;
   static constexpr int kMmaWarp = 13;
@@ -62,7 +75,11 @@ struct BwdCfg {
   // too small and dS gets one buffer per stage.
   static constexpr int kDsOff = kDsumOff + kStages * kBlockM * 4;
   static constexpr int kDsBytes = (D == 128) ? 0 : kStages * kDsTileBytes;
-  static constexpr int kBarOff = kDsOff + kDsBytes;
+  // dQ staging: two chunks of 128 rows x 16 fp32 (64-byte swizzled rows)
+  static constexpr int kDqCols = 16;
+  static constexpr int kDqChunkBytes = kBlockM * kDqCols * 4;
+  static constexpr int kDqOff = kDsOff + kDsBytes;
+  static constexpr int kBarOff = kDqOff + 2 * kDqChunkBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarStFull = 1;
   static constexpr int kBarStEmpty = kBarStFull + kStages;
@@ -80,9 +97,10 @@ struct BwdCfg {
   static constexpr int kSmemBytes = kAbortOff + 4 + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColDP = 128;
+  static constexpr uint32_t kColDP = 128;  // dP^T, dS^T, then dQ
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
+  static constexpr int kDrainBarrier = 1;  // named barrier of the drain warpgroup
   // Shared-memory offset of stage s's dS tile.
   static __device__ __forceinline__ int ds_off(int s) {
     return (D == 128) ? kDOOff + s * kTileBytes : kDsOff + s * kDsTileBytes;
@@ -160,59 +178,60 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == C::kProducerWarp) {
-    // ------------------------------------------------------------- loads
-    if (lane == 0) {
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
-      tma_prefetch_desc(&p.tm_v);
-      tma_prefetch_desc(&p.tm_do);
-      mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTileBytes);
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_3d(sbase + C::kKOff + h * C::kHalfBytes, &p.tm_k, bar(C::kBarKV), h * 64, k0, bh);
-        tma_load_3d(sbase + C::kVOff + h * C::kHalfBytes, &p.tm_v, bar(C::kBarKV), h * 64, k0, bh);
-      }
-    }
-    int issued = 0;
-    for (int it = 0; it < n_iter; ++it) {
-      const int s = it % C::kStages;
-      const int use = it / C::kStages;
-      if (use > 0) {
-        bool ok = mbar_wait(bar(C::kBarStEmpty + s), (use - 1) & 1, ctl, kSiteStEmpty);
-        if (!__all_sync(0xffffffffu, ok)) break;
-      }
-      const int q0 = (i_first + it) * kBlockM;
+  if (warp >= C::kProducerWarp) {
+    regs_dec<C::kOtherRegs>();
+    if (warp == C::kProducerWarp) {
+      // ----------------------------------------------------------- loads
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(C::kBarStFull + s), 2 * C::kTileBytes);
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_do);
+        mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTileBytes);
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_3d(sbase + C::kQOff + s * C::kTileBytes + h * C::kHalfBytes, &p.tm_q,
-                      bar(C::kBarStFull + s), h * 64, q0, bh);
-          tma_load_3d(sbase + C::kDOOff + s * C::kTileBytes + h * C::kHalfBytes, &p.tm_do,
-                      bar(C::kBarStFull + s), h * 64, q0, bh);
+          tma_load_3d(sbase + C::kKOff + h * C::kHalfBytes, &p.tm_k, bar(C::kBarKV), h * 64, k0, bh);
+          tma_load_3d(sbase + C::kVOff + h * C::kHalfBytes, &p.tm_v, bar(C::kBarKV), h * 64, k0, bh);
         }
       }
-      // LSE in log2 units and D for the 128 rows; rows past N get LSE = +inf
-      // (so P = 0) and D = 0.
+      int issued = 0;
+      for (int it = 0; it < n_iter; ++it) {
+        const int s = it % C::kStages;
+        const int use = it / C::kStages;
+        if (use > 0) {
+          bool ok = mbar_wait(bar(C::kBarStEmpty + s), (use - 1) & 1, ctl, kSiteStEmpty);
+          if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        const int q0 = (i_first + it) * kBlockM;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(C::kBarStFull + s), 2 * C::kTileBytes);
+          for (int h = 0; h < D / 64; ++h) {
+            tma_load_3d(sbase + C::kQOff + s * C::kTileBytes + h * C::kHalfBytes, &p.tm_q,
+                        bar(C::kBarStFull + s), h * 64, q0, bh);
+            tma_load_3d(sbase + C::kDOOff + s * C::kTileBytes + h * C::kHalfBytes, &p.tm_do,
+                        bar(C::kBarStFull + s), h * 64, q0, bh);
+          }
+        }
+        // LSE in log2 units and D for the 128 rows; rows past N get LSE = +inf
+        // (so P = 0) and D = 0.
 #pragma unroll
-      for (int r4 = 0; r4 < 4; ++r4) {
-        const int r = lane * 4 + r4;
-        const int q = q0 + r;
-        const size_t gi = static_cast<size_t>(bh) * p.N + q;
-        lse_s[s * kBlockM + r] = (q < p.N) ? p.lse[gi] * p.log2e : INFINITY;
-        dsum_s[s * kBlockM + r] = (q < p.N) ? p.dsum[gi] : 0.0f;
+        for (int r4 = 0; r4 < 4; ++r4) {
+          const int r = lane * 4 + r4;
+          const int q = q0 + r;
+          const size_t gi = static_cast<size_t>(bh) * p.N + q;
+          lse_s[s * kBlockM + r] = (q < p.N) ? p.lse[gi] * p.log2e : INFINITY;
+          dsum_s[s * kBlockM + r] = (q < p.N) ? p.dsum[gi] : 0.0f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kBarStFull + s));
+        issued = it + 1;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kBarStFull + s));
-      issued = it + 1;
-    }
-    if (lane == 0) {
-      mbar_wait_drain(bar(C::kBarKV), 0);
-      for (int it = max(0, issued - C::kStages); it < issued; ++it)
-        mbar_wait_drain(bar(C::kBarStFull + it % C::kStages), (it / C::kStages) & 1);
-    }
-  } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------- MMA issue
-    if (lane == 0) {
+      if (lane == 0) {
+        mbar_wait_drain(bar(C::kBarKV), 0);
+        for (int it = max(0, issued - C::kStages); it < issued; ++it)
+          mbar_wait_drain(bar(C::kBarStFull + it % C::kStages), (it / C::kStages) & 1);
+      }
+    } else if (warp == C::kMmaWarp && lane == 0) {
+      // ----------------------------------------------------------- MMA issue
       constexpr uint32_t kIdescSq = idesc_bf16_f32(kBlockN, kBlockM, false, false);  // S^T, dP^T
       constexpr uint32_t kIdescKV = idesc_bf16_f32(kBlockN, D, false, true);          // dV, dK
       constexpr uint32_t kIdescQ = idesc_bf16_f32(kBlockM, D, true, true);            // dQ
@@ -237,13 +256,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                  sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024), kIdescKV,
                  (accumulate || kk > 0) ? 1u : 0u);
       };
-      // dQ_i = dS K: A = dS (queries x keys) MN-major in the dO_i buffer
-      // (64-query blocks 16 KB apart, 8-key groups 1024 B apart); B = K as an
-      // MN-major operand (d contiguous).
+      // dQ_i = dS K: A = dS (queries x keys) MN-major (64-query blocks 16 KB
+      // apart, 8-key groups 1024 B apart); B = K as an MN-major operand (d
+      // contiguous).  The result goes to the dP^T columns.
       auto issue_dq = [&](uint32_t ds0) {
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ss(tmem_base + C::kColS, sdesc_sw128(ds0 + kk * 2048, kBlockN * 128, 1024),
+          mma_ss(tmem_base + C::kColDP, sdesc_sw128(ds0 + kk * 2048, kBlockN * 128, 1024),
                  sdesc_sw128(k_smem + kk * 2048, C::kHalfBytes, 1024), kIdescQ, kk > 0 ? 1u : 0u);
       };
 
@@ -254,14 +273,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t do_s = sbase + C::kDOOff + s * C::kTileBytes;
         if (!(ok = mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull))) break;
         tc_fence_after();
-        issue_nt(v_smem, do_s, C::kColDP);
-        mma_commit(bar(C::kBarDPFull));
+        issue_nt(k_smem, q_s, C::kColS);
+        mma_commit(bar(C::kBarSFull));
         if (it > 0) {
           if (!(ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl, kSiteDQEmpty))) break;
           tc_fence_after();
         }
-        issue_nt(k_smem, q_s, C::kColS);
-        mma_commit(bar(C::kBarSFull));
+        issue_nt(v_smem, do_s, C::kColDP);
+        mma_commit(bar(C::kBarDPFull));
         if (!(ok = mbar_wait(bar(C::kBarPFull), it & 1, ctl, kSitePFull))) break;
         tc_fence_after();
         issue_tn(C::kColS, do_s, C::kColDV, it > 0);
@@ -277,33 +296,52 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (!ok) mbar_wait_drain(bar(C::kBarMmaDone), 0);
     }
   } else if (warp >= C::kDrainWarp0) {
+    regs_dec<C::kDrainRegs>();
     // ------------------------------------------------------------- dQ drain
     const int quarter = warp & 3;
-    const int qr = quarter * 32 + lane;
-    const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColS;
+    const int qr = quarter * 32 + lane;  // query row within the tile
+    const bool leader = (warp == C::kDrainWarp0 && lane == 0);
+    const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
+    uint8_t* stage0 = smem + C::kDqOff;
+    bool pending = false;
     for (int it = 0; it < n_iter; ++it) {
       bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int q = (i_first + it) * kBlockM + qr;
-      float4* dst = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.N + q) * D);
+      const int q0 = (i_first + it) * kBlockM;
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(t_dq + ch * 32, r);
-        tmem_ld_wait(r);
-        if (q < p.N) {
+      for (int ch = 0; ch < D / C::kDqCols; ++ch) {
+        uint32_t r[16];
+        tmem_ld16(t_dq + ch * C::kDqCols, r);
+        tmem_ld_wait16(r);
+        if (ch == D / C::kDqCols - 1) {
+          // dQ_i has left tensor memory: the MMA may write the columns again.
+          tc_fence_before();
+          mbar_arrive(bar(C::kBarDQEmpty));
+        }
+        // 128 rows x 64 bytes, 64-byte swizzle: 16-byte chunk index XOR
+        // ((row / 2) mod 4).  The buffer written here was last read by the
+        // reduction issued two chunks ago, which the leader waited for before
+        // the previous barrier.
+        uint8_t* buf = stage0 + (ch & 1) * C::kDqChunkBytes + qr * 64;
 #pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4)
-            atomicAdd(dst + ch * 8 + v4,
-                      make_float4(__uint_as_float(r[4 * v4]), __uint_as_float(r[4 * v4 + 1]),
-                                  __uint_as_float(r[4 * v4 + 2]), __uint_as_float(r[4 * v4 + 3])));
+        for (int c4 = 0; c4 < 4; ++c4)
+          *reinterpret_cast<uint4*>(buf + ((c4 ^ ((qr >> 1) & 3)) << 4)) =
+              make_uint4(r[4 * c4], r[4 * c4 + 1], r[4 * c4 + 2], r[4 * c4 + 3]);
+        fence_proxy_async_smem();
+        if (leader && pending) bulk_wait_read<0>();
+        named_bar_sync(C::kDrainBarrier, kBlockM);
+        if (leader) {
+          tma_reduce_add_3d(&p.tm_dq, smem_u32(stage0 + (ch & 1) * C::kDqChunkBytes),
+                            ch * C::kDqCols, q0, bh);
+          bulk_commit();
+          pending = true;
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarDQEmpty));
     }
+    if (leader) bulk_wait<0>();
   } else {
+    regs_inc<C::kComputeRegs>();
     // ------------------------------------------------------------- compute
     const int wg = warp >> 2;  // query-column half
     const int quarter = warp & 3;
@@ -311,8 +349,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int kpos = k0 + kr;
     const bool row_valid = kpos < p.N;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float c = p.c;
-    const float scale = p.scale;
+    const f32x2 c2 = f2_pack(p.c, p.c);
+    const f32x2 scale2 = f2_pack(p.scale, p.scale);
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % C::kStages;
@@ -327,21 +365,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
       // P^T = exp2(S^T c - LSE log2 e); masked entries (query < key on the
       // diagonal tile, keys past N) are 0.
+      uint32_t sr[2][32];
+      tmem_ld32(lane_base + C::kColS + wg * 64, sr[0]);
+      tmem_ld32(lane_base + C::kColS + wg * 64 + 32, sr[1]);
+      tmem_ld_wait(sr[0]);
+      reg_fence(sr[1]);
       float pf[64];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int col0 = wg * 64 + ch * 32;
-        uint32_t r[32];
-        tmem_ld32(lane_base + C::kColS + col0, r);
-        tmem_ld_wait(r);
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse2 + col0 + 4 * e4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][4 * e4]), __uint_as_float(sr[ch][4 * e4 + 1])),
+                           c2, f2_pack(-l4.x, -l4.y)),
+                    x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][4 * e4 + 2]), __uint_as_float(sr[ch][4 * e4 + 3])),
+                           c2, f2_pack(-l4.z, -l4.w)),
+                    x2, x3);
+          const float xs[4] = {x0, x1, x2, x3};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int col = col0 + 4 * e4 + e;
-            float pv = ex2_mufu(fmaf(__uint_as_float(r[4 * e4 + e]), c, -lv[e]));
+            float pv = ex2_mufu(xs[e]);
             if (!row_valid || (diag && col < kr)) pv = 0.0f;
             pf[ch * 32 + 4 * e4 + e] = pv;
           }
@@ -356,29 +403,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_arrive(bar(C::kBarPFull));
 
       // dS = scale * P (dP - D): to tensor memory (for dK) and, once dV has
-      // finished reading dO_i, into the dO_i buffer (for dQ).
+      // finished reading dO_i, into shared memory (for dQ).
       ok = mbar_wait(bar(C::kBarDPFull), it & 1, ctl, kSiteDPFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
+      uint32_t dr[2][32];
+      tmem_ld32(lane_base + C::kColDP + wg * 64, dr[0]);
+      tmem_ld32(lane_base + C::kColDP + wg * 64 + 32, dr[1]);
+      tmem_ld_wait(dr[0]);
+      reg_fence(dr[1]);
       uint32_t dsw[32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int col0 = wg * 64 + ch * 32;
-        uint32_t r[32];
-        tmem_ld32(lane_base + C::kColDP + col0, r);
-        tmem_ld_wait(r);
-        float dsv[32];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 d4 = *reinterpret_cast<const float4*>(dsm + col0 + 4 * e4);
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dsv[4 * e4 + e] =
-                scale * pf[ch * 32 + 4 * e4 + e] * (__uint_as_float(r[4 * e4 + e]) - dv[e]);
+          float a0, a1, a2, a3;
+          f2_unpack(f2_mul(f2_mul(f2_add(f2_pack(__uint_as_float(dr[ch][4 * e4]), __uint_as_float(dr[ch][4 * e4 + 1])),
+                                         f2_pack(-d4.x, -d4.y)),
+                                  f2_pack(pf[ch * 32 + 4 * e4], pf[ch * 32 + 4 * e4 + 1])),
+                           scale2),
+                    a0, a1);
+          f2_unpack(f2_mul(f2_mul(f2_add(f2_pack(__uint_as_float(dr[ch][4 * e4 + 2]), __uint_as_float(dr[ch][4 * e4 + 3])),
+                                         f2_pack(-d4.z, -d4.w)),
+                                  f2_pack(pf[ch * 32 + 4 * e4 + 2], pf[ch * 32 + 4 * e4 + 3])),
+                           scale2),
+                    a2, a3);
+          dsw[ch * 16 + 2 * e4] = pack_bf16x2(a0, a1);
+          dsw[ch * 16 + 2 * e4 + 1] = pack_bf16x2(a2, a3);
         }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) dsw[ch * 16 + e] = pack_bf16x2(dsv[2 * e], dsv[2 * e + 1]);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = dsw[ch * 16 + e];
@@ -443,8 +497,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 template <int D>
 cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  cudaError_t err = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+  // The setmaxnreg split assumes the launch allocation; refuse to run a build
+  // whose register count differs (an over-committed split would never finish).
+  cudaFuncAttributes attr;
+  cudaError_t err = cudaFuncGetAttributes(&attr, fa_bwd_kernel<D>);
+  if (err != cudaSuccess) return err;
+  if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  err = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(p.n_kblk) * p.BH;
   fa_bwd_kernel<D><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);

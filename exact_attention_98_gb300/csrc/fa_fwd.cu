@@ -15,11 +15,15 @@
 // CTA = two 128-row query tiles of one (batch, head); keys and values stream
 // through a ring of shared-memory slots (K_j and V_j alternate).
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax warpgroup for query tile 0 (thread = one query row)
-//   warps 4-7  softmax warpgroup for query tile 1
-//   warp  8    TMA producer
-//   warp  9    tensor-memory allocator; lane 0 issues every MMA
+// Warp roles (384 threads = three warpgroups):
+//   warps 0-3   softmax warpgroup for query tile 0 (thread = one query row)
+//   warps 4-7   softmax warpgroup for query tile 1
+//   warp  8     TMA producer
+//   warp  9     tensor-memory allocator; lane 0 issues every MMA
+//   warps 10-11 idle
+// The CTA is launched with 168 registers per thread (12 warps, three per SM
+// sub-partition); the third warpgroup gives registers up (80) so that each
+// softmax thread can hold a whole row of S (208).
 //
 // MMA order per key tile j (ping-pong: while one warpgroup computes the
 // softmax of its tile the tensor core works on the other tile):
@@ -37,7 +41,12 @@ namespace {
 template <int D>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 384;
+  static constexpr int kLaunchRegs = 168;   // what ptxas must allocate (checked at launch)
+  static constexpr int kSoftmaxRegs = 208;  // 2 x 128 threads
+  static constexpr int kOtherRegs = 80;     // 128 threads
+  static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
+                "register split exceeds the launch allocation");
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;
   static constexpr int kTileBytes = kBlockM * D * 2;  // one Q, K or V tile (bf16)
@@ -62,7 +71,6 @@ struct FwdCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol0 = 0;    // S_t / P_t at t * 128
   static constexpr uint32_t kOCol0 = 256;  // O_t at 256 + t * D
-  static constexpr int kPolyPerOctet = 2;  // of every 8 exponentials, this many on the FMA pipe
 };
 
 // Wait-site codes recorded on a timeout (bits 8..23 of the status word).
@@ -76,7 +84,9 @@ enum : unsigned int {
   kSiteOFull = 0x107,
 };
 
-template <int D>
+// POLY: of every 8 exponentials of the softmax, this many are evaluated by
+// exp2_poly on the FMA pipe, the rest by MUFU ex2.
+template <int D, int POLY>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
@@ -129,7 +139,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == C::kProducerWarp) {
+  if (warp >= 8) {
+   regs_dec<C::kOtherRegs>();
+   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
@@ -242,7 +254,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mma_commit(bar(C::kBarMmaDone));
       mbar_wait_drain(bar(C::kBarMmaDone), 0);
     }
+   }
   } else {
+    regs_inc<C::kSoftmaxRegs>();
     // ------------------------------------------------------------- softmax
     const int t = warp >> 2;             // query tile of this warpgroup
     const int quarter = warp & 3;        // tensor-memory lane quarter
@@ -252,102 +266,117 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const uint32_t t_s = lane_base + C::kSCol0 + t * 128;
     const uint32_t t_o = lane_base + C::kOCol0 + t * D;
     const float c = p.c;
+    const f32x2 c2 = f2_pack(c, c);
     const bool ragged = (p.N % kBlockN) != 0;
 
     float m_used = -INFINITY;  // running row max in log2 units (scores * c)
-    float l = 0.0f;            // row sum of exp2(x - m_used), unrounded: gives LSE
-    float l_bf = 0.0f;         // row sum of the bf16-rounded P: normalises O
+    f32x2 l2 = f2_pack(0.0f, 0.0f);   // row sum of exp2(x - m_used), unrounded: gives LSE
+    f32x2 lb2 = f2_pack(0.0f, 0.0f);  // row sum of the bf16-rounded P: normalises O
     bool ok = true;
     for (int j = 0; j < nkv[t]; ++j) {
       ok = mbar_wait(bar(C::kBarSFull + t), j & 1, ctl, kSiteSFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int kbase = j * kBlockN;
-      const bool edge = (p.causal && j == nkv[t] - 1) || (ragged && j == n_ktiles - 1);
-      auto valid = [&](int col) {
-        const int kpos = kbase + col;
-        return kpos < p.N && (!p.causal || kpos <= qpos);
-      };
+      // The whole row of S (128 fp32) in registers: four loads, one wait.
+      uint32_t r[4][32];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld32(t_s + ch * 32, r[ch]);
+      tmem_ld_wait(r[0]);
+      reg_fence(r[1]);
+      reg_fence(r[2]);
+      reg_fence(r[3]);
 
-      // pass 1: row max of this tile
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int ch = 0; ch < kBlockN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(t_s + ch * 32, r);
-        tmem_ld_wait(r);
-        if (edge) {
+      const bool edge = (p.causal && j == nkv[t] - 1) || (ragged && j == n_ktiles - 1);
+      if (edge) {
+        const int kbase = j * kBlockN;
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (valid(ch * 32 + e)) mx = fmaxf(mx, __uint_as_float(r[e]) * c);
-        } else {
-          float m2 = -INFINITY;
+        for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) m2 = fmaxf(m2, __uint_as_float(r[e]));
-          mx = fmaxf(mx, m2 * c);
-        }
+          for (int e = 0; e < 32; ++e) {
+            const int kpos = kbase + ch * 32 + e;
+            if (kpos >= p.N || (p.causal && kpos > qpos)) r[ch][e] = __float_as_uint(-INFINITY);
+          }
       }
+      // row max of the tile (raw scores; c > 0)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          mx = fmax3(mx, __uint_as_float(r[ch][e]), __uint_as_float(r[ch][e + 1]));
       // Conditional rescale: move the reference max only when it grows by
       // more than the threshold (always on the first tile, m_used = -inf).
-      const float m_new = fmaxf(m_used, mx);
+      const float m_new = fmaxf(m_used, mx * c);
       const bool need = (m_new - m_used) > kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
         const float alpha = need ? ex2_mufu(m_used - m_new) : 1.0f;
         if (j > 0) {
+          const f32x2 a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(t_o + ch * 32, r);
-            tmem_ld_wait(r);
+            uint32_t o[32];
+            tmem_ld32(t_o + ch * 32, o);
+            tmem_ld_wait(o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(t_o + ch * 32, r);
+            for (int e = 0; e < 32; e += 2) {
+              float lo, hi;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
+              o[e] = __float_as_uint(lo);
+              o[e + 1] = __float_as_uint(hi);
+            }
+            tmem_st32(t_o + ch * 32, o);
           }
           tmem_st_wait();
         }
         if (need) {
-          l *= alpha;
-          l_bf *= alpha;
+          const f32x2 a2 = f2_pack(alpha, alpha);
+          l2 = f2_mul(l2, a2);
+          lb2 = f2_mul(lb2, a2);
           m_used = m_new;
         }
       }
 
-      // pass 2: P = exp2(x - m_used) -> bf16 into tensor memory over S
-      const float neg_m = -m_used;
-#pragma unroll 1
-      for (int ch = 0; ch < kBlockN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(t_s + ch * 32, r);
-        tmem_ld_wait(r);
-        float pv[32];
+      // P = exp2(x - m_used) -> bf16 into tensor memory over S.  Masked
+      // entries are -inf and give exact zeros from MUFU; edge tiles use MUFU
+      // only.  O is normalised by the sum of the bf16-rounded P (the very
+      // weights the P V MMA uses: O is then an exact convex combination of V
+      // rows, and the rounding of a dominant weight, anything in [1, 2^8]
+      // under a stale reference max, cancels in O / l_bf); LSE keeps the
+      // unrounded sum.
+      const f32x2 negm2 = f2_pack(-m_used, -m_used);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x = fmaf(__uint_as_float(r[e]), c, neg_m);
-          pv[e] = ((e & 7) < C::kPolyPerOctet) ? exp2_poly(x) : ex2_mufu(x);
-        }
-        if (edge) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!valid(ch * 32 + e)) pv[e] = 0.0f;
-        }
-        // O is normalised by the sum of the bf16-rounded P, the very weights
-        // the P V MMA uses: O is then an exact convex combination of V rows,
-        // and the rounding of a dominant weight (a stale reference max makes
-        // it anything in [1, 2^8]) cancels in O / l_bf.  LSE keeps the
-        // unrounded sum.
+      for (int ch = 0; ch < 4; ++ch) {
         uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          w[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-          l += pv[2 * e] + pv[2 * e + 1];
-          l_bf += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
+        for (int e = 0; e < 32; e += 2) {
+          float x0, x1, p0, p1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[ch][e]), __uint_as_float(r[ch][e + 1])), c2, negm2),
+                    x0, x1);
+          if (!edge && ((ch * 32 + e) & 7) < POLY) {
+            exp2_poly2(x0, x1, p0, p1);
+          } else {
+            p0 = ex2_mufu(x0);
+            p1 = ex2_mufu(x1);
+          }
+          const uint32_t wp = pack_bf16x2(p0, p1);
+          w[e >> 1] = wp;
+          l2 = f2_add(l2, f2_pack(p0, p1));
+          lb2 = f2_add(lb2, f2_pack(__uint_as_float(wp << 16), __uint_as_float(wp & 0xFFFF0000u)));
         }
         tmem_st16(t_s + ch * 16, w);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull + t));
+    }
+    float l, l_bf;
+    {
+      float a, b;
+      f2_unpack(l2, a, b);
+      l = a + b;
+      f2_unpack(lb2, a, b);
+      l_bf = a + b;
     }
 
     // epilogue: O / l_bf -> bf16, LSE = ln(2) * m_used + ln(l)
@@ -389,15 +418,32 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
+template <int D, int POLY>
+cudaError_t launch_fwd_dp(const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  cudaError_t err = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+  // The setmaxnreg split assumes the launch allocation; refuse to run a build
+  // whose register count differs (an over-committed split would never finish).
+  cudaFuncAttributes attr;
+  cudaError_t err = cudaFuncGetAttributes(&attr, fa_fwd_kernel<D, POLY>);
+  if (err != cudaSuccess) return err;
+  if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  err = cudaFuncSetAttribute(fa_fwd_kernel<D, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(p.n_qblk) * p.BH;
-  fa_fwd_kernel<D><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
+  fa_fwd_kernel<D, POLY><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
+  switch (p.poly_per_octet) {
+    case 0: return launch_fwd_dp<D, 0>(p, stream);
+    case 1: return launch_fwd_dp<D, 1>(p, stream);
+    case 2: return launch_fwd_dp<D, 2>(p, stream);
+    case 3: return launch_fwd_dp<D, 3>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace

@@ -32,13 +32,20 @@ struct FwdParams {
   int causal;
   float c;          // scale * log2(e): scores enter exp2 in these units
   float ln2;        // ln(2), to turn the log2-unit row max into LSE
+  int poly_per_octet;  // exponentials per 8 on the FMA pipe (0..3)
 };
+
+// Default share of the forward's exponentials evaluated by the polynomial on
+// the FMA pipe (per 8); FA_FWD_POLY_PER_OCTET in the environment selects
+// another pre-built instantiation (0..3).
+constexpr int kDefaultPolyPerOctet = 2;
 
 struct BwdParams {
   CUtensorMap tm_q;   // bf16 [BH, N, d]
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
+  CUtensorMap tm_dq;  // fp32 dQ accumulator [BH, N, d], box {16, 128, 1}, 64B swizzle
   const float* lse;   // fp32 [BH, N]
   const float* dsum;  // fp32 [BH, N]: D = rowsum(dO * O)
   float* dq_acc;      // fp32 [BH, N, d], zeroed before the main kernel
