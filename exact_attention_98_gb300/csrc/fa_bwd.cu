@@ -34,13 +34,17 @@
 //   warps 0-7   compute: two warpgroups, thread = key row, warpgroup w takes
 //               query columns [64w, 64w + 64); at the end warpgroup 0 writes
 //               dV, warpgroup 1 dK
-//   warps 8-11  dQ drain: thread = query row; tensor memory -> swizzled
-//               shared-memory chunks of 16 columns -> TMA reduce-add
+//   warps 8-11  dQ drain: thread = query row; tensor memory -> registers (in
+//               two batches, after which the columns are free again) ->
+//               swizzled 16-column fp32 chunks in the Q_i and dO_i buffers
+//               (dead once dQ_i is computed: together exactly one fp32 dQ
+//               tile) -> TMA reduce-adds; the stage goes back to the loader
+//               when the TMA has read it
 //   warp  12    loads: K, V once; Q_i, dO_i by TMA; LSE_i, D_i by plain loads
 //   warp  13    tensor-memory allocator; lane 0 issues every MMA
 //   warps 14-15 idle
 // Launched with 128 registers per thread; the warpgroups then re-split them
-// (compute 176, drain 80, load/MMA 72).
+// (compute 176, drain 96, load/MMA 64).
 #include "fa_device.cuh"
 #include "fa_kernels.h"
 
@@ -53,8 +57,8 @@ struct BwdCfg {
   static constexpr int kThreads = 512;
   static constexpr int kLaunchRegs = 128;
   static constexpr int kComputeRegs = 176;  // 2 x 128 threads
-  static constexpr int kDrainRegs = 80;     // 128 threads
-  static constexpr int kOtherRegs = 72;     // 128 threads
+  static constexpr int kDrainRegs = 96;     // 128 threads
+  static constexpr int kOtherRegs = 64;     // 128 threads
   static_assert(2 * 128 * kComputeRegs + 128 * kDrainRegs + 128 * kOtherRegs <=
                     kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
@@ -75,11 +79,13 @@ struct BwdCfg {
   // too small and dS gets one buffer per stage.
   static constexpr int kDsOff = kDsumOff + kStages * kBlockM * 4;
   static constexpr int kDsBytes = (D == 128) ? 0 : kStages * kDsTileBytes;
-  // dQ staging: two chunks of 128 rows x 16 fp32 (64-byte swizzled rows)
+  // dQ staging: d/16 chunks of 128 rows x 16 fp32 (64-byte swizzled rows),
+  // the first half in the stage's Q buffer, the second in its dO buffer.
   static constexpr int kDqCols = 16;
+  static constexpr int kDqChunks = D / kDqCols;
   static constexpr int kDqChunkBytes = kBlockM * kDqCols * 4;
-  static constexpr int kDqOff = kDsOff + kDsBytes;
-  static constexpr int kBarOff = kDqOff + 2 * kDqChunkBytes;
+  static_assert(kDqChunks / 2 * kDqChunkBytes == kTileBytes, "dQ staging must fill Q and dO");
+  static constexpr int kBarOff = kDsOff + kDsBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarStFull = 1;
   static constexpr int kBarStEmpty = kBarStFull + kStages;
@@ -289,8 +295,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_after();
         issue_tn(C::kColDP, q_s, C::kColDK, it > 0);
         issue_dq(sbase + C::ds_off(s));
-        mma_commit(bar(C::kBarDQFull));
-        mma_commit(bar(C::kBarStEmpty + s));
+        mma_commit(bar(C::kBarDQFull));  // the drain returns stage s to the loader
       }
       mma_commit(bar(C::kBarMmaDone));
       if (!ok) mbar_wait_drain(bar(C::kBarMmaDone), 0);
@@ -302,41 +307,52 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int qr = quarter * 32 + lane;  // query row within the tile
     const bool leader = (warp == C::kDrainWarp0 && lane == 0);
     const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
-    uint8_t* stage0 = smem + C::kDqOff;
-    bool pending = false;
     for (int it = 0; it < n_iter; ++it) {
+      const int s = it % C::kStages;
       bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int q0 = (i_first + it) * kBlockM;
-#pragma unroll 1
-      for (int ch = 0; ch < D / C::kDqCols; ++ch) {
-        uint32_t r[16];
-        tmem_ld16(t_dq + ch * C::kDqCols, r);
-        tmem_ld_wait16(r);
-        if (ch == D / C::kDqCols - 1) {
+      // dK_i and dQ_i, the last readers of Q_i and dO_i, are complete: their
+      // buffers take the fp32 dQ tile.
+      auto chunk_base = [&](int ch) -> uint8_t* {
+        return smem + (ch < C::kDqChunks / 2 ? C::kQOff : C::kDOOff) + s * C::kTileBytes +
+               (ch % (C::kDqChunks / 2)) * C::kDqChunkBytes;
+      };
+#pragma unroll
+      for (int b = 0; b < C::kDqChunks / 4; ++b) {
+        uint32_t r[4][16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld16(t_dq + (4 * b + c) * C::kDqCols, r[c]);
+        tmem_ld_wait16(r[0]);
+        reg_fence16(r[1]);
+        reg_fence16(r[2]);
+        reg_fence16(r[3]);
+        if (b == C::kDqChunks / 4 - 1) {
           // dQ_i has left tensor memory: the MMA may write the columns again.
           tc_fence_before();
           mbar_arrive(bar(C::kBarDQEmpty));
         }
-        // 128 rows x 64 bytes, 64-byte swizzle: 16-byte chunk index XOR
-        // ((row / 2) mod 4).  The buffer written here was last read by the
-        // reduction issued two chunks ago, which the leader waited for before
-        // the previous barrier.
-        uint8_t* buf = stage0 + (ch & 1) * C::kDqChunkBytes + qr * 64;
+        // 128 rows x 64 bytes per chunk, 64-byte swizzle: 16-byte chunk index
+        // XOR ((row / 2) mod 4).
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          *reinterpret_cast<uint4*>(buf + ((c4 ^ ((qr >> 1) & 3)) << 4)) =
-              make_uint4(r[4 * c4], r[4 * c4 + 1], r[4 * c4 + 2], r[4 * c4 + 3]);
-        fence_proxy_async_smem();
-        if (leader && pending) bulk_wait_read<0>();
-        named_bar_sync(C::kDrainBarrier, kBlockM);
-        if (leader) {
-          tma_reduce_add_3d(&p.tm_dq, smem_u32(stage0 + (ch & 1) * C::kDqChunkBytes),
-                            ch * C::kDqCols, q0, bh);
-          bulk_commit();
-          pending = true;
+        for (int c = 0; c < 4; ++c) {
+          uint8_t* row = chunk_base(4 * b + c) + qr * 64;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<uint4*>(row + ((c4 ^ ((qr >> 1) & 3)) << 4)) =
+                make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]);
         }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(C::kDrainBarrier, kBlockM);
+      if (leader) {
+        const int q0 = (i_first + it) * kBlockM;
+#pragma unroll 1
+        for (int ch = 0; ch < C::kDqChunks; ++ch)
+          tma_reduce_add_3d(&p.tm_dq, smem_u32(chunk_base(ch)), ch * C::kDqCols, q0, bh);
+        bulk_commit();
+        bulk_wait_read<0>();  // the TMA has read the staged tile: stage s is free
+        mbar_arrive(bar(C::kBarStEmpty + s));
       }
     }
     if (leader) bulk_wait<0>();

@@ -11,6 +11,11 @@
 //   * exponentials partly on the FMA pipe (exp2_poly) and partly on MUFU;
 //   * conditional rescaling: O_t and the row sum are rescaled only when a row
 //     max grows by more than kRescaleThreshold (log2 units).
+// On GB300 the MUFU unit is not what limits this softmax (its issue slots
+// are): measured on B2 H16 N4096 d128, the forward ran at 1073 TFLOP/s with
+// every exponential on MUFU and at 861 / 859 / 699 TFLOP/s with 1 / 2 / 3 of
+// every 8 on the FMA pipe, so the default share is 0; the other shares stay
+// instantiated and selectable.
 //
 // CTA = two 128-row query tiles of one (batch, head); keys and values stream
 // through a ring of shared-memory slots (K_j and V_j alternate).
@@ -270,8 +275,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const bool ragged = (p.N % kBlockN) != 0;
 
     float m_used = -INFINITY;  // running row max in log2 units (scores * c)
-    f32x2 l2 = f2_pack(0.0f, 0.0f);   // row sum of exp2(x - m_used), unrounded: gives LSE
-    f32x2 lb2 = f2_pack(0.0f, 0.0f);  // row sum of the bf16-rounded P: normalises O
+    f32x2 l2 = f2_pack(0.0f, 0.0f);  // row sum of exp2(x - m_used), two partial sums
     bool ok = true;
     for (int j = 0; j < nkv[t]; ++j) {
       ok = mbar_wait(bar(C::kBarSFull + t), j & 1, ctl, kSiteSFull);
@@ -332,18 +336,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         if (need) {
           const f32x2 a2 = f2_pack(alpha, alpha);
           l2 = f2_mul(l2, a2);
-          lb2 = f2_mul(lb2, a2);
           m_used = m_new;
         }
       }
 
       // P = exp2(x - m_used) -> bf16 into tensor memory over S.  Masked
       // entries are -inf and give exact zeros from MUFU; edge tiles use MUFU
-      // only.  O is normalised by the sum of the bf16-rounded P (the very
-      // weights the P V MMA uses: O is then an exact convex combination of V
-      // rows, and the rounding of a dominant weight, anything in [1, 2^8]
-      // under a stale reference max, cancels in O / l_bf); LSE keeps the
-      // unrounded sum.
+      // only.
       const f32x2 negm2 = f2_pack(-m_used, -m_used);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
@@ -359,10 +358,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             p0 = ex2_mufu(x0);
             p1 = ex2_mufu(x1);
           }
-          const uint32_t wp = pack_bf16x2(p0, p1);
-          w[e >> 1] = wp;
+          w[e >> 1] = pack_bf16x2(p0, p1);
           l2 = f2_add(l2, f2_pack(p0, p1));
-          lb2 = f2_add(lb2, f2_pack(__uint_as_float(wp << 16), __uint_as_float(wp & 0xFFFF0000u)));
         }
         tmem_st16(t_s + ch * 16, w);
       }
@@ -370,22 +367,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull + t));
     }
-    float l, l_bf;
+    float l;
     {
       float a, b;
       f2_unpack(l2, a, b);
       l = a + b;
-      f2_unpack(lb2, a, b);
-      l_bf = a + b;
     }
 
-    // epilogue: O / l_bf -> bf16, LSE = ln(2) * m_used + ln(l)
+    // epilogue: O / l -> bf16, LSE = ln(2) * m_used + ln(l)
     if (ok && nkv[t] > 0) {
       ok = mbar_wait(bar(C::kBarOFull + t), 0, ctl, kSiteOFull);
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        const float inv_l = 1.0f / l_bf;
+        const float inv_l = 1.0f / l;
         const bool in_range = qpos < p.N;
         __nv_bfloat16* orow =
             static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
