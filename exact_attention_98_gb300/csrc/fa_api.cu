@@ -30,10 +30,6 @@ struct KernelTiming {
 };
 KernelTiming g_timing;
 
-bool timing_on() {
-  std::lock_guard<std::mutex> lock(g_timing.mu);
-  return g_timing.enabled;
-}
 
 cudaError_t timing_record(int kernel, bool at_start, cudaStream_t s) {
   std::lock_guard<std::mutex> lock(g_timing.mu);

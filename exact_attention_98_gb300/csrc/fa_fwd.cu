@@ -56,7 +56,7 @@ struct FwdCfg {
   static constexpr int kMmaWarp = 9;
   static constexpr int kTileBytes = kBlockM * D * 2;  // one Q, K or V tile (bf16)
   static constexpr int kHalfBytes = kBlockM * 64 * 2;  // one 64-column swizzle block
-  static constexpr int kSlots = (D == 128) ? 4 : 6;
+  static constexpr int kSlots = (D == 128) ? 5 : 6;
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
@@ -275,7 +275,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const bool ragged = (p.N % kBlockN) != 0;
 
     float m_used = -INFINITY;  // running row max in log2 units (scores * c)
-    f32x2 l2 = f2_pack(0.0f, 0.0f);  // row sum of exp2(x - m_used), two partial sums
+    // row sum of exp2(x - m_used): four f32x2 accumulators (eight partial sums)
+    f32x2 l2[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
+                   f2_pack(0.0f, 0.0f)};
     bool ok = true;
     for (int j = 0; j < nkv[t]; ++j) {
       ok = mbar_wait(bar(C::kBarSFull + t), j & 1, ctl, kSiteSFull);
@@ -302,13 +304,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             if (kpos >= p.N || (p.causal && kpos > qpos)) r[ch][e] = __float_as_uint(-INFINITY);
           }
       }
-      // row max of the tile (raw scores; c > 0)
-      float mx = -INFINITY;
+      // row max of the tile (raw scores; c > 0), eight independent chains
+      float mxa[8];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch)
+      for (int a = 0; a < 8; ++a) mxa[a] = fmaxf(__uint_as_float(r[a >> 1][(a & 1) * 16]),
+                                                 __uint_as_float(r[a >> 1][(a & 1) * 16 + 1]));
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          mx = fmax3(mx, __uint_as_float(r[ch][e]), __uint_as_float(r[ch][e + 1]));
+      for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int e = 2; e < 16; e += 2)
+          mxa[a] = fmax3(mxa[a], __uint_as_float(r[a >> 1][(a & 1) * 16 + e]),
+                         __uint_as_float(r[a >> 1][(a & 1) * 16 + e + 1]));
+      const float mx = fmaxf(fmax3(mxa[0], mxa[1], mxa[2]),
+                             fmaxf(fmax3(mxa[3], mxa[4], mxa[5]), fmax3(mxa[6], mxa[7], mxa[0])));
       // Conditional rescale: move the reference max only when it grows by
       // more than the threshold (always on the first tile, m_used = -inf).
       const float m_new = fmaxf(m_used, mx * c);
@@ -335,7 +343,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         if (need) {
           const f32x2 a2 = f2_pack(alpha, alpha);
-          l2 = f2_mul(l2, a2);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) l2[a] = f2_mul(l2[a], a2);
           m_used = m_new;
         }
       }
@@ -359,7 +368,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             p1 = ex2_mufu(x1);
           }
           w[e >> 1] = pack_bf16x2(p0, p1);
-          l2 = f2_add(l2, f2_pack(p0, p1));
+          l2[(e >> 1) & 3] = f2_add(l2[(e >> 1) & 3], f2_pack(p0, p1));
         }
         tmem_st16(t_s + ch * 16, w);
       }
@@ -370,7 +379,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     float l;
     {
       float a, b;
-      f2_unpack(l2, a, b);
+      f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])), a, b);
       l = a + b;
     }
 
