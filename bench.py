@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: one JSON line per configuration of the "
+                         "fixed-token sweep (B*N = 32768, H = 16, N = 1k..32k, d = 64/128, both masks)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (for profiler runs)")
     return ap.parse_args()
@@ -367,8 +370,56 @@ def native_arm(args):
         torch.distributed.destroy_process_group()
 
 
+def sweep_arm(args):
+    """Kernel-level throughput over the fixed-token sweep: forward kernel and
+    backward main kernel, CUDA events recorded by the library around each
+    launch, median of `steps` launches after `warmup`, L2 flushed in between."""
+    import torch
+
+    from exact_attention_98_gb300 import fa
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    steps, warmup = max(3, args.steps), max(3, args.warmup)
+    for d in (128, 64):
+        for N in (1024, 2048, 4096, 8192, 16384, 32768):
+            B, H = 32768 // N, 16
+            scale = 1.0 / math.sqrt(d)
+            q, k, v, do = (t.to(dev) for t in attention_inputs(B, H, N, d, seed=0))
+            o = torch.empty_like(q)
+            lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+            ws = fa.workspace_for(q)
+            for causal in (False, True):
+                f_fwd, f_bwd = flops(B, H, N, d, causal)
+                fwd_ms, bwd_ms = [], []
+                for i in range(warmup + steps):
+                    flush.zero_()
+                    fa.fa_timing_enable(i >= warmup)
+                    fa.fa_fwd(q, k, v, o, lse, scale, causal)
+                    fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, ws)
+                    if i >= warmup:
+                        fwd_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
+                        bwd_ms.append(fa.fa_timing_last_ms(fa.KERNEL_BWD_MAIN))
+                fa.fa_timing_enable(False)
+                if fa.fa_last_device_status() != fa.FA_OK:
+                    raise RuntimeError("device status")
+                fm, bm = statistics.median(fwd_ms), statistics.median(bwd_ms)
+                print(json.dumps({"sweep": True, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                                  "fwd_ms": fm, "fwd_tflops": f_fwd / fm / 1e9,
+                                  "fwd_pct_of_2250": 100 * f_fwd / fm / 1e9 / PAGES_PEAK_TFLOPS,
+                                  "bwd_main_ms": bm, "bwd_main_tflops": f_bwd / bm / 1e9,
+                                  "bwd_pct_of_2250": 100 * f_bwd / bm / 1e9 / PAGES_PEAK_TFLOPS}),
+                      flush=True)
+            del q, k, v, do, o, lse, dq, dk, dv, ws
+
+
 def main():
     args = parse()
+    if args.sweep:
+        sweep_arm(args)
+        return
     if args.impl == "reference":
         reference_arm(args)
     else:

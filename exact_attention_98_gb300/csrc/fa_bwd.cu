@@ -217,15 +217,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         bar(C::kBarStFull + s), h * 64, q0, bh);
           }
         }
-        // LSE in log2 units and D for the 128 rows; rows past N get LSE = +inf
-        // (so P = 0) and D = 0.
+        // -LSE in log2 units and -D for the 128 rows (negated once here so the
+        // compute warps add them); rows past N get -LSE = -inf (so P = 0) and
+        // D = 0.
 #pragma unroll
         for (int r4 = 0; r4 < 4; ++r4) {
           const int r = lane * 4 + r4;
           const int q = q0 + r;
           const size_t gi = static_cast<size_t>(bh) * p.N + q;
-          lse_s[s * kBlockM + r] = (q < p.N) ? p.lse[gi] * p.log2e : INFINITY;
-          dsum_s[s * kBlockM + r] = (q < p.N) ? p.dsum[gi] : 0.0f;
+          lse_s[s * kBlockM + r] = (q < p.N) ? -(p.lse[gi] * p.log2e) : -INFINITY;
+          dsum_s[s * kBlockM + r] = (q < p.N) ? -p.dsum[gi] : 0.0f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::kBarStFull + s));
@@ -386,29 +387,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_ld32(lane_base + C::kColS + wg * 64 + 32, sr[1]);
       tmem_ld_wait(sr[0]);
       reg_fence(sr[1]);
+      const f32x2* neg_lse = reinterpret_cast<const f32x2*>(lse2 + wg * 64);
       float pf[64];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int col0 = wg * 64 + ch * 32;
+      for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + col0 + 4 * e4);
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][4 * e4]), __uint_as_float(sr[ch][4 * e4 + 1])),
-                           c2, f2_pack(-l4.x, -l4.y)),
+        for (int e2 = 0; e2 < 16; ++e2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
+                           c2, neg_lse[ch * 16 + e2]),
                     x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][4 * e4 + 2]), __uint_as_float(sr[ch][4 * e4 + 3])),
-                           c2, f2_pack(-l4.z, -l4.w)),
-                    x2, x3);
-          const float xs[4] = {x0, x1, x2, x3};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = col0 + 4 * e4 + e;
-            float pv = ex2_mufu(xs[e]);
-            if (!row_valid || (diag && col < kr)) pv = 0.0f;
-            pf[ch * 32 + 4 * e4 + e] = pv;
-          }
+          pf[ch * 32 + 2 * e2] = ex2_mufu(x0);
+          pf[ch * 32 + 2 * e2 + 1] = ex2_mufu(x1);
         }
+      if (diag) {  // uniform: only the diagonal tile pays for the mask
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (wg * 64 + e < kr) pf[e] = 0.0f;
+      }
+      if (!row_valid) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) pf[e] = 0.0f;
+      }
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]);
@@ -428,26 +430,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_ld32(lane_base + C::kColDP + wg * 64 + 32, dr[1]);
       tmem_ld_wait(dr[0]);
       reg_fence(dr[1]);
+      const f32x2* neg_d = reinterpret_cast<const f32x2*>(dsm + wg * 64);
       uint32_t dsw[32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        const int col0 = wg * 64 + ch * 32;
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(dsm + col0 + 4 * e4);
-          float a0, a1, a2, a3;
-          f2_unpack(f2_mul(f2_mul(f2_add(f2_pack(__uint_as_float(dr[ch][4 * e4]), __uint_as_float(dr[ch][4 * e4 + 1])),
-                                         f2_pack(-d4.x, -d4.y)),
-                                  f2_pack(pf[ch * 32 + 4 * e4], pf[ch * 32 + 4 * e4 + 1])),
+        for (int e2 = 0; e2 < 16; ++e2) {
+          float a0, a1;
+          f2_unpack(f2_mul(f2_mul(f2_add(f2_pack(__uint_as_float(dr[ch][2 * e2]),
+                                                 __uint_as_float(dr[ch][2 * e2 + 1])),
+                                         neg_d[ch * 16 + e2]),
+                                  f2_pack(pf[ch * 32 + 2 * e2], pf[ch * 32 + 2 * e2 + 1])),
                            scale2),
                     a0, a1);
-          f2_unpack(f2_mul(f2_mul(f2_add(f2_pack(__uint_as_float(dr[ch][4 * e4 + 2]), __uint_as_float(dr[ch][4 * e4 + 3])),
-                                         f2_pack(-d4.z, -d4.w)),
-                                  f2_pack(pf[ch * 32 + 4 * e4 + 2], pf[ch * 32 + 4 * e4 + 3])),
-                           scale2),
-                    a2, a3);
-          dsw[ch * 16 + 2 * e4] = pack_bf16x2(a0, a1);
-          dsw[ch * 16 + 2 * e4 + 1] = pack_bf16x2(a2, a3);
+          dsw[ch * 16 + e2] = pack_bf16x2(a0, a1);
         }
         uint32_t w[16];
 #pragma unroll
