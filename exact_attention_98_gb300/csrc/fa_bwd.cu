@@ -151,11 +151,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // Work item: key tile j of head bh; causal tiles with small j see the most
-  // query tiles, so they go first.
+  // Work item: key tile kt of head bh, head-major, so that the key tiles of
+  // one head run in the same wave and add into the same dQ rows while those
+  // are in L2; within a head the heaviest tile (causal: kt = 0) goes first.
   const int blk = blockIdx.x;
-  const int kt = blk / p.BH;
-  const int bh = blk % p.BH;
+  const int bh = blk / p.n_kblk;
+  const int kt = blk % p.n_kblk;
   const int k0 = kt * kBlockN;
   const int n_qtiles = (p.N + kBlockM - 1) / kBlockM;
   const int i_first = p.causal ? kt : 0;

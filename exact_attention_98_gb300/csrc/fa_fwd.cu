@@ -107,11 +107,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // Work item: heaviest query blocks first (causal blocks near the end of the
-  // sequence see the most keys).
+  // Work item: head-major, so that the query blocks of one head run in the
+  // same wave and share its K and V in L2; within a head the heaviest block
+  // (causal: the last one, which sees the most keys) goes first.
   const int blk = blockIdx.x;
-  const int qblk = p.n_qblk - 1 - blk / p.BH;
-  const int bh = blk % p.BH;
+  const int bh = blk / p.n_qblk;
+  const int qblk = p.n_qblk - 1 - blk % p.n_qblk;
   const int q0 = qblk * 2 * kBlockM;
   const int n_ktiles = (p.N + kBlockN - 1) / kBlockN;
   int nkv[2];
