@@ -107,12 +107,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
 
-  // Work item: head-major, so that the query blocks of one head run in the
-  // same wave and share its K and V in L2; within a head the heaviest block
-  // (causal: the last one, which sees the most keys) goes first.
+  // Work item.  Non-causal: head-major, so that the query blocks of one head
+  // run in the same wave and share its K and V in L2.  Causal: the heaviest
+  // blocks (the last query blocks, which see the most keys) of every head
+  // first, so that the short ones fill the tail.
   const int blk = blockIdx.x;
-  const int bh = blk / p.n_qblk;
-  const int qblk = p.n_qblk - 1 - blk % p.n_qblk;
+  const int bh = p.causal ? blk % p.BH : blk / p.n_qblk;
+  const int qblk = p.n_qblk - 1 - (p.causal ? blk / p.BH : blk % p.n_qblk);
   const int q0 = qblk * 2 * kBlockM;
   const int n_ktiles = (p.N + kBlockN - 1) / kBlockN;
   int nkv[2];
