@@ -1,6 +1,7 @@
-// Backward exact attention for sm_103a: key/value-stationary CTAs, all five
-// GEMMs of a tile on tcgen05 with their accumulators in tensor memory, dQ
-// added into an fp32 accumulator by bulk TMA reductions.
+// Backward exact attention for sm_103a: key/value-stationary CTAs paired in
+// two-CTA clusters, all five GEMMs of a tile on tcgen05 with their
+// accumulators in tensor memory, dQ added into an fp32 accumulator by bulk TMA
+// reductions of which each pair issues half as many as two lone CTAs would.
 //
 // The pages single out the backward pass as limited by shared-memory traffic
 // and by its reductions and atomic updates ("Pourquoi l'approche standard ne
@@ -19,10 +20,18 @@
 //   Each compute warpgroup owns 64 query columns of S^T and dP^T and packs
 //   its bf16 P^T / dS^T into the first 32 of them, so neither warpgroup
 //   overwrites fp32 values the other has not read yet.  dQ_i = dS K has the
-//   query as its row, so its A operand is dS in shared memory (at d = 128
-//   written over the dO_i tile once dV has consumed it; at d = 64 in its own
-//   buffer).  dQ_i lands in the dP^T columns, so draining it overlaps the next
-//   tile's S^T product and softmax.
+//   query as its row, so its A operand is dS in its own shared-memory buffer.
+//   dQ_i lands in the dP^T columns, so draining it overlaps the next tile's
+//   S^T product and softmax.
+//
+// Two-CTA clusters (the pages' 2-CTA mode: the pair cooperates so that the
+// backward's reductions cost half): key tiles 2m and 2m+1 of a head form a
+// cluster and walk the same query tiles.  Their dQ_i partials cover the same
+// 128 x d block, so instead of both adding all of it into global memory,
+// CTA r keeps columns [r d/2, (r+1) d/2): each CTA writes the half its peer
+// keeps into its own (then dead) dO_i buffer, reads the peer's copy of its own
+// half through distributed shared memory, adds, and issues one bulk
+// reduce-add of d/2 columns.  Global dQ reduction traffic halves.
 //
 // Per query tile i (MMA issue order):
 //   S^T = K Q_i^T ; [dQ_{i-1} drained] dP^T = V dO_i^T ;
@@ -34,12 +43,13 @@
 //   warps 0-7   compute: two warpgroups, thread = key row, warpgroup w takes
 //               query columns [64w, 64w + 64); at the end warpgroup 0 writes
 //               dV, warpgroup 1 dK
-//   warps 8-11  dQ drain: thread = query row; tensor memory -> registers (in
-//               two batches, after which the columns are free again) ->
-//               swizzled 16-column fp32 chunks in the Q_i and dO_i buffers
-//               (dead once dQ_i is computed: together exactly one fp32 dQ
-//               tile) -> TMA reduce-adds; the stage goes back to the loader
-//               when the TMA has read it
+//   warps 8-11  dQ drain: thread = query row; the peer's half of dQ_i from
+//               tensor memory into this CTA's dO_i buffer, its own half into
+//               registers (the columns are then free again); plus the peer's
+//               copy of that half, read across the cluster; the sum staged as
+//               swizzled 16-column fp32 chunks in the Q_i buffer -> TMA
+//               reduce-adds; the stage goes back to the loader when the TMA
+//               has read Q_i and the peer has read dO_i
 //   warp  12    loads: K, V once; Q_i, dO_i by TMA; LSE_i, D_i by plain loads
 //   warp  13    tensor-memory allocator; lane 0 issues every MMA
 //   warps 14-15 idle
@@ -74,17 +84,20 @@ struct BwdCfg {
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;      // kStages tiles
   static constexpr int kLseOff = kDOOff + kStages * kTileBytes;    // kStages x 128 fp32
   static constexpr int kDsumOff = kLseOff + kStages * kBlockM * 4;  // kStages x 128 fp32
-  static constexpr int kDsTileBytes = kBlockN * kBlockM * 2;  // dS is 128 x 128 for any d
-  // At d = 128 the dS tile reuses the dO_i buffer; at d = 64 that buffer is
-  // too small and dS gets one buffer per stage.
+  // dS (128 x 128 bf16 for any d): one buffer, 1024-byte aligned
   static constexpr int kDsOff = kDsumOff + kStages * kBlockM * 4;
-  static constexpr int kDsBytes = (D == 128) ? 0 : kStages * kDsTileBytes;
-  // dQ staging: d/16 chunks of 128 rows x 16 fp32 (64-byte swizzled rows),
-  // the first half in the stage's Q buffer, the second in its dO buffer.
+  static_assert(kDsOff % 1024 == 0, "dS buffer must be 1024-byte aligned");
+  static constexpr int kDsBytes = kBlockN * kBlockM * 2;
+  // dQ: this CTA keeps d/2 columns.  The sum is staged in the stage's Q
+  // buffer as d/32 chunks of 128 rows x 16 fp32 (64-byte swizzled rows); the
+  // peer's half goes out through the stage's dO buffer, row-major with
+  // 16-byte chunks swizzled by (row mod 8).
+  static constexpr int kHalf = D / 2;
   static constexpr int kDqCols = 16;
-  static constexpr int kDqChunks = D / kDqCols;
+  static constexpr int kDqChunks = kHalf / kDqCols;
   static constexpr int kDqChunkBytes = kBlockM * kDqCols * 4;
-  static_assert(kDqChunks / 2 * kDqChunkBytes == kTileBytes, "dQ staging must fill Q and dO");
+  static_assert(kDqChunks * kDqChunkBytes == kTileBytes, "dQ staging must fill the Q buffer");
+  static_assert(kBlockM * kHalf * 4 == kTileBytes, "the peer's half must fill the dO buffer");
   static constexpr int kBarOff = kDsOff + kDsBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarStFull = 1;
@@ -92,25 +105,26 @@ struct BwdCfg {
   static constexpr int kBarSFull = kBarStEmpty + kStages;
   static constexpr int kBarDPFull = kBarSFull + 1;
   static constexpr int kBarPFull = kBarDPFull + 1;
-  static constexpr int kBarDVDone = kBarPFull + 1;
-  static constexpr int kBarDSFull = kBarDVDone + 1;
+  static constexpr int kBarDSFull = kBarPFull + 1;
   static constexpr int kBarDQFull = kBarDSFull + 1;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarMmaDone = kBarDQEmpty + 1;
-  static constexpr int kNumBars = kBarMmaDone + 1;
+  static constexpr int kBarRxFull = kBarMmaDone + 1;  // peer's half for us is in its dO buffer
+  static constexpr int kBarRxDone = kBarRxFull + 1;   // peer has read our dO buffer
+  static constexpr int kNumBars = kBarRxDone + 1;
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAbortOff = kTmemSlotOff + 4;
-  static constexpr int kSmemBytes = kAbortOff + 4 + 1024;
+  static constexpr int kSmemUsed = kAbortOff + 4;
+  // d = 128 needs all but ~1 KB of the 227 KB: no room for alignment slack,
+  // so the kernel requires (and checks) a 1024-byte aligned dynamic segment.
+  static constexpr bool kNeedsAlignedBase = kSmemUsed + 1024 > 232448;
+  static constexpr int kSmemBytes = kNeedsAlignedBase ? kSmemUsed : kSmemUsed + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColDP = 128;  // dP^T, dS^T, then dQ
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
   static constexpr int kDrainBarrier = 1;  // named barrier of the drain warpgroup
-  // Shared-memory offset of stage s's dS tile.
-  static __device__ __forceinline__ int ds_off(int s) {
-    return (D == 128) ? kDOOff + s * kTileBytes : kDsOff + s * kDsTileBytes;
-  }
   // Tensor-memory column (relative to the S^T or dP^T region) of the packed
   // bf16 pair for query columns 16*kk.. of the tile: warpgroup kk/4 owns
   // columns [64*(kk/4), +64) and packs into the first 32.
@@ -126,19 +140,26 @@ enum : unsigned int {
   kSiteSFull = 0x204,
   kSiteDPFull = 0x205,
   kSitePFull = 0x206,
-  kSiteDVDone = 0x207,
+  kSiteRxFull = 0x207,
   kSiteDSFull = 0x208,
   kSiteDQFull = 0x209,
   kSiteDQEmpty = 0x20A,
   kSiteMmaDone = 0x20B,
+  kSiteRxDone = 0x20C,
+  kSiteAlign = 0x20D,
 };
 
 template <int D>
-__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
+  if (C::kNeedsAlignedBase && (raw_base & 1023u) != 0) {
+    // Both CTAs of the cluster see the same offset and leave here together.
+    if (threadIdx.x == 0) record_status(p.status, kStatusTimeout, kSiteAlign);
+    return;
+  }
   uint8_t* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
@@ -154,12 +175,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   // Work item: key tile kt of head bh, head-major, so that the key tiles of
   // one head run in the same wave and add into the same dQ rows while those
   // are in L2; within a head the heaviest tile (causal: kt = 0) goes first.
+  // p.n_kblk is even (a last, empty key tile pads an odd count); tiles 2m and
+  // 2m+1 form a cluster and both walk the query tiles from the pair's first
+  // one (causal: 2m), the odd tile's first query tile being fully masked.
   const int blk = blockIdx.x;
   const int bh = blk / p.n_kblk;
   const int kt = blk % p.n_kblk;
+  const uint32_t rank = cluster_rank();
+  const uint32_t peer = rank ^ 1u;
   const int k0 = kt * kBlockN;
   const int n_qtiles = (p.N + kBlockM - 1) / kBlockM;
-  const int i_first = p.causal ? kt : 0;
+  const int i_first = p.causal ? (kt & ~1) : 0;
   const int n_iter = n_qtiles - i_first;
 
   if (threadIdx.x == 0) {
@@ -172,16 +198,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(bar(C::kBarSFull), 1);
     mbar_init(bar(C::kBarDPFull), 1);
     mbar_init(bar(C::kBarPFull), 2 * kBlockM);
-    mbar_init(bar(C::kBarDVDone), 1);
     mbar_init(bar(C::kBarDSFull), 2 * kBlockM);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQEmpty), kBlockM);
     mbar_init(bar(C::kBarMmaDone), 1);
+    mbar_init(bar(C::kBarRxFull), kBlockM);
+    mbar_init(bar(C::kBarRxDone), kBlockM);
     fence_mbar_init();
   }
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  // Both CTAs' barriers are initialised before either arrives on the other's.
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -292,11 +320,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (!(ok = mbar_wait(bar(C::kBarPFull), it & 1, ctl, kSitePFull))) break;
         tc_fence_after();
         issue_tn(C::kColS, do_s, C::kColDV, it > 0);
-        mma_commit(bar(C::kBarDVDone));
         if (!(ok = mbar_wait(bar(C::kBarDSFull), it & 1, ctl, kSiteDSFull))) break;
         tc_fence_after();
         issue_tn(C::kColDP, q_s, C::kColDK, it > 0);
-        issue_dq(sbase + C::ds_off(s));
+        issue_dq(sbase + C::kDsOff);
         mma_commit(bar(C::kBarDQFull));  // the drain returns stage s to the loader
       }
       mma_commit(bar(C::kBarMmaDone));
@@ -309,52 +336,88 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int qr = quarter * 32 + lane;  // query row within the tile
     const bool leader = (warp == C::kDrainWarp0 && lane == 0);
     const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
+    const uint32_t peer_rx_full = cluster_map(bar(C::kBarRxFull), peer);
+    const uint32_t peer_rx_done = cluster_map(bar(C::kBarRxDone), peer);
+    constexpr int kRowBytes = C::kHalf * 4;  // one row of a half in the dO buffer
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % C::kStages;
       bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      // dK_i and dQ_i, the last readers of Q_i and dO_i, are complete: their
-      // buffers take the fp32 dQ tile.
-      auto chunk_base = [&](int ch) -> uint8_t* {
-        return smem + (ch < C::kDqChunks / 2 ? C::kQOff : C::kDOOff) + s * C::kTileBytes +
-               (ch % (C::kDqChunks / 2)) * C::kDqChunkBytes;
-      };
+      // dK_i and dQ_i, the last readers of Q_i and dO_i, are complete: the
+      // two buffers now carry dQ.
+      uint8_t* out_row = smem + C::kDOOff + s * C::kTileBytes + qr * kRowBytes;
+      uint32_t r[C::kDqChunks][16];
+      // the peer's half -> this CTA's dO buffer
 #pragma unroll
-      for (int b = 0; b < C::kDqChunks / 4; ++b) {
-        uint32_t r[4][16];
+      for (int c = 0; c < C::kDqChunks; ++c)
+        tmem_ld16(t_dq + peer * C::kHalf + c * C::kDqCols, r[c]);
+      tmem_ld_wait16(r[0]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld16(t_dq + (4 * b + c) * C::kDqCols, r[c]);
-        tmem_ld_wait16(r[0]);
-        reg_fence16(r[1]);
-        reg_fence16(r[2]);
-        reg_fence16(r[3]);
-        if (b == C::kDqChunks / 4 - 1) {
-          // dQ_i has left tensor memory: the MMA may write the columns again.
-          tc_fence_before();
-          mbar_arrive(bar(C::kBarDQEmpty));
+      for (int c = 1; c < C::kDqChunks; ++c) reg_fence16(r[c]);
+#pragma unroll
+      for (int c = 0; c < C::kDqChunks; ++c)
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int chunk = c * 4 + c4;
+          *reinterpret_cast<uint4*>(out_row + ((chunk ^ (qr & 7)) << 4)) =
+              make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]);
         }
-        // 128 rows x 64 bytes per chunk, 64-byte swizzle: 16-byte chunk index
-        // XOR ((row / 2) mod 4).
+      // this CTA's half -> registers; tensor memory is then free
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint8_t* row = chunk_base(4 * b + c) + qr * 64;
+      for (int c = 0; c < C::kDqChunks; ++c)
+        tmem_ld16(t_dq + rank * C::kHalf + c * C::kDqCols, r[c]);
+      tmem_ld_wait16(r[0]);
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            *reinterpret_cast<uint4*>(row + ((c4 ^ ((qr >> 1) & 3)) << 4)) =
-                make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]);
+      for (int c = 1; c < C::kDqChunks; ++c) reg_fence16(r[c]);
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarDQEmpty));
+      // Tell the peer its half is ready -- once it has read the previous
+      // one, so that the two barriers never run two phases apart.
+      if (it > 0) {
+        ok = mbar_wait_cluster(bar(C::kBarRxDone), (it - 1) & 1, ctl, kSiteRxDone);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      mbar_arrive_cluster(peer_rx_full);
+      ok = mbar_wait_cluster(bar(C::kBarRxFull), it & 1, ctl, kSiteRxFull);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // add the peer's copy of this CTA's half, read from the peer's dO buffer
+      const uint32_t in_row = cluster_map(sbase + C::kDOOff + s * C::kTileBytes, peer) + qr * kRowBytes;
+#pragma unroll
+      for (int c = 0; c < C::kDqChunks; ++c)
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int chunk = c * 4 + c4;
+          const uint4 v = ld_cluster_v4(in_row + ((chunk ^ (qr & 7)) << 4));
+          r[c][4 * c4] = __float_as_uint(__uint_as_float(r[c][4 * c4]) + __uint_as_float(v.x));
+          r[c][4 * c4 + 1] = __float_as_uint(__uint_as_float(r[c][4 * c4 + 1]) + __uint_as_float(v.y));
+          r[c][4 * c4 + 2] = __float_as_uint(__uint_as_float(r[c][4 * c4 + 2]) + __uint_as_float(v.z));
+          r[c][4 * c4 + 3] = __float_as_uint(__uint_as_float(r[c][4 * c4 + 3]) + __uint_as_float(v.w));
         }
+      mbar_arrive_cluster(peer_rx_done);
+      // the sum -> 128 rows x 64 bytes per chunk in the Q buffer, 64-byte
+      // swizzle: 16-byte chunk index XOR ((row / 2) mod 4)
+#pragma unroll
+      for (int c = 0; c < C::kDqChunks; ++c) {
+        uint8_t* row = smem + C::kQOff + s * C::kTileBytes + c * C::kDqChunkBytes + qr * 64;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          *reinterpret_cast<uint4*>(row + ((c4 ^ ((qr >> 1) & 3)) << 4)) =
+              make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]);
       }
       fence_proxy_async_smem();
       named_bar_sync(C::kDrainBarrier, kBlockM);
       if (leader) {
         const int q0 = (i_first + it) * kBlockM;
 #pragma unroll 1
-        for (int ch = 0; ch < C::kDqChunks; ++ch)
-          tma_reduce_add_3d(&p.tm_dq, smem_u32(chunk_base(ch)), ch * C::kDqCols, q0, bh);
+        for (int c = 0; c < C::kDqChunks; ++c)
+          tma_reduce_add_3d(&p.tm_dq, sbase + C::kQOff + s * C::kTileBytes + c * C::kDqChunkBytes,
+                            rank * C::kHalf + c * C::kDqCols, q0, bh);
         bulk_commit();
-        bulk_wait_read<0>();  // the TMA has read the staged tile: stage s is free
-        mbar_arrive(bar(C::kBarStEmpty + s));
+        bulk_wait_read<0>();  // the TMA has read the staged sum
+        // and the peer has read this CTA's dO buffer: stage s is free
+        if (mbar_wait_cluster(bar(C::kBarRxDone), it & 1, ctl, kSiteRxDone))
+          mbar_arrive(bar(C::kBarStEmpty + s));
       }
     }
     if (leader) bulk_wait<0>();
@@ -374,6 +437,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const int s = it % C::kStages;
       const int i = i_first + it;
       const bool diag = p.causal && i == kt;
+      const bool all_masked = p.causal && i < kt;  // the pair's first tile, seen by key tile 2m+1
       ok = mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull);
       ok = ok && mbar_wait(bar(C::kBarSFull), it & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -406,7 +470,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int e = 0; e < 64; ++e)
           if (wg * 64 + e < kr) pf[e] = 0.0f;
       }
-      if (!row_valid) {
+      if (!row_valid || all_masked) {
 #pragma unroll
         for (int e = 0; e < 64; ++e) pf[e] = 0.0f;
       }
@@ -421,8 +485,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull));
 
-      // dS = scale * P (dP - D): to tensor memory (for dK) and, once dV has
-      // finished reading dO_i, into shared memory (for dQ).
+      // dS = scale * P (dP - D): to tensor memory (for dK) and into shared
+      // memory (for dQ).
       ok = mbar_wait(bar(C::kBarDPFull), it & 1, ctl, kSiteDPFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -451,12 +515,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int e = 0; e < 16; ++e) w[e] = dsw[ch * 16 + e];
         tmem_st16(lane_base + C::kColDP + wg * 64 + ch * 16, w);
       }
-      ok = mbar_wait(bar(C::kBarDVDone), it & 1, ctl, kSiteDVDone);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       // dS tile laid out as an MN-major operand with 128B swizzle:
       // [query half][key row][64 queries], 16-byte chunk index XOR (key row
-      // mod 8).
-      uint8_t* ds_tile = smem + C::ds_off(s);
+      // mod 8).  The previous tile's dQ product, its last reader, completed
+      // before this tile's dP^T (issued after that dQ was drained).
+      uint8_t* ds_tile = smem + C::kDsOff;
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         const int q = wg * 64 + c8 * 8;  // first query of this 16-byte chunk
@@ -500,7 +563,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // Neither CTA leaves while its peer may still read its shared memory or
+  // arrive on its barriers.
+  cluster_sync();
   if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
