@@ -28,10 +28,11 @@
 // backward's reductions cost half): key tiles 2m and 2m+1 of a head form a
 // cluster and walk the same query tiles.  Their dQ_i partials cover the same
 // 128 x d block, so instead of both adding all of it into global memory,
-// CTA r keeps columns [r d/2, (r+1) d/2): each CTA writes the half its peer
-// keeps into its own (then dead) dO_i buffer, reads the peer's copy of its own
-// half through distributed shared memory, adds, and issues one bulk
-// reduce-add of d/2 columns.  Global dQ reduction traffic halves.
+// CTA r keeps columns [r d/2, (r+1) d/2): each CTA stages the half its peer
+// keeps in its own (then dead) Q_i buffer and pushes it with one bulk copy
+// into the peer's (then dead) dO_i buffer; the peer adds its own half there in
+// place and issues one bulk reduce-add of d/2 columns.  Global dQ reduction
+// traffic halves; the exchange is one 16/32 KB copy between the pair.
 //
 // Per query tile i (MMA issue order):
 //   S^T = K Q_i^T ; [dQ_{i-1} drained] dP^T = V dO_i^T ;
@@ -44,12 +45,13 @@
 //               query columns [64w, 64w + 64); at the end warpgroup 0 writes
 //               dV, warpgroup 1 dK
 //   warps 8-11  dQ drain: thread = query row; the peer's half of dQ_i from
-//               tensor memory into this CTA's dO_i buffer, its own half into
-//               registers (the columns are then free again); plus the peer's
-//               copy of that half, read across the cluster; the sum staged as
-//               swizzled 16-column fp32 chunks in the Q_i buffer -> TMA
-//               reduce-adds; the stage goes back to the loader when the TMA
-//               has read Q_i and the peer has read dO_i
+//               tensor memory into this CTA's Q_i buffer, its own half into
+//               registers (the columns are then free again); the peer's half
+//               for this CTA arrives in its dO_i buffer, the sum is written
+//               back in place -> TMA reduce-adds; the stage goes back to the
+//               loader when the TMA has read dO_i and the copy has read Q_i.
+//               Both buffers hold 16-column fp32 chunks of 128 rows x 64 B,
+//               64-byte swizzled (the TMA reduce layout).
 //   warp  12    loads: K, V once; Q_i, dO_i by TMA; LSE_i, D_i by plain loads
 //   warp  13    tensor-memory allocator; lane 0 issues every MMA
 //   warps 14-15 idle
@@ -88,16 +90,15 @@ struct BwdCfg {
   static constexpr int kDsOff = kDsumOff + kStages * kBlockM * 4;
   static_assert(kDsOff % 1024 == 0, "dS buffer must be 1024-byte aligned");
   static constexpr int kDsBytes = kBlockN * kBlockM * 2;
-  // dQ: this CTA keeps d/2 columns.  The sum is staged in the stage's Q
-  // buffer as d/32 chunks of 128 rows x 16 fp32 (64-byte swizzled rows); the
-  // peer's half goes out through the stage's dO buffer, row-major with
-  // 16-byte chunks swizzled by (row mod 8).
+  // dQ: this CTA keeps d/2 columns.  A half is d/32 chunks of 128 rows x 16
+  // fp32 (64-byte swizzled rows): outgoing in the stage's Q buffer, incoming
+  // (and then the sum) in its dO buffer.
   static constexpr int kHalf = D / 2;
   static constexpr int kDqCols = 16;
   static constexpr int kDqChunks = kHalf / kDqCols;
   static constexpr int kDqChunkBytes = kBlockM * kDqCols * 4;
-  static_assert(kDqChunks * kDqChunkBytes == kTileBytes, "dQ staging must fill the Q buffer");
-  static_assert(kBlockM * kHalf * 4 == kTileBytes, "the peer's half must fill the dO buffer");
+  static constexpr int kHalfBytes32 = kDqChunks * kDqChunkBytes;
+  static_assert(kHalfBytes32 == kTileBytes, "a dQ half must fill a Q / dO buffer");
   static constexpr int kBarOff = kDsOff + kDsBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarStFull = 1;
@@ -109,9 +110,10 @@ struct BwdCfg {
   static constexpr int kBarDQFull = kBarDSFull + 1;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarMmaDone = kBarDQEmpty + 1;
-  static constexpr int kBarRxFull = kBarMmaDone + 1;  // peer's half for us is in its dO buffer
-  static constexpr int kBarRxDone = kBarRxFull + 1;   // peer has read our dO buffer
-  static constexpr int kNumBars = kBarRxDone + 1;
+  static constexpr int kBarPeerReady = kBarMmaDone + 1;  // peer's dO buffer may receive
+  static constexpr int kBarRxFull = kBarPeerReady + 1;    // peer's half landed in our dO buffer
+  static constexpr int kBarTxDone = kBarRxFull + 1;       // our half landed in the peer's
+  static constexpr int kNumBars = kBarTxDone + 1;
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAbortOff = kTmemSlotOff + 4;
   static constexpr int kSmemUsed = kAbortOff + 4;
@@ -145,7 +147,8 @@ enum : unsigned int {
   kSiteDQFull = 0x209,
   kSiteDQEmpty = 0x20A,
   kSiteMmaDone = 0x20B,
-  kSiteRxDone = 0x20C,
+  kSiteTxDone = 0x20C,
+  kSitePeerReady = 0x20E,
   kSiteAlign = 0x20D,
 };
 
@@ -202,8 +205,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQEmpty), kBlockM);
     mbar_init(bar(C::kBarMmaDone), 1);
-    mbar_init(bar(C::kBarRxFull), kBlockM);
-    mbar_init(bar(C::kBarRxDone), kBlockM);
+    mbar_init(bar(C::kBarPeerReady), 1);
+    mbar_init(bar(C::kBarRxFull), 1);
+    mbar_init(bar(C::kBarTxDone), 1);
     fence_mbar_init();
   }
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -336,19 +340,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
     const int qr = quarter * 32 + lane;  // query row within the tile
     const bool leader = (warp == C::kDrainWarp0 && lane == 0);
     const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
+    const uint32_t peer_ready = cluster_map(bar(C::kBarPeerReady), peer);
     const uint32_t peer_rx_full = cluster_map(bar(C::kBarRxFull), peer);
-    const uint32_t peer_rx_done = cluster_map(bar(C::kBarRxDone), peer);
-    constexpr int kRowBytes = C::kHalf * 4;  // one row of a half in the dO buffer
+    const uint32_t peer_tx_done = cluster_map(bar(C::kBarTxDone), peer);
+    // 16-column chunk c of a half, row qr: 64 bytes, 16-byte pieces swizzled
+    auto piece = [&](uint32_t buf, int c, int c4) -> uint32_t {
+      return buf + c * C::kDqChunkBytes + qr * 64 + ((c4 ^ ((qr >> 1) & 3)) << 4);
+    };
+    int rx_armed = -1;  // iteration whose incoming copy was invited but not yet seen
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % C::kStages;
+      const uint32_t out_buf = sbase + C::kQOff + s * C::kTileBytes;  // the peer's half
+      const uint32_t in_buf = sbase + C::kDOOff + s * C::kTileBytes;   // ours, then the sum
       bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       // dK_i and dQ_i, the last readers of Q_i and dO_i, are complete: the
-      // two buffers now carry dQ.
-      uint8_t* out_row = smem + C::kDOOff + s * C::kTileBytes + qr * kRowBytes;
+      // two buffers now carry dQ.  Expect the peer's half, and tell the peer
+      // it may send it.
+      if (leader) {
+        mbar_arrive_expect_tx(bar(C::kBarRxFull), C::kHalfBytes32);
+        mbar_arrive_cluster(peer_ready);
+        rx_armed = it;
+      }
       uint32_t r[C::kDqChunks][16];
-      // the peer's half -> this CTA's dO buffer
+      // the peer's half -> Q buffer
 #pragma unroll
       for (int c = 0; c < C::kDqChunks; ++c)
         tmem_ld16(t_dq + peer * C::kHalf + c * C::kDqCols, r[c]);
@@ -358,11 +374,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
 #pragma unroll
       for (int c = 0; c < C::kDqChunks; ++c)
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int chunk = c * 4 + c4;
-          *reinterpret_cast<uint4*>(out_row + ((chunk ^ (qr & 7)) << 4)) =
+        for (int c4 = 0; c4 < 4; ++c4)
+          *reinterpret_cast<uint4*>(smem + (piece(out_buf, c, c4) - sbase)) =
               make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]);
-        }
       // this CTA's half -> registers; tensor memory is then free
 #pragma unroll
       for (int c = 0; c < C::kDqChunks; ++c)
@@ -372,55 +386,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
       for (int c = 1; c < C::kDqChunks; ++c) reg_fence16(r[c]);
       tc_fence_before();
       mbar_arrive(bar(C::kBarDQEmpty));
-      // Tell the peer its half is ready -- once it has read the previous
-      // one, so that the two barriers never run two phases apart.
-      if (it > 0) {
-        ok = mbar_wait_cluster(bar(C::kBarRxDone), (it - 1) & 1, ctl, kSiteRxDone);
-        if (!__all_sync(0xffffffffu, ok)) break;
+      fence_proxy_async_smem();
+      named_bar_sync(C::kDrainBarrier, kBlockM);
+      if (leader) {
+        // push the staged half once the peer's dO buffer is dead
+        ok = mbar_wait_cluster(bar(C::kBarPeerReady), it & 1, ctl, kSitePeerReady);
+        if (ok)
+          bulk_copy_to_peer(cluster_map(in_buf, peer), out_buf, C::kHalfBytes32, peer_rx_full);
       }
-      mbar_arrive_cluster(peer_rx_full);
-      ok = mbar_wait_cluster(bar(C::kBarRxFull), it & 1, ctl, kSiteRxFull);
+      ok = __all_sync(0xffffffffu, ok) && mbar_wait(bar(C::kBarRxFull), it & 1, ctl, kSiteRxFull);
       if (!__all_sync(0xffffffffu, ok)) break;
-      // add the peer's copy of this CTA's half, read from the peer's dO buffer
-      const uint32_t in_row = cluster_map(sbase + C::kDOOff + s * C::kTileBytes, peer) + qr * kRowBytes;
+      // The peer's half has landed in our dO buffer, so our own half, staged
+      // in the peer's Q buffer, has been read: say so.
+      if (leader) {
+        rx_armed = -1;
+        mbar_arrive_cluster(peer_tx_done);
+      }
+      // sum in place
 #pragma unroll
       for (int c = 0; c < C::kDqChunks; ++c)
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          const int chunk = c * 4 + c4;
-          const uint4 v = ld_cluster_v4(in_row + ((chunk ^ (qr & 7)) << 4));
-          r[c][4 * c4] = __float_as_uint(__uint_as_float(r[c][4 * c4]) + __uint_as_float(v.x));
-          r[c][4 * c4 + 1] = __float_as_uint(__uint_as_float(r[c][4 * c4 + 1]) + __uint_as_float(v.y));
-          r[c][4 * c4 + 2] = __float_as_uint(__uint_as_float(r[c][4 * c4 + 2]) + __uint_as_float(v.z));
-          r[c][4 * c4 + 3] = __float_as_uint(__uint_as_float(r[c][4 * c4 + 3]) + __uint_as_float(v.w));
+          uint4* ptr = reinterpret_cast<uint4*>(smem + (piece(in_buf, c, c4) - sbase));
+          const uint4 v = *ptr;
+          *ptr = make_uint4(__float_as_uint(__uint_as_float(r[c][4 * c4]) + __uint_as_float(v.x)),
+                            __float_as_uint(__uint_as_float(r[c][4 * c4 + 1]) + __uint_as_float(v.y)),
+                            __float_as_uint(__uint_as_float(r[c][4 * c4 + 2]) + __uint_as_float(v.z)),
+                            __float_as_uint(__uint_as_float(r[c][4 * c4 + 3]) + __uint_as_float(v.w)));
         }
-      mbar_arrive_cluster(peer_rx_done);
-      // the sum -> 128 rows x 64 bytes per chunk in the Q buffer, 64-byte
-      // swizzle: 16-byte chunk index XOR ((row / 2) mod 4)
-#pragma unroll
-      for (int c = 0; c < C::kDqChunks; ++c) {
-        uint8_t* row = smem + C::kQOff + s * C::kTileBytes + c * C::kDqChunkBytes + qr * 64;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          *reinterpret_cast<uint4*>(row + ((c4 ^ ((qr >> 1) & 3)) << 4)) =
-              make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]);
-      }
       fence_proxy_async_smem();
       named_bar_sync(C::kDrainBarrier, kBlockM);
       if (leader) {
         const int q0 = (i_first + it) * kBlockM;
 #pragma unroll 1
         for (int c = 0; c < C::kDqChunks; ++c)
-          tma_reduce_add_3d(&p.tm_dq, sbase + C::kQOff + s * C::kTileBytes + c * C::kDqChunkBytes,
-                            rank * C::kHalf + c * C::kDqCols, q0, bh);
+          tma_reduce_add_3d(&p.tm_dq, in_buf + c * C::kDqChunkBytes, rank * C::kHalf + c * C::kDqCols,
+                            q0, bh);
         bulk_commit();
-        bulk_wait_read<0>();  // the TMA has read the staged sum
-        // and the peer has read this CTA's dO buffer: stage s is free
-        if (mbar_wait_cluster(bar(C::kBarRxDone), it & 1, ctl, kSiteRxDone))
+        bulk_wait_read<0>();  // the TMA has read the sum in dO
+        // and our outgoing half in Q has been read by the copy: stage s is free
+        if (mbar_wait_cluster(bar(C::kBarTxDone), it & 1, ctl, kSiteTxDone))
           mbar_arrive(bar(C::kBarStEmpty + s));
       }
     }
-    if (leader) bulk_wait<0>();
+    if (leader) {
+      bulk_wait<0>();
+      // give-up path: a copy this CTA invited may still be landing in its
+      // shared memory; let it finish before the CTA can leave
+      if (rx_armed >= 0) mbar_wait_drain(bar(C::kBarRxFull), rx_armed & 1);
+    }
   } else {
     regs_inc<C::kComputeRegs>();
     // ------------------------------------------------------------- compute

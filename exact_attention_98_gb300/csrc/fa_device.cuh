@@ -225,6 +225,18 @@ __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t cluster_addr) {
   return v;
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into the
+// shared memory of a CTA of the cluster, completing `bytes` transactions on
+// that CTA's mbarrier.  dst and bar are shared::cluster addresses.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // All threads of all CTAs of the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
