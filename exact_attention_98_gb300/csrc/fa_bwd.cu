@@ -28,11 +28,11 @@
 // backward's reductions cost half): key tiles 2m and 2m+1 of a head form a
 // cluster and walk the same query tiles.  Their dQ_i partials cover the same
 // 128 x d block, so instead of both adding all of it into global memory,
-// CTA r keeps columns [r d/2, (r+1) d/2): each CTA stages the half its peer
-// keeps in its own (then dead) Q_i buffer and pushes it with one bulk copy
-// into the peer's (then dead) dO_i buffer; the peer adds its own half there in
-// place and issues one bulk reduce-add of d/2 columns.  Global dQ reduction
-// traffic halves; the exchange is one 16/32 KB copy between the pair.
+// CTA r keeps columns [r d/2, (r+1) d/2): each CTA stores the half its peer
+// keeps straight into the peer's (then dead) dO_i buffer with distributed
+// shared-memory stores; the peer adds its own half there in place and issues
+// one bulk reduce-add of d/2 columns.  Global dQ reduction traffic halves,
+// while each CTA's shared memory carries what it did with one CTA alone.
 //
 // Per query tile i (MMA issue order):
 //   S^T = K Q_i^T ; [dQ_{i-1} drained] dP^T = V dO_i^T ;
@@ -45,13 +45,13 @@
 //               query columns [64w, 64w + 64); at the end warpgroup 0 writes
 //               dV, warpgroup 1 dK
 //   warps 8-11  dQ drain: thread = query row; the peer's half of dQ_i from
-//               tensor memory into this CTA's Q_i buffer, its own half into
+//               tensor memory into the peer's dO_i buffer, its own half into
 //               registers (the columns are then free again); the peer's half
-//               for this CTA arrives in its dO_i buffer, the sum is written
-//               back in place -> TMA reduce-adds; the stage goes back to the
-//               loader when the TMA has read dO_i and the copy has read Q_i.
-//               Both buffers hold 16-column fp32 chunks of 128 rows x 64 B,
-//               64-byte swizzled (the TMA reduce layout).
+//               for this CTA arrives in its own dO_i buffer, the sum is
+//               written back in place (16-column fp32 chunks of 128 rows x
+//               64 B, 64-byte swizzled: the TMA reduce layout) -> TMA
+//               reduce-adds; the stage goes back to the loader when the TMA
+//               has read it.
 //   warp  12    loads: K, V once; Q_i, dO_i by TMA; LSE_i, D_i by plain loads
 //   warp  13    tensor-memory allocator; lane 0 issues every MMA
 //   warps 14-15 idle
@@ -91,8 +91,8 @@ struct BwdCfg {
   static_assert(kDsOff % 1024 == 0, "dS buffer must be 1024-byte aligned");
   static constexpr int kDsBytes = kBlockN * kBlockM * 2;
   // dQ: this CTA keeps d/2 columns.  A half is d/32 chunks of 128 rows x 16
-  // fp32 (64-byte swizzled rows): outgoing in the stage's Q buffer, incoming
-  // (and then the sum) in its dO buffer.
+  // fp32 (64-byte swizzled rows); the peer's half for this CTA, and then the
+  // sum, live in the stage's dO buffer.
   static constexpr int kHalf = D / 2;
   static constexpr int kDqCols = 16;
   static constexpr int kDqChunks = kHalf / kDqCols;
@@ -111,9 +111,8 @@ struct BwdCfg {
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarMmaDone = kBarDQEmpty + 1;
   static constexpr int kBarPeerReady = kBarMmaDone + 1;  // peer's dO buffer may receive
-  static constexpr int kBarRxFull = kBarPeerReady + 1;    // peer's half landed in our dO buffer
-  static constexpr int kBarTxDone = kBarRxFull + 1;       // our half landed in the peer's
-  static constexpr int kNumBars = kBarTxDone + 1;
+  static constexpr int kBarRxFull = kBarPeerReady + 1;    // peer's half is in our dO buffer
+  static constexpr int kNumBars = kBarRxFull + 1;
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAbortOff = kTmemSlotOff + 4;
   static constexpr int kSmemUsed = kAbortOff + 4;
@@ -147,7 +146,6 @@ enum : unsigned int {
   kSiteDQFull = 0x209,
   kSiteDQEmpty = 0x20A,
   kSiteMmaDone = 0x20B,
-  kSiteTxDone = 0x20C,
   kSitePeerReady = 0x20E,
   kSiteAlign = 0x20D,
 };
@@ -206,8 +204,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
     mbar_init(bar(C::kBarDQEmpty), kBlockM);
     mbar_init(bar(C::kBarMmaDone), 1);
     mbar_init(bar(C::kBarPeerReady), 1);
-    mbar_init(bar(C::kBarRxFull), 1);
-    mbar_init(bar(C::kBarTxDone), 1);
+    mbar_init(bar(C::kBarRxFull), kBlockM);
     fence_mbar_init();
   }
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -342,41 +339,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
     const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
     const uint32_t peer_ready = cluster_map(bar(C::kBarPeerReady), peer);
     const uint32_t peer_rx_full = cluster_map(bar(C::kBarRxFull), peer);
-    const uint32_t peer_tx_done = cluster_map(bar(C::kBarTxDone), peer);
     // 16-column chunk c of a half, row qr: 64 bytes, 16-byte pieces swizzled
-    auto piece = [&](uint32_t buf, int c, int c4) -> uint32_t {
-      return buf + c * C::kDqChunkBytes + qr * 64 + ((c4 ^ ((qr >> 1) & 3)) << 4);
+    auto piece = [&](int c, int c4) -> uint32_t {
+      return c * C::kDqChunkBytes + qr * 64 + ((c4 ^ ((qr >> 1) & 3)) << 4);
     };
-    int rx_armed = -1;  // iteration whose incoming copy was invited but not yet seen
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % C::kStages;
-      const uint32_t out_buf = sbase + C::kQOff + s * C::kTileBytes;  // the peer's half
-      const uint32_t in_buf = sbase + C::kDOOff + s * C::kTileBytes;   // ours, then the sum
+      const uint32_t buf = C::kDOOff + s * C::kTileBytes;  // offset of the dO buffer
       bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      // dK_i and dQ_i, the last readers of Q_i and dO_i, are complete: the
-      // two buffers now carry dQ.  Expect the peer's half, and tell the peer
-      // it may send it.
-      if (leader) {
-        mbar_arrive_expect_tx(bar(C::kBarRxFull), C::kHalfBytes32);
-        mbar_arrive_cluster(peer_ready);
-        rx_armed = it;
-      }
+      // dK_i and dQ_i, the last readers of Q_i and dO_i, are complete: our
+      // dO buffer may take the peer's half.
+      if (leader) mbar_arrive_cluster(peer_ready);
       uint32_t r[C::kDqChunks][16];
-      // the peer's half -> Q buffer
+      // the peer's half -> the peer's dO buffer
 #pragma unroll
       for (int c = 0; c < C::kDqChunks; ++c)
         tmem_ld16(t_dq + peer * C::kHalf + c * C::kDqCols, r[c]);
       tmem_ld_wait16(r[0]);
 #pragma unroll
       for (int c = 1; c < C::kDqChunks; ++c) reg_fence16(r[c]);
+      ok = mbar_wait_cluster(bar(C::kBarPeerReady), it & 1, ctl, kSitePeerReady);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const uint32_t peer_buf = cluster_map(sbase + buf, peer);
 #pragma unroll
       for (int c = 0; c < C::kDqChunks; ++c)
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4)
-          *reinterpret_cast<uint4*>(smem + (piece(out_buf, c, c4) - sbase)) =
-              make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]);
+          st_cluster_v4(peer_buf + piece(c, c4),
+                        make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]));
+      mbar_arrive_cluster(peer_rx_full);
       // this CTA's half -> registers; tensor memory is then free
 #pragma unroll
       for (int c = 0; c < C::kDqChunks; ++c)
@@ -386,28 +379,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
       for (int c = 1; c < C::kDqChunks; ++c) reg_fence16(r[c]);
       tc_fence_before();
       mbar_arrive(bar(C::kBarDQEmpty));
-      fence_proxy_async_smem();
-      named_bar_sync(C::kDrainBarrier, kBlockM);
-      if (leader) {
-        // push the staged half once the peer's dO buffer is dead
-        ok = mbar_wait_cluster(bar(C::kBarPeerReady), it & 1, ctl, kSitePeerReady);
-        if (ok)
-          bulk_copy_to_peer(cluster_map(in_buf, peer), out_buf, C::kHalfBytes32, peer_rx_full);
-      }
-      ok = __all_sync(0xffffffffu, ok) && mbar_wait(bar(C::kBarRxFull), it & 1, ctl, kSiteRxFull);
+      // The peer's half is in our dO buffer: the sum, in place.  (Neither
+      // barrier can run two phases ahead: the peer's next readiness follows
+      // its wait for our stores, and its next stores follow our readiness.)
+      ok = mbar_wait_cluster(bar(C::kBarRxFull), it & 1, ctl, kSiteRxFull);
       if (!__all_sync(0xffffffffu, ok)) break;
-      // The peer's half has landed in our dO buffer, so our own half, staged
-      // in the peer's Q buffer, has been read: say so.
-      if (leader) {
-        rx_armed = -1;
-        mbar_arrive_cluster(peer_tx_done);
-      }
-      // sum in place
 #pragma unroll
       for (int c = 0; c < C::kDqChunks; ++c)
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
-          uint4* ptr = reinterpret_cast<uint4*>(smem + (piece(in_buf, c, c4) - sbase));
+          uint4* ptr = reinterpret_cast<uint4*>(smem + buf + piece(c, c4));
           const uint4 v = *ptr;
           *ptr = make_uint4(__float_as_uint(__uint_as_float(r[c][4 * c4]) + __uint_as_float(v.x)),
                             __float_as_uint(__uint_as_float(r[c][4 * c4 + 1]) + __uint_as_float(v.y)),
@@ -420,21 +401,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
         const int q0 = (i_first + it) * kBlockM;
 #pragma unroll 1
         for (int c = 0; c < C::kDqChunks; ++c)
-          tma_reduce_add_3d(&p.tm_dq, in_buf + c * C::kDqChunkBytes, rank * C::kHalf + c * C::kDqCols,
-                            q0, bh);
+          tma_reduce_add_3d(&p.tm_dq, sbase + buf + c * C::kDqChunkBytes,
+                            rank * C::kHalf + c * C::kDqCols, q0, bh);
         bulk_commit();
-        bulk_wait_read<0>();  // the TMA has read the sum in dO
-        // and our outgoing half in Q has been read by the copy: stage s is free
-        if (mbar_wait_cluster(bar(C::kBarTxDone), it & 1, ctl, kSiteTxDone))
-          mbar_arrive(bar(C::kBarStEmpty + s));
+        bulk_wait_read<0>();  // the TMA has read the sum: stage s is free
+        mbar_arrive(bar(C::kBarStEmpty + s));
       }
     }
-    if (leader) {
-      bulk_wait<0>();
-      // give-up path: a copy this CTA invited may still be landing in its
-      // shared memory; let it finish before the CTA can leave
-      if (rx_armed >= 0) mbar_wait_drain(bar(C::kBarRxFull), rx_armed & 1);
-    }
+    if (leader) bulk_wait<0>();
   } else {
     regs_inc<C::kComputeRegs>();
     // ------------------------------------------------------------- compute
