@@ -288,8 +288,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (!p.status) return FA_ERR_CUDA;
   p.N = N;
   p.BH = BH;
-  // key tiles go in two-CTA clusters: an odd count gets one empty tile
-  p.n_kblk = (((N + kBlockN - 1) / kBlockN) + 1) & ~1;
+  p.n_kblk = (N + kBlockN - 1) / kBlockN;
   p.causal = causal;
   p.c = scale * 1.4426950408889634f;
   p.scale = scale;

@@ -1,7 +1,6 @@
-// Backward exact attention for sm_103a: key/value-stationary CTAs paired in
-// two-CTA clusters, all five GEMMs of a tile on tcgen05 with their
-// accumulators in tensor memory, dQ added into an fp32 accumulator by bulk TMA
-// reductions of which each pair issues half as many as two lone CTAs would.
+// Backward exact attention for sm_103a: key/value-stationary CTAs, all five
+// GEMMs of a tile on tcgen05 with their accumulators in tensor memory, dQ
+// added into an fp32 accumulator by bulk TMA reductions.
 //
 // The pages single out the backward pass as limited by shared-memory traffic
 // and by its reductions and atomic updates ("Pourquoi l'approche standard ne
@@ -20,19 +19,10 @@
 //   Each compute warpgroup owns 64 query columns of S^T and dP^T and packs
 //   its bf16 P^T / dS^T into the first 32 of them, so neither warpgroup
 //   overwrites fp32 values the other has not read yet.  dQ_i = dS K has the
-//   query as its row, so its A operand is dS in its own shared-memory buffer.
-//   dQ_i lands in the dP^T columns, so draining it overlaps the next tile's
-//   S^T product and softmax.
-//
-// Two-CTA clusters (the pages' 2-CTA mode: the pair cooperates so that the
-// backward's reductions cost half): key tiles 2m and 2m+1 of a head form a
-// cluster and walk the same query tiles.  Their dQ_i partials cover the same
-// 128 x d block, so instead of both adding all of it into global memory,
-// CTA r keeps columns [r d/2, (r+1) d/2): each CTA stores the half its peer
-// keeps straight into the peer's (then dead) dO_i buffer with distributed
-// shared-memory stores; the peer adds its own half there in place and issues
-// one bulk reduce-add of d/2 columns.  Global dQ reduction traffic halves,
-// while each CTA's shared memory carries what it did with one CTA alone.
+//   query as its row, so its A operand is dS in shared memory (at d = 128
+//   written over the dO_i tile once dV has consumed it; at d = 64 in its own
+//   buffer).  dQ_i lands in the dP^T columns, so draining it overlaps the next
+//   tile's S^T product and softmax.
 //
 // Per query tile i (MMA issue order):
 //   S^T = K Q_i^T ; [dQ_{i-1} drained] dP^T = V dO_i^T ;
@@ -44,14 +34,12 @@
 //   warps 0-7   compute: two warpgroups, thread = key row, warpgroup w takes
 //               query columns [64w, 64w + 64); at the end warpgroup 0 writes
 //               dV, warpgroup 1 dK
-//   warps 8-11  dQ drain: thread = query row; the peer's half of dQ_i from
-//               tensor memory into the peer's dO_i buffer, its own half into
-//               registers (the columns are then free again); the peer's half
-//               for this CTA arrives in its own dO_i buffer, the sum is
-//               written back in place (16-column fp32 chunks of 128 rows x
-//               64 B, 64-byte swizzled: the TMA reduce layout) -> TMA
-//               reduce-adds; the stage goes back to the loader when the TMA
-//               has read it.
+//   warps 8-11  dQ drain: thread = query row; tensor memory -> registers (in
+//               two batches, after which the columns are free again) ->
+//               swizzled 16-column fp32 chunks in the Q_i and dO_i buffers
+//               (dead once dQ_i is computed: together exactly one fp32 dQ
+//               tile) -> TMA reduce-adds; the stage goes back to the loader
+//               when the TMA has read it
 //   warp  12    loads: K, V once; Q_i, dO_i by TMA; LSE_i, D_i by plain loads
 //   warp  13    tensor-memory allocator; lane 0 issues every MMA
 //   warps 14-15 idle
@@ -86,19 +74,17 @@ struct BwdCfg {
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;      // kStages tiles
   static constexpr int kLseOff = kDOOff + kStages * kTileBytes;    // kStages x 128 fp32
   static constexpr int kDsumOff = kLseOff + kStages * kBlockM * 4;  // kStages x 128 fp32
-  // dS (128 x 128 bf16 for any d): one buffer, 1024-byte aligned
+  static constexpr int kDsTileBytes = kBlockN * kBlockM * 2;  // dS is 128 x 128 for any d
+  // At d = 128 the dS tile reuses the dO_i buffer; at d = 64 that buffer is
+  // too small and dS gets one buffer per stage.
   static constexpr int kDsOff = kDsumOff + kStages * kBlockM * 4;
-  static_assert(kDsOff % 1024 == 0, "dS buffer must be 1024-byte aligned");
-  static constexpr int kDsBytes = kBlockN * kBlockM * 2;
-  // dQ: this CTA keeps d/2 columns.  A half is d/32 chunks of 128 rows x 16
-  // fp32 (64-byte swizzled rows); the peer's half for this CTA, and then the
-  // sum, live in the stage's dO buffer.
-  static constexpr int kHalf = D / 2;
+  static constexpr int kDsBytes = (D == 128) ? 0 : kStages * kDsTileBytes;
+  // dQ staging: d/16 chunks of 128 rows x 16 fp32 (64-byte swizzled rows),
+  // the first half in the stage's Q buffer, the second in its dO buffer.
   static constexpr int kDqCols = 16;
-  static constexpr int kDqChunks = kHalf / kDqCols;
+  static constexpr int kDqChunks = D / kDqCols;
   static constexpr int kDqChunkBytes = kBlockM * kDqCols * 4;
-  static constexpr int kHalfBytes32 = kDqChunks * kDqChunkBytes;
-  static_assert(kHalfBytes32 == kTileBytes, "a dQ half must fill a Q / dO buffer");
+  static_assert(kDqChunks / 2 * kDqChunkBytes == kTileBytes, "dQ staging must fill Q and dO");
   static constexpr int kBarOff = kDsOff + kDsBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarStFull = 1;
@@ -106,26 +92,25 @@ struct BwdCfg {
   static constexpr int kBarSFull = kBarStEmpty + kStages;
   static constexpr int kBarDPFull = kBarSFull + 1;
   static constexpr int kBarPFull = kBarDPFull + 1;
-  static constexpr int kBarDSFull = kBarPFull + 1;
+  static constexpr int kBarDVDone = kBarPFull + 1;
+  static constexpr int kBarDSFull = kBarDVDone + 1;
   static constexpr int kBarDQFull = kBarDSFull + 1;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarMmaDone = kBarDQEmpty + 1;
-  static constexpr int kBarPeerReady = kBarMmaDone + 1;  // peer's dO buffer may receive
-  static constexpr int kBarRxFull = kBarPeerReady + 1;    // peer's half is in our dO buffer
-  static constexpr int kNumBars = kBarRxFull + 1;
+  static constexpr int kNumBars = kBarMmaDone + 1;
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAbortOff = kTmemSlotOff + 4;
-  static constexpr int kSmemUsed = kAbortOff + 4;
-  // d = 128 needs all but ~1 KB of the 227 KB: no room for alignment slack,
-  // so the kernel requires (and checks) a 1024-byte aligned dynamic segment.
-  static constexpr bool kNeedsAlignedBase = kSmemUsed + 1024 > 232448;
-  static constexpr int kSmemBytes = kNeedsAlignedBase ? kSmemUsed : kSmemUsed + 1024;
+  static constexpr int kSmemBytes = kAbortOff + 4 + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColDP = 128;  // dP^T, dS^T, then dQ
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
   static constexpr int kDrainBarrier = 1;  // named barrier of the drain warpgroup
+  // Shared-memory offset of stage s's dS tile.
+  static __device__ __forceinline__ int ds_off(int s) {
+    return (D == 128) ? kDOOff + s * kTileBytes : kDsOff + s * kDsTileBytes;
+  }
   // Tensor-memory column (relative to the S^T or dP^T region) of the packed
   // bf16 pair for query columns 16*kk.. of the tile: warpgroup kk/4 owns
   // columns [64*(kk/4), +64) and packs into the first 32.
@@ -141,26 +126,19 @@ enum : unsigned int {
   kSiteSFull = 0x204,
   kSiteDPFull = 0x205,
   kSitePFull = 0x206,
-  kSiteRxFull = 0x207,
+  kSiteDVDone = 0x207,
   kSiteDSFull = 0x208,
   kSiteDQFull = 0x209,
   kSiteDQEmpty = 0x20A,
   kSiteMmaDone = 0x20B,
-  kSitePeerReady = 0x20E,
-  kSiteAlign = 0x20D,
 };
 
 template <int D>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
-  if (C::kNeedsAlignedBase && (raw_base & 1023u) != 0) {
-    // Both CTAs of the cluster see the same offset and leave here together.
-    if (threadIdx.x == 0) record_status(p.status, kStatusTimeout, kSiteAlign);
-    return;
-  }
   uint8_t* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
@@ -176,17 +154,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
   // Work item: key tile kt of head bh, head-major, so that the key tiles of
   // one head run in the same wave and add into the same dQ rows while those
   // are in L2; within a head the heaviest tile (causal: kt = 0) goes first.
-  // p.n_kblk is even (a last, empty key tile pads an odd count); tiles 2m and
-  // 2m+1 form a cluster and both walk the query tiles from the pair's first
-  // one (causal: 2m), the odd tile's first query tile being fully masked.
   const int blk = blockIdx.x;
   const int bh = blk / p.n_kblk;
   const int kt = blk % p.n_kblk;
-  const uint32_t rank = cluster_rank();
-  const uint32_t peer = rank ^ 1u;
   const int k0 = kt * kBlockN;
   const int n_qtiles = (p.N + kBlockM - 1) / kBlockM;
-  const int i_first = p.causal ? (kt & ~1) : 0;
+  const int i_first = p.causal ? kt : 0;
   const int n_iter = n_qtiles - i_first;
 
   if (threadIdx.x == 0) {
@@ -199,18 +172,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
     mbar_init(bar(C::kBarSFull), 1);
     mbar_init(bar(C::kBarDPFull), 1);
     mbar_init(bar(C::kBarPFull), 2 * kBlockM);
+    mbar_init(bar(C::kBarDVDone), 1);
     mbar_init(bar(C::kBarDSFull), 2 * kBlockM);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQEmpty), kBlockM);
     mbar_init(bar(C::kBarMmaDone), 1);
-    mbar_init(bar(C::kBarPeerReady), 1);
-    mbar_init(bar(C::kBarRxFull), kBlockM);
     fence_mbar_init();
   }
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
-  // Both CTAs' barriers are initialised before either arrives on the other's.
-  cluster_sync();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -321,10 +292,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
         if (!(ok = mbar_wait(bar(C::kBarPFull), it & 1, ctl, kSitePFull))) break;
         tc_fence_after();
         issue_tn(C::kColS, do_s, C::kColDV, it > 0);
+        mma_commit(bar(C::kBarDVDone));
         if (!(ok = mbar_wait(bar(C::kBarDSFull), it & 1, ctl, kSiteDSFull))) break;
         tc_fence_after();
         issue_tn(C::kColDP, q_s, C::kColDK, it > 0);
-        issue_dq(sbase + C::kDsOff);
+        issue_dq(sbase + C::ds_off(s));
         mma_commit(bar(C::kBarDQFull));  // the drain returns stage s to the loader
       }
       mma_commit(bar(C::kBarMmaDone));
@@ -337,74 +309,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
     const int qr = quarter * 32 + lane;  // query row within the tile
     const bool leader = (warp == C::kDrainWarp0 && lane == 0);
     const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
-    const uint32_t peer_ready = cluster_map(bar(C::kBarPeerReady), peer);
-    const uint32_t peer_rx_full = cluster_map(bar(C::kBarRxFull), peer);
-    // 16-column chunk c of a half, row qr: 64 bytes, 16-byte pieces swizzled
-    auto piece = [&](int c, int c4) -> uint32_t {
-      return c * C::kDqChunkBytes + qr * 64 + ((c4 ^ ((qr >> 1) & 3)) << 4);
-    };
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % C::kStages;
-      const uint32_t buf = C::kDOOff + s * C::kTileBytes;  // offset of the dO buffer
       bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      // dK_i and dQ_i, the last readers of Q_i and dO_i, are complete: our
-      // dO buffer may take the peer's half.
-      if (leader) mbar_arrive_cluster(peer_ready);
-      uint32_t r[C::kDqChunks][16];
-      // the peer's half -> the peer's dO buffer
+      // dK_i and dQ_i, the last readers of Q_i and dO_i, are complete: their
+      // buffers take the fp32 dQ tile.
+      auto chunk_base = [&](int ch) -> uint8_t* {
+        return smem + (ch < C::kDqChunks / 2 ? C::kQOff : C::kDOOff) + s * C::kTileBytes +
+               (ch % (C::kDqChunks / 2)) * C::kDqChunkBytes;
+      };
 #pragma unroll
-      for (int c = 0; c < C::kDqChunks; ++c)
-        tmem_ld16(t_dq + peer * C::kHalf + c * C::kDqCols, r[c]);
-      tmem_ld_wait16(r[0]);
+      for (int b = 0; b < C::kDqChunks / 4; ++b) {
+        uint32_t r[4][16];
 #pragma unroll
-      for (int c = 1; c < C::kDqChunks; ++c) reg_fence16(r[c]);
-      ok = mbar_wait_cluster(bar(C::kBarPeerReady), it & 1, ctl, kSitePeerReady);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      const uint32_t peer_buf = cluster_map(sbase + buf, peer);
-#pragma unroll
-      for (int c = 0; c < C::kDqChunks; ++c)
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          st_cluster_v4(peer_buf + piece(c, c4),
-                        make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]));
-      mbar_arrive_cluster(peer_rx_full);
-      // this CTA's half -> registers; tensor memory is then free
-#pragma unroll
-      for (int c = 0; c < C::kDqChunks; ++c)
-        tmem_ld16(t_dq + rank * C::kHalf + c * C::kDqCols, r[c]);
-      tmem_ld_wait16(r[0]);
-#pragma unroll
-      for (int c = 1; c < C::kDqChunks; ++c) reg_fence16(r[c]);
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarDQEmpty));
-      // The peer's half is in our dO buffer: the sum, in place.  (Neither
-      // barrier can run two phases ahead: the peer's next readiness follows
-      // its wait for our stores, and its next stores follow our readiness.)
-      ok = mbar_wait_cluster(bar(C::kBarRxFull), it & 1, ctl, kSiteRxFull);
-      if (!__all_sync(0xffffffffu, ok)) break;
-#pragma unroll
-      for (int c = 0; c < C::kDqChunks; ++c)
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint4* ptr = reinterpret_cast<uint4*>(smem + buf + piece(c, c4));
-          const uint4 v = *ptr;
-          *ptr = make_uint4(__float_as_uint(__uint_as_float(r[c][4 * c4]) + __uint_as_float(v.x)),
-                            __float_as_uint(__uint_as_float(r[c][4 * c4 + 1]) + __uint_as_float(v.y)),
-                            __float_as_uint(__uint_as_float(r[c][4 * c4 + 2]) + __uint_as_float(v.z)),
-                            __float_as_uint(__uint_as_float(r[c][4 * c4 + 3]) + __uint_as_float(v.w)));
+        for (int c = 0; c < 4; ++c) tmem_ld16(t_dq + (4 * b + c) * C::kDqCols, r[c]);
+        tmem_ld_wait16(r[0]);
+        reg_fence16(r[1]);
+        reg_fence16(r[2]);
+        reg_fence16(r[3]);
+        if (b == C::kDqChunks / 4 - 1) {
+          // dQ_i has left tensor memory: the MMA may write the columns again.
+          tc_fence_before();
+          mbar_arrive(bar(C::kBarDQEmpty));
         }
+        // 128 rows x 64 bytes per chunk, 64-byte swizzle: 16-byte chunk index
+        // XOR ((row / 2) mod 4).
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint8_t* row = chunk_base(4 * b + c) + qr * 64;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<uint4*>(row + ((c4 ^ ((qr >> 1) & 3)) << 4)) =
+                make_uint4(r[c][4 * c4], r[c][4 * c4 + 1], r[c][4 * c4 + 2], r[c][4 * c4 + 3]);
+        }
+      }
       fence_proxy_async_smem();
       named_bar_sync(C::kDrainBarrier, kBlockM);
       if (leader) {
         const int q0 = (i_first + it) * kBlockM;
 #pragma unroll 1
-        for (int c = 0; c < C::kDqChunks; ++c)
-          tma_reduce_add_3d(&p.tm_dq, sbase + buf + c * C::kDqChunkBytes,
-                            rank * C::kHalf + c * C::kDqCols, q0, bh);
+        for (int ch = 0; ch < C::kDqChunks; ++ch)
+          tma_reduce_add_3d(&p.tm_dq, smem_u32(chunk_base(ch)), ch * C::kDqCols, q0, bh);
         bulk_commit();
-        bulk_wait_read<0>();  // the TMA has read the sum: stage s is free
+        bulk_wait_read<0>();  // the TMA has read the staged tile: stage s is free
         mbar_arrive(bar(C::kBarStEmpty + s));
       }
     }
@@ -425,7 +374,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
       const int s = it % C::kStages;
       const int i = i_first + it;
       const bool diag = p.causal && i == kt;
-      const bool all_masked = p.causal && i < kt;  // the pair's first tile, seen by key tile 2m+1
       ok = mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull);
       ok = ok && mbar_wait(bar(C::kBarSFull), it & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -458,7 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
         for (int e = 0; e < 64; ++e)
           if (wg * 64 + e < kr) pf[e] = 0.0f;
       }
-      if (!row_valid || all_masked) {
+      if (!row_valid) {
 #pragma unroll
         for (int e = 0; e < 64; ++e) pf[e] = 0.0f;
       }
@@ -473,8 +421,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull));
 
-      // dS = scale * P (dP - D): to tensor memory (for dK) and into shared
-      // memory (for dQ).
+      // dS = scale * P (dP - D): to tensor memory (for dK) and, once dV has
+      // finished reading dO_i, into shared memory (for dQ).
       ok = mbar_wait(bar(C::kBarDPFull), it & 1, ctl, kSiteDPFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -503,11 +451,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
         for (int e = 0; e < 16; ++e) w[e] = dsw[ch * 16 + e];
         tmem_st16(lane_base + C::kColDP + wg * 64 + ch * 16, w);
       }
+      ok = mbar_wait(bar(C::kBarDVDone), it & 1, ctl, kSiteDVDone);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       // dS tile laid out as an MN-major operand with 128B swizzle:
       // [query half][key row][64 queries], 16-byte chunk index XOR (key row
-      // mod 8).  The previous tile's dQ product, its last reader, completed
-      // before this tile's dP^T (issued after that dQ was drained).
-      uint8_t* ds_tile = smem + C::kDsOff;
+      // mod 8).
+      uint8_t* ds_tile = smem + C::ds_off(s);
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         const int q = wg * 64 + c8 * 8;  // first query of this 16-byte chunk
@@ -551,9 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(BwdCfg<D>::kThreads,
   }
 
   tc_fence_before();
-  // Neither CTA leaves while its peer may still read its shared memory or
-  // arrive on its barriers.
-  cluster_sync();
+  __syncthreads();
   if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);

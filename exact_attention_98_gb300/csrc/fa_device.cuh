@@ -103,39 +103,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
-// As mbar_wait, for a barrier that threads of another CTA of the cluster
-// arrive on: the acquire is at cluster scope, so what they wrote into this
-// CTA's shared memory before arriving is visible afterwards.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
-                                                  unsigned int site,
-                                                  unsigned long long limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 15u) == 0u) {
-      if (*ctl.abort_flag) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        *ctl.abort_flag = 1;
-        record_status(ctl.status, kStatusTimeout, site);
-        return false;
-      }
-    }
-  }
-}
-
 // Clean-up wait on the give-up path: ignores the abort flag, bounded by
 // kDrainLimitNs, records nothing.  Used to let this CTA's own TMA copies and
 // MMAs finish before it frees tensor memory and exits.
@@ -190,63 +157,6 @@ __device__ __forceinline__ void bulk_wait() {
 // Named barrier over `count` threads (id 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// Thread-block clusters: rank, shared-memory addresses of the peer CTA,
-// remote arrivals and the cluster-wide barrier.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Address, in the cluster's shared window, of `local` in CTA `rank`'s memory.
-__device__ __forceinline__ uint32_t cluster_map(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-
-// Arrive on an mbarrier of a CTA of the cluster, releasing this thread's
-// earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t cluster_addr) {
-  uint4 v;
-  asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(cluster_addr)
-               : "memory");
-  return v;
-}
-
-// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into the
-// shared memory of a CTA of the cluster, completing `bytes` transactions on
-// that CTA's mbarrier.  dst and bar are shared::cluster addresses.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
-                                                  uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "r"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_v4(uint32_t cluster_addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-// All threads of all CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                   "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later

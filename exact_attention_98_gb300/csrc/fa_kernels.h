@@ -59,7 +59,7 @@ struct BwdParams {
   unsigned int* status;
   int N;
   int BH;
-  int n_kblk;  // ceil(N / 128) rounded up to even (two-CTA clusters)
+  int n_kblk;  // ceil(N / 128)
   int causal;
   float c;      // scale * log2(e)
   float scale;  // folded into dS so that dQ and dK come out scaled
