@@ -142,3 +142,19 @@ def compare_bwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_
                 worst["dk"] = max(worst["dk"], check_grad(dk[b, h][ks], r[1], what + " dK"))
                 worst["dv"] = max(worst["dv"], check_grad(dv[b, h][ks], r[2], what + " dV"))
     return worst, grads, inputs
+
+
+def run_fwd_bwd(B, H, N, d, causal, seed=0, stress=False):
+    """GPU forward then backward.  Returns (inputs, (o, lse), (dq, dk, dv), scale)
+    with the GPU results as fp64 numpy arrays."""
+    from exact_attention_98_gb300 import fa
+
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = attention_inputs(B, H, N, d, seed=seed, stress=stress)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    status = fa.fa_last_device_status()
+    assert status == fa.FA_OK, fa.status_string(status)
+    return (q, k, v, do), (to64(o), to64(lse)), (to64(dq), to64(dk), to64(dv)), scale
