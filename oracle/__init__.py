@@ -51,8 +51,10 @@ def _load():
             lib.oracle_fwd_rows.restype = ctypes.c_int
             lib.oracle_bwd_rows.argtypes = [dp, dp, dp, dp, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_double, ctypes.c_int, ip, ctypes.c_int, dp,
-                                            ip, ctypes.c_int, dp, dp]
+                                            ip, ctypes.c_int, dp, dp, ctypes.c_int]
             lib.oracle_bwd_rows.restype = ctypes.c_int
+            lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_round_bf16.restype = ctypes.c_double
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -103,10 +105,19 @@ def fwd_head(q, k, v, scale: float, causal: bool, rows=None):
     return o, lse
 
 
-def bwd_head(q, k, v, dout, scale: float, causal: bool, qrows=None, krows=None):
+def round_bf16(x: float) -> float:
+    """x rounded to the nearest bf16 value (ties to even), as the oracle does it."""
+    return float(_load().oracle_round_bf16(float(x)))
+
+
+def bwd_head(q, k, v, dout, scale: float, causal: bool, qrows=None, krows=None,
+             o_bf16: bool = False):
     """Backward of one head with loss sum(O * dO).  q, k, v, dout: [N, d].
     qrows: rows of dQ to compute (default all); krows: rows of dK/dV (default
-    all).  Returns (dq [len(qrows), d], dk [len(krows), d], dv [len(krows), d])."""
+    all).  o_bf16: form D = rowsum(dO * O) from the oracle's own O rounded to
+    bf16 -- the backward's O input as the library's API carries it -- instead
+    of the exact fp64 O.  Returns (dq [len(qrows), d], dk [len(krows), d],
+    dv [len(krows), d])."""
     lib = _load()
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     N, d = k.shape
@@ -117,7 +128,7 @@ def bwd_head(q, k, v, dout, scale: float, causal: bool, qrows=None, krows=None):
     dv = np.empty((len(krows), d), dtype=np.float64)
     rc = lib.oracle_bwd_rows(_dp(q), _dp(k), _dp(v), _dp(dout), N, d, float(scale),
                              int(bool(causal)), _ip(qrows), len(qrows), _dp(dq),
-                             _ip(krows), len(krows), _dp(dk), _dp(dv))
+                             _ip(krows), len(krows), _dp(dk), _dp(dv), int(bool(o_bf16)))
     if rc != 0:
         raise RuntimeError(f"oracle_bwd_rows failed with code {rc}")
     return dq, dk, dv
@@ -135,7 +146,7 @@ def fwd(q, k, v, scale: float, causal: bool):
     return o, lse
 
 
-def bwd(q, k, v, dout, scale: float, causal: bool):
+def bwd(q, k, v, dout, scale: float, causal: bool, o_bf16: bool = False):
     """Full backward over [B, H, N, d].  Returns (dq, dk, dv), each [B,H,N,d]."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, H, N, d = q.shape
@@ -143,5 +154,5 @@ def bwd(q, k, v, dout, scale: float, causal: bool):
     for b in range(B):
         for h in range(H):
             dq[b, h], dk[b, h], dv[b, h] = bwd_head(q[b, h], k[b, h], v[b, h], dout[b, h],
-                                                    scale, causal)
+                                                    scale, causal, o_bf16=o_bf16)
     return dq, dk, dv

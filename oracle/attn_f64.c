@@ -51,6 +51,16 @@
 
 static int key_allowed(int i, int j, int causal) { return !causal || j <= i; }
 
+/* x rounded to the nearest bfloat16 value (8 significant bits, ties to even),
+ * directly from fp64.  Used only to model the point where the library hands
+ * O to the backward pass in bf16. */
+double oracle_round_bf16(double x) {
+  if (x == 0.0 || !isfinite(x)) return x;
+  int e;
+  const double m = frexp(x, &e); /* x = m * 2^e, 0.5 <= |m| < 1 */
+  return ldexp(nearbyint(ldexp(m, 8)), e - 8);
+}
+
 /* Scores of one query row against all keys: s[j] = scale * q . k_j, and the
  * row max and LSE over the allowed keys.  Returns the number of allowed keys. */
 static int row_scores(const double* q_row, int i, const double* k, int N, int d,
@@ -128,11 +138,17 @@ int oracle_fwd_rows(const double* q, int nq, const int* qidx, const double* k,
  * statistics (LSE_i and D_i) of every row are computed first.  All of it uses
  * the oracle's own fp64 forward: O_i and LSE_i are not taken from outside.
  * Passing every row in qrows and krows gives the full backward of the head.
+ *
+ * o_bf16: 0 = D_i = dO_i . O_i with the exact fp64 O (the plain definition);
+ *         1 = D_i = dO_i . bf16(O_i): the backward's O input as the library's
+ *             API carries it between the passes (bf16), each element of the
+ *             oracle's own fp64 O rounded to nearest-even bf16.  Everything
+ *             else is identical.
  */
 int oracle_bwd_rows(const double* q, const double* k, const double* v,
                     const double* dout, int N, int d, double scale, int causal,
                     const int* qrows, int nqr, double* dq, const int* krows,
-                    int nkr, double* dk, double* dv) {
+                    int nkr, double* dk, double* dv, int o_bf16) {
   if (N < 1 || d < 1 || nqr < 0 || nkr < 0 || !q || !k || !v || !dout)
     return ORACLE_BAD_ARG;
   if ((nqr > 0 && (!qrows || !dq)) || (nkr > 0 && (!krows || !dk || !dv)))
@@ -164,6 +180,7 @@ int oracle_bwd_rows(const double* q, const double* k, const double* v,
     for (int t = 0; t < d; ++t) {
       double o_it = 0.0;
       for (int j = 0; j < N; ++j) o_it += p[j] * v[(size_t)j * d + t];
+      if (o_bf16) o_it = oracle_round_bf16(o_it);
       Di += dout[(size_t)i * d + t] * o_it;
     }
     lse[i] = L;

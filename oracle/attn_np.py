@@ -38,13 +38,22 @@ def forward(q, k, v, scale: float, causal: bool):
     return o, lse, p
 
 
-def backward(q, k, v, dout, scale: float, causal: bool):
-    """Gradients of sum(O * dO).  Returns (dq, dk, dv), each [N, d]."""
+def round_bf16(x):
+    """Nearest bf16 value of each element (8 significant bits, ties to even)."""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def backward(q, k, v, dout, scale: float, causal: bool, o_bf16: bool = False):
+    """Gradients of sum(O * dO).  Returns (dq, dk, dv), each [N, d].  o_bf16:
+    D = rowsum(dO * O) from O rounded to bf16 (the backward's O input as the
+    library carries it) instead of the exact O."""
     q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
     o, _, p = forward(q, k, v, scale, causal)
     dv = p.T @ dout
     dp = dout @ v.T
-    D = (dout * o).sum(axis=1, keepdims=True)
+    D = (dout * (round_bf16(o) if o_bf16 else o)).sum(axis=1, keepdims=True)
     ds = p * (dp - D)
     dq = scale * (ds @ k)
     dk = scale * (ds.T @ q)

@@ -8,6 +8,11 @@ Tolerances (the bounds the library is held to):
          reported next to it;
   * LSE: max |LSE - LSE_ref| <= 1e-3;
   * dQ, dK, dV: ||X - X_ref||_F / ||X_ref||_F <= 2e-2 over the compared rows.
+    The backward's O input is the forward's bf16 output (the API carries O in
+    bf16), so the oracle forms D = rowsum(dO * O) from its own O rounded to
+    bf16 (o_bf16=True).  With the exact O instead, peaked softmax-stress rows
+    show up to ~5e-2 on dQ from that rounding alone: dP - D cancels for the
+    dominant key and large key rows amplify the remainder.
     Where the exact gradient vanishes by an identity of the method (N = 1:
     the softmax over a single key is constant, so dQ = dK = 0) a relative
     error is undefined; the denominator therefore never drops below an RMS of
@@ -134,7 +139,7 @@ def compare_bwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_
                 qrows = sampled_rows(N, rows_per_head, b, h, H)
                 krows = qrows if idx in kv_heads else []
             r = oracle.bwd_head(q64[b, h], k64[b, h], v64[b, h], do64[b, h], scale, causal,
-                                qrows=qrows, krows=krows)
+                                qrows=qrows, krows=krows, o_bf16=True)
             qs = slice(None) if qrows is None else qrows
             worst["dq"] = max(worst["dq"], check_grad(dq[b, h][qs], r[0], what + " dQ"))
             if krows is None or len(krows):

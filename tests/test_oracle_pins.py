@@ -279,3 +279,45 @@ def test_oracle_regression_fixture():
         dq, dk, dv = oracle.bwd_head(q, k, v, do, rec["scale"], causal)
         for got, key in ((o, "o"), (lse, "lse"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
             np.testing.assert_allclose(got, np.array(want[key]), rtol=1e-12, atol=1e-14)
+
+
+# --- the backward's O input in bf16 -------------------------------------------
+
+
+def test_round_bf16_against_torch_and_by_hand():
+    """The oracle's bf16 rounding: exact values stay, halfway cases go to the
+    even neighbour, and random doubles agree with PyTorch's bf16 conversion of
+    their fp32 value where that fp32 value is itself exact."""
+    torch = pytest.importorskip("torch")
+    r = oracle.round_bf16
+    assert r(1.0) == 1.0 and r(-0.15625) == -0.15625 and r(0.0) == 0.0
+    # 1 + 2^-8 lies halfway between 1 and 1 + 2^-7: ties to even -> 1
+    assert r(1.0 + 2.0 ** -8) == 1.0
+    # 1 + 3 * 2^-8 lies halfway between 1 + 2^-7 and 1 + 2^-6: even -> 1 + 2^-6
+    assert r(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+    assert r(1.0 + 2.0 ** -8 + 2.0 ** -20) == 1.0 + 2.0 ** -7
+    xs = np.random.default_rng(3).standard_normal(2000).astype(np.float32).astype(np.float64)
+    want = torch.from_numpy(xs.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    got = np.array([r(x) for x in xs])
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(attn_np.round_bf16(xs), want)
+
+
+def test_backward_with_bf16_o_matches_numpy_and_differs_only_through_D():
+    """o_bf16 changes only D: against the NumPy restatement with the same
+    option, and exactly equal to the plain backward when O is already a bf16
+    value (V rows bf16-exact and P one-hot: identical keys and N = 1)."""
+    N, d = 24, 8
+    q, k, v, do = rand(N, d), rand(N, d), rand(N, d), rand(N, d)
+    for causal in (False, True):
+        g1 = oracle.bwd_head(q, k, v, do, 0.5, causal, o_bf16=True)
+        g2 = attn_np.backward(q, k, v, do, 0.5, causal, o_bf16=True)
+        for a, b in zip(g1, g2):
+            np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+        g0 = oracle.bwd_head(q, k, v, do, 0.5, causal)
+        assert not np.allclose(g1[0], g0[0], rtol=1e-14, atol=0)
+        np.testing.assert_array_equal(g1[2], g0[2])  # dV does not involve D
+    vb = attn_np.round_bf16(rand(1, d))
+    q1, k1, do1 = rand(1, d), rand(1, d), rand(1, d)
+    np.testing.assert_array_equal(oracle.bwd_head(q1, k1, vb, do1, 0.5, False)[0],
+                                  oracle.bwd_head(q1, k1, vb, do1, 0.5, False, o_bf16=True)[0])
