@@ -84,6 +84,11 @@ struct BwdCfg {
   static constexpr int kDqCols = 16;
   static constexpr int kDqChunks = D / kDqCols;
   static constexpr int kDqChunkBytes = kBlockM * kDqCols * 4;
+  // d = 128: dQ^T in tensor memory (lane = d, column = query), added with
+  // coalesced fp32 reductions straight from registers; d = 64: dQ (lane =
+  // query) staged in shared memory for bulk TMA reduce-adds (an M = 64 dQ^T
+  // would use a different tensor-memory layout).
+  static constexpr bool kDqTransposed = (D == 128);
   static_assert(kDqChunks / 2 * kDqChunkBytes == kTileBytes, "dQ staging must fill Q and dO");
   static constexpr int kBarOff = kDsOff + kDsBytes;
   static constexpr int kBarKV = 0;
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // D = 0.
 #pragma unroll
         for (int r4 = 0; r4 < 4; ++r4) {
-          const int r = lane * 4 + r4;
+          const int r = r4 * 32 + lane;  // consecutive lanes, consecutive words
           const int q = q0 + r;
           const size_t gi = static_cast<size_t>(bh) * p.N + q;
           lse_s[s * kBlockM + r] = (q < p.N) ? -(p.lse[gi] * p.log2e) : -INFINITY;
@@ -267,11 +272,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // dQ_i = dS K: A = dS (queries x keys) MN-major (64-query blocks 16 KB
       // apart, 8-key groups 1024 B apart); B = K as an MN-major operand (d
       // contiguous).  The result goes to the dP^T columns.
+      // At d = 128 the product is computed transposed, dQ_i^T = K^T dS^T
+      // (the same two operands with A and B swapped): tensor-memory lane =
+      // d index, column = query, so the drain adds whole query rows of the
+      // accumulator with warp-coalesced reductions.
       auto issue_dq = [&](uint32_t ds0) {
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ss(tmem_base + C::kColDP, sdesc_sw128(ds0 + kk * 2048, kBlockN * 128, 1024),
-                 sdesc_sw128(k_smem + kk * 2048, C::kHalfBytes, 1024), kIdescQ, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint64_t ds_desc = sdesc_sw128(ds0 + kk * 2048, kBlockN * 128, 1024);
+          const uint64_t k_desc = sdesc_sw128(k_smem + kk * 2048, C::kHalfBytes, 1024);
+          if (C::kDqTransposed)
+            mma_ss(tmem_base + C::kColDP, k_desc, ds_desc, kIdescQ, kk > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem_base + C::kColDP, ds_desc, k_desc, kIdescQ, kk > 0 ? 1u : 0u);
+        }
       };
 
       bool ok = mbar_wait(bar(C::kBarKV), 0, ctl, kSiteKV);
@@ -297,7 +311,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_after();
         issue_tn(C::kColDP, q_s, C::kColDK, it > 0);
         issue_dq(sbase + C::ds_off(s));
-        mma_commit(bar(C::kBarDQFull));  // the drain returns stage s to the loader
+        mma_commit(bar(C::kBarDQFull));
+        // With the transposed dQ the drain needs no shared memory: dQ_i was
+        // the last reader of the stage.  Otherwise the drain returns it.
+        if (C::kDqTransposed) mma_commit(bar(C::kBarStEmpty + s));
       }
       mma_commit(bar(C::kBarMmaDone));
       if (!ok) mbar_wait_drain(bar(C::kBarMmaDone), 0);
@@ -309,6 +326,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int qr = quarter * 32 + lane;  // query row within the tile
     const bool leader = (warp == C::kDrainWarp0 && lane == 0);
     const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
+    if constexpr (C::kDqTransposed) {
+      // thread = d index (lane of dQ_i^T); each warp adds 32 consecutive
+      // floats of one query row per reduction
+      const int dcol = quarter * 32 + lane;
+      const uint32_t t_dqt = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
+      for (int it = 0; it < n_iter; ++it) {
+        bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        tc_fence_after();
+        const int q0 = (i_first + it) * kBlockM;
+        float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.N + q0) * D + dcol;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          uint32_t r[2][32];
+          tmem_ld32(t_dqt + b * 64, r[0]);
+          tmem_ld32(t_dqt + b * 64 + 32, r[1]);
+          tmem_ld_wait(r[0]);
+          reg_fence(r[1]);
+          if (b == 1) {
+            // dQ_i^T has left tensor memory: the MMA may write the columns.
+            tc_fence_before();
+            mbar_arrive(bar(C::kBarDQEmpty));
+          }
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int qc = b * 64 + c;
+            if (q0 + qc < p.N) atomicAdd(acc + static_cast<size_t>(qc) * D, __uint_as_float(r[c >> 5][c & 31]));
+          }
+        }
+      }
+    } else {
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % C::kStages;
       bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
@@ -358,6 +406,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
     }
     if (leader) bulk_wait<0>();
+    }
   } else {
     regs_inc<C::kComputeRegs>();
     // ------------------------------------------------------------- compute
