@@ -44,7 +44,7 @@
 //   warp  13    tensor-memory allocator; lane 0 issues every MMA
 //   warps 14-15 idle
 // Launched with 128 registers per thread; the warpgroups then re-split them
-// (compute 176, drain 96, load/MMA 64).
+// (compute 144, drain 144, load/MMA 64).
 #include "fa_device.cuh"
 #include "fa_kernels.h"
 
@@ -56,8 +56,8 @@ struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kThreads = 512;
   static constexpr int kLaunchRegs = 128;
-  static constexpr int kComputeRegs = 176;  // 2 x 128 threads
-  static constexpr int kDrainRegs = 96;     // 128 threads
+  static constexpr int kComputeRegs = 144;  // 2 x 128 threads
+  static constexpr int kDrainRegs = 144;    // 128 threads: a whole dQ^T row in registers
   static constexpr int kOtherRegs = 64;     // 128 threads
   static_assert(2 * 128 * kComputeRegs + 128 * kDrainRegs + 128 * kOtherRegs <=
                     kThreads * kLaunchRegs,
@@ -337,24 +337,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_after();
         const int q0 = (i_first + it) * kBlockM;
         float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.N + q0) * D + dcol;
+        uint32_t r[4][32];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          uint32_t r[2][32];
-          tmem_ld32(t_dqt + b * 64, r[0]);
-          tmem_ld32(t_dqt + b * 64 + 32, r[1]);
-          tmem_ld_wait(r[0]);
-          reg_fence(r[1]);
-          if (b == 1) {
-            // dQ_i^T has left tensor memory: the MMA may write the columns.
-            tc_fence_before();
-            mbar_arrive(bar(C::kBarDQEmpty));
-          }
+        for (int b = 0; b < 4; ++b) tmem_ld32(t_dqt + b * 32, r[b]);
+        tmem_ld_wait(r[0]);
+        reg_fence(r[1]);
+        reg_fence(r[2]);
+        reg_fence(r[3]);
+        // dQ_i^T has left tensor memory: the MMA may write the columns again.
+        tc_fence_before();
+        mbar_arrive(bar(C::kBarDQEmpty));
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int qc = b * 64 + c;
-            if (q0 + qc < p.N) atomicAdd(acc + static_cast<size_t>(qc) * D, __uint_as_float(r[c >> 5][c & 31]));
-          }
-        }
+        for (int qc = 0; qc < kBlockM; ++qc)
+          if (q0 + qc < p.N) atomicAdd(acc + static_cast<size_t>(qc) * D, __uint_as_float(r[qc >> 5][qc & 31]));
       }
     } else {
     for (int it = 0; it < n_iter; ++it) {
@@ -438,32 +433,48 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_ld_wait(sr[0]);
       reg_fence(sr[1]);
       const f32x2* neg_lse = reinterpret_cast<const f32x2*>(lse2 + wg * 64);
-      float pf[64];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-        for (int e2 = 0; e2 < 16; ++e2) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
-                           c2, neg_lse[ch * 16 + e2]),
-                    x0, x1);
-          pf[ch * 32 + 2 * e2] = ex2_mufu(x0);
-          pf[ch * 32 + 2 * e2 + 1] = ex2_mufu(x1);
-        }
+      // P kept packed as bf16: the very values the dV product uses, and the
+      // ones dS is formed from.
+      uint32_t pw[32];
+      auto exp_pair = [&](int ch, int e2, float& p0, float& p1) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
+                         c2, neg_lse[ch * 16 + e2]),
+                  x0, x1);
+        p0 = ex2_mufu(x0);
+        p1 = ex2_mufu(x1);
+      };
       if (diag) {  // uniform: only the diagonal tile pays for the mask
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
-          if (wg * 64 + e < kr) pf[e] = 0.0f;
+        for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) {
+            float p0, p1;
+            exp_pair(ch, e2, p0, p1);
+            const int col = wg * 64 + ch * 32 + 2 * e2;
+            if (col < kr) p0 = 0.0f;
+            if (col + 1 < kr) p1 = 0.0f;
+            pw[ch * 16 + e2] = pack_bf16x2(p0, p1);
+          }
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) {
+            float p0, p1;
+            exp_pair(ch, e2, p0, p1);
+            pw[ch * 16 + e2] = pack_bf16x2(p0, p1);
+          }
       }
       if (!row_valid) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) pf[e] = 0.0f;
+        for (int e = 0; e < 32; ++e) pw[e] = 0u;
       }
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(pf[ch * 32 + 2 * e], pf[ch * 32 + 2 * e + 1]);
+        for (int e = 0; e < 16; ++e) w[e] = pw[ch * 16 + e];
         tmem_st16(lane_base + C::kColS + wg * 64 + ch * 16, w);
       }
       tmem_st_wait();
@@ -490,7 +501,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           f2_unpack(f2_mul(f2_mul(f2_add(f2_pack(__uint_as_float(dr[ch][2 * e2]),
                                                  __uint_as_float(dr[ch][2 * e2 + 1])),
                                          neg_d[ch * 16 + e2]),
-                                  f2_pack(pf[ch * 32 + 2 * e2], pf[ch * 32 + 2 * e2 + 1])),
+                                  f2_pack(__uint_as_float(pw[ch * 16 + e2] << 16),
+                                          __uint_as_float(pw[ch * 16 + e2] & 0xFFFF0000u))),
                            scale2),
                     a0, a1);
           dsw[ch * 16 + e2] = pack_bf16x2(a0, a1);
