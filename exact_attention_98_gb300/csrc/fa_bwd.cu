@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp >= C::kProducerWarp) {
-    regs_dec<C::kOtherRegs>();
+    regs_set<C::kOtherRegs, C::kLaunchRegs>();
     if (warp == C::kProducerWarp) {
       // ----------------------------------------------------------- loads
       if (lane == 0) {
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (!ok) mbar_wait_drain(bar(C::kBarMmaDone), 0);
     }
   } else if (warp >= C::kDrainWarp0) {
-    regs_dec<C::kDrainRegs>();
+    regs_set<C::kDrainRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------- dQ drain
     const int quarter = warp & 3;
     const int qr = quarter * 32 + lane;  // query row within the tile
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (leader) bulk_wait<0>();
     }
   } else {
-    regs_inc<C::kComputeRegs>();
+    regs_set<C::kComputeRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------- compute
     const int wg = warp >> 2;  // query-column half
     const int quarter = warp & 3;

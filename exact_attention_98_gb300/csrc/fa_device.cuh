@@ -452,6 +452,17 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                  "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 
+// Moves this warpgroup from the launch allocation `kFrom` to `kTo` registers
+// per thread with the instruction that goes that way: setmaxnreg.dec to a
+// count above the current one (or .inc to one below) is an illegal
+// instruction.
+template <int kTo, int kFrom>
+__device__ __forceinline__ void regs_set() {
+  static_assert(kTo % 8 == 0 && kTo >= 24 && kTo <= 256, "setmaxnreg count");
+  if constexpr (kTo > kFrom) regs_inc<kTo>();
+  else if constexpr (kTo < kFrom) regs_dec<kTo>();
+}
+
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 

@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp >= 8) {
-   regs_dec<C::kOtherRegs>();
+   regs_set<C::kOtherRegs, C::kLaunchRegs>();
    if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
    }
   } else {
-    regs_inc<C::kSoftmaxRegs>();
+    regs_set<C::kSoftmaxRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------- softmax
     const int t = warp >> 2;             // query tile of this warpgroup
     const int quarter = warp & 3;        // tensor-memory lane quarter
