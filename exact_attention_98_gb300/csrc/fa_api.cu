@@ -292,6 +292,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   p.causal = causal;
   p.c = scale * 1.4426950408889634f;
   p.scale = scale;
+  p.inv_scale = 1.0f / scale;
   p.log2e = 1.4426950408889634f;
   if (static_cast<long long>(p.n_kblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
 

@@ -30,6 +30,20 @@
 // with P^T = exp2(S^T c - LSE_i log2 e) and dS = scale * P (dP - D_i): the
 // softmax scale is folded into dS, so dK and dQ come out scaled.
 //
+// The per-query terms -LSE_i / scale and -D_i enter through the tensor core
+// as a rank-1 bias: one more K = 16 MMA adds ones(128 x 16) * b^T onto S^T
+// (and onto dP^T), where column k of b holds the query's value split into
+// bf16 hi + lo parts (about 16 significant bits) in its first two entries and
+// zeros elsewhere.  The compute warps then need no per-query loads at all:
+// P = exp2(c S'^T) and dS = scale P dP'^T.
+//
+// The per-query terms -LSE_i / scale and -D_i enter through the tensor core
+// as a rank-1 bias: one more K = 16 MMA adds ones(128 x 16) * b^T onto S^T
+// (and onto dP^T), where column k of b holds the query's value split into
+// bf16 hi + lo parts (about 16 significant bits) in its first two entries and
+// zeros elsewhere.  The compute warps then need no per-query loads at all:
+// P = exp2(c S'^T) and dS = scale P dP'^T.
+//
 // Warp roles (512 threads = four warpgroups):
 //   warps 0-7   compute: two warpgroups, thread = key row, warpgroup w takes
 //               query columns [64w, 64w + 64); at the end warpgroup 0 writes
@@ -72,8 +86,15 @@ struct BwdCfg {
   static constexpr int kVOff = kTileBytes;
   static constexpr int kQOff = 2 * kTileBytes;                     // kStages tiles
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;      // kStages tiles
-  static constexpr int kLseOff = kDOOff + kStages * kTileBytes;    // kStages x 128 fp32
-  static constexpr int kDsumOff = kLseOff + kStages * kBlockM * 4;  // kStages x 128 fp32
+  // bias operands: all-ones A (128 x 16 bf16), and per stage the LSE and D
+  // B tiles (128 x 16 bf16, K-major without swizzle: [8-row group][K half]
+  // [row mod 8][16 bytes] -> LBO = 128 B, SBO = 256 B)
+  static constexpr int kBiasTileBytes = kBlockM * 16 * 2;
+  static constexpr int kBiasLbo = 128;
+  static constexpr int kBiasSbo = 256;
+  static constexpr int kOnesOff = kDOOff + kStages * kTileBytes;
+  static constexpr int kBiasOff = kOnesOff + kBiasTileBytes;  // [stage][lse, d]
+  static constexpr int kDsumOff = kBiasOff + kStages * 2 * kBiasTileBytes - kStages * kBlockM * 4;
   static constexpr int kDsTileBytes = kBlockN * kBlockM * 2;  // dS is 128 x 128 for any d
   // At d = 128 the dS tile reuses the dO_i buffer; at d = 64 that buffer is
   // too small and dS gets one buffer per stage.
@@ -149,8 +170,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::kBarOff + 8u * static_cast<uint32_t>(i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kTmemSlotOff);
-  float* lse_s = reinterpret_cast<float*>(smem + C::kLseOff);
-  float* dsum_s = reinterpret_cast<float*>(smem + C::kDsumOff);
   const WaitCtl ctl{abort_flag, p.status};
 
   const int warp = warp_id();
@@ -184,6 +203,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(bar(C::kBarMmaDone), 1);
     fence_mbar_init();
   }
+  // bias operands: A = all ones; the B tiles start at zero and the loader
+  // writes only the two hi/lo entries of each row
+  for (int w = threadIdx.x; w < C::kBiasTileBytes / 4; w += C::kThreads)
+    reinterpret_cast<uint32_t*>(smem + C::kOnesOff)[w] = 0x3F803F80u;  // bf16 1.0 pairs
+  for (int w = threadIdx.x; w < C::kStages * 2 * C::kBiasTileBytes / 4; w += C::kThreads)
+    reinterpret_cast<uint32_t*>(smem + C::kBiasOff)[w] = 0u;
+  fence_proxy_async_smem();
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -223,17 +249,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                         bar(C::kBarStFull + s), h * 64, q0, bh);
           }
         }
-        // -LSE in log2 units and -D for the 128 rows (negated once here so the
-        // compute warps add them); rows past N get -LSE = -inf (so P = 0) and
-        // D = 0.
+        // Bias rows: -LSE_q / scale (raw score units, so that c (S^T + b)
+        // = S^T c - LSE_q log2 e) and -D_q, each as bf16 hi + lo.  Rows past
+        // N get a bias of -10^4 (P = 0 there) and D = 0.
+        uint8_t* bias_lse = smem + C::kBiasOff + (2 * s) * C::kBiasTileBytes;
+        uint8_t* bias_d = bias_lse + C::kBiasTileBytes;
 #pragma unroll
         for (int r4 = 0; r4 < 4; ++r4) {
-          const int r = r4 * 32 + lane;  // consecutive lanes, consecutive words
+          const int r = r4 * 32 + lane;
           const int q = q0 + r;
           const size_t gi = static_cast<size_t>(bh) * p.N + q;
-          lse_s[s * kBlockM + r] = (q < p.N) ? -(p.lse[gi] * p.log2e) : -INFINITY;
-          dsum_s[s * kBlockM + r] = (q < p.N) ? -p.dsum[gi] : 0.0f;
+          const float vl = (q < p.N) ? -p.lse[gi] * p.inv_scale : -1.0e4f;
+          const float vd = (q < p.N) ? -p.dsum[gi] : 0.0f;
+          const int off = (r >> 3) * C::kBiasSbo + (r & 7) * 16;  // K half 0, entries 0 and 1
+          const float lh = __bfloat162float(__float2bfloat16_rn(vl));
+          const float dh = __bfloat162float(__float2bfloat16_rn(vd));
+          *reinterpret_cast<uint32_t*>(bias_lse + off) = pack_bf16x2(lh, vl - lh);
+          *reinterpret_cast<uint32_t*>(bias_d + off) = pack_bf16x2(dh, vd - dh);
         }
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::kBarStFull + s));
         issued = it + 1;
@@ -259,6 +293,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_ss(tmem_base + dcol, sdesc_sw128(a0 + off, 16, 1024),
                  sdesc_sw128(b0 + off, 16, 1024), kIdescSq, kk > 0 ? 1u : 0u);
         }
+      };
+      // X^T += ones b^T: the rank-1 bias of tile `which` (stage-major: LSE, D)
+      auto issue_bias = [&](int which, uint32_t dcol) {
+        mma_ss(tmem_base + dcol, sdesc_plain(sbase + C::kOnesOff, C::kBiasLbo, C::kBiasSbo),
+               sdesc_plain(sbase + C::kBiasOff + which * C::kBiasTileBytes, C::kBiasLbo, C::kBiasSbo),
+               kIdescSq, 1u);
       };
       // acc += X^T Y with X^T (keys x queries, bf16) in tensor memory and Y =
       // dO_i or Q_i in shared memory as an MN-major B (d contiguous).
@@ -296,12 +336,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (!(ok = mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull))) break;
         tc_fence_after();
         issue_nt(k_smem, q_s, C::kColS);
+        issue_bias(2 * s, C::kColS);
         mma_commit(bar(C::kBarSFull));
         if (it > 0) {
           if (!(ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl, kSiteDQEmpty))) break;
           tc_fence_after();
         }
         issue_nt(v_smem, do_s, C::kColDP);
+        issue_bias(2 * s + 1, C::kColDP);
         mma_commit(bar(C::kBarDPFull));
         if (!(ok = mbar_wait(bar(C::kBarPFull), it & 1, ctl, kSitePFull))) break;
         tc_fence_after();
@@ -422,24 +464,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ok = ok && mbar_wait(bar(C::kBarSFull), it & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      const float* lse2 = lse_s + s * kBlockM;
-      const float* dsm = dsum_s + s * kBlockM;
 
-      // P^T = exp2(S^T c - LSE log2 e); masked entries (query < key on the
-      // diagonal tile, keys past N) are 0.
+      // P^T = exp2(c S'^T), S'^T = S^T - LSE / scale by the bias MMA; masked
+      // entries (query < key on the diagonal tile, keys past N) are 0.
       uint32_t sr[2][32];
       tmem_ld32(lane_base + C::kColS + wg * 64, sr[0]);
       tmem_ld32(lane_base + C::kColS + wg * 64 + 32, sr[1]);
       tmem_ld_wait(sr[0]);
       reg_fence(sr[1]);
-      const f32x2* neg_lse = reinterpret_cast<const f32x2*>(lse2 + wg * 64);
       // P kept packed as bf16: the very values the dV product uses, and the
       // ones dS is formed from.
       uint32_t pw[32];
       auto exp_pair = [&](int ch, int e2, float& p0, float& p1) {
         float x0, x1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
-                         c2, neg_lse[ch * 16 + e2]),
+        f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
+                         c2),
                   x0, x1);
         p0 = ex2_mufu(x0);
         p1 = ex2_mufu(x1);
@@ -481,8 +520,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull));
 
-      // dS = scale * P (dP - D): to tensor memory (for dK) and, once dV has
-      // finished reading dO_i, into shared memory (for dQ).
+      // dS = scale * P dP'^T, dP'^T = dP^T - D by the bias MMA: to tensor
+      // memory (for dK) and, once dV has finished reading dO_i, into shared
+      // memory (for dQ).
       ok = mbar_wait(bar(C::kBarDPFull), it & 1, ctl, kSiteDPFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -491,16 +531,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_ld32(lane_base + C::kColDP + wg * 64 + 32, dr[1]);
       tmem_ld_wait(dr[0]);
       reg_fence(dr[1]);
-      const f32x2* neg_d = reinterpret_cast<const f32x2*>(dsm + wg * 64);
       uint32_t dsw[32];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
 #pragma unroll
         for (int e2 = 0; e2 < 16; ++e2) {
           float a0, a1;
-          f2_unpack(f2_mul(f2_mul(f2_add(f2_pack(__uint_as_float(dr[ch][2 * e2]),
-                                                 __uint_as_float(dr[ch][2 * e2 + 1])),
-                                         neg_d[ch * 16 + e2]),
+          f2_unpack(f2_mul(f2_mul(f2_pack(__uint_as_float(dr[ch][2 * e2]),
+                                          __uint_as_float(dr[ch][2 * e2 + 1])),
                                   f2_pack(__uint_as_float(pw[ch * 16 + e2] << 16),
                                           __uint_as_float(pw[ch * 16 + e2] & 0xFFFF0000u))),
                            scale2),

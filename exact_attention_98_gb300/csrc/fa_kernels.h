@@ -63,6 +63,7 @@ struct BwdParams {
   int causal;
   float c;      // scale * log2(e)
   float scale;  // folded into dS so that dQ and dK come out scaled
+  float inv_scale;  // 1 / scale: -LSE / scale is the bias in raw score units
   float log2e;
 };
 
