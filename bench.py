@@ -55,6 +55,29 @@ def parse():
     return ap.parse_args()
 
 
+def replica_seed(rank: int) -> int:
+    """Seed of rank `rank`'s replica batch: each rank works on its own batch."""
+    return rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The max of a per-rank scalar over the process group (the job's time is
+    its slowest rank's); x itself when there is no group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_replica: float, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs one replica of the workload."""
+    return world * flops_per_replica / (ms * 1e-3) / 1e12
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -210,15 +233,8 @@ def native_arm(args):
             torch.distributed.barrier()
             torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
-
     # each rank: its own replica batch (different seed per rank)
-    q, k, v, do = attention_inputs(B, H, N, d, seed=rank)
+    q, k, v, do = attention_inputs(B, H, N, d, seed=replica_seed(rank))
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     o = torch.empty_like(qd)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -263,9 +279,9 @@ def native_arm(args):
     with ClockSampler(local) as clocks:
         step_ms, fwd_ms, bwd_ms, wall = timed(False, args.steps, args.warmup, kernel_times=True)
     clk = clocks.summary()
-    mean_ms = max_over_ranks(statistics.mean(step_ms))
+    mean_ms = max_over_ranks(statistics.mean(step_ms), dev)
     f_fwd, f_bwd = flops(B, H, N, d, False)
-    value = world * (f_fwd + f_bwd) / (mean_ms * 1e-3) / 1e12
+    value = job_tflops(f_fwd + f_bwd, world, mean_ms)
     fwd_med, bwd_med = statistics.median(fwd_ms), statistics.median(bwd_ms)
     fwd_tf = f_fwd / (fwd_med * 1e-3) / 1e12
     bwd_main_tf = f_bwd / (bwd_med * 1e-3) / 1e12
@@ -305,8 +321,8 @@ def native_arm(args):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
-    e2e_value = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e_value = job_tflops(f_fwd + f_bwd, world, e2e_ms)
     tensor_bytes = q.numel() * q.element_size()
 
     peaks = {}
