@@ -72,7 +72,7 @@ struct BwdCfg {
   static constexpr int kLaunchRegs = 128;
   static constexpr int kComputeRegs = 144;  // 2 x 128 threads
   static constexpr int kDrainRegs = 144;    // 128 threads: a whole dQ^T row in registers
-  static constexpr int kOtherRegs = 64;     // 128 threads
+  static constexpr int kOtherRegs = 80;     // 128 threads (load, MMA): no spills
   static_assert(2 * 128 * kComputeRegs + 128 * kDrainRegs + 128 * kOtherRegs <=
                     kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
@@ -99,7 +99,8 @@ struct BwdCfg {
   // At d = 128 the dS tile reuses the dO_i buffer; at d = 64 that buffer is
   // too small and dS gets one buffer per stage.
   static constexpr int kDsOff = kDsumOff + kStages * kBlockM * 4;
-  static constexpr int kDsBytes = (D == 128) ? 0 : kStages * kDsTileBytes;
+  static constexpr bool kDsInDO = (D == 128);
+  static constexpr int kDsBytes = kDsInDO ? 0 : kStages * kDsTileBytes;
   // dQ staging: d/16 chunks of 128 rows x 16 fp32 (64-byte swizzled rows),
   // the first half in the stage's Q buffer, the second in its dO buffer.
   static constexpr int kDqCols = 16;
@@ -119,7 +120,8 @@ struct BwdCfg {
   static constexpr int kBarDPFull = kBarSFull + 1;
   static constexpr int kBarPFull = kBarDPFull + 1;
   static constexpr int kBarDVDone = kBarPFull + 1;
-  static constexpr int kBarDSFull = kBarDVDone + 1;
+  static constexpr int kBarDSTmem = kBarDVDone + 1;  // dS^T_i in tensor memory
+  static constexpr int kBarDSFull = kBarDSTmem + 1;  // dS_i in shared memory
   static constexpr int kBarDQFull = kBarDSFull + 1;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarMmaDone = kBarDQEmpty + 1;
@@ -157,6 +159,7 @@ enum : unsigned int {
   kSiteDQFull = 0x209,
   kSiteDQEmpty = 0x20A,
   kSiteMmaDone = 0x20B,
+  kSiteDSTmem = 0x20C,
 };
 
 template <int D>
@@ -197,6 +200,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(bar(C::kBarDPFull), 1);
     mbar_init(bar(C::kBarPFull), 2 * kBlockM);
     mbar_init(bar(C::kBarDVDone), 1);
+    mbar_init(bar(C::kBarDSTmem), 2 * kBlockM);
     mbar_init(bar(C::kBarDSFull), 2 * kBlockM);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQEmpty), kBlockM);
@@ -349,9 +353,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_after();
         issue_tn(C::kColS, do_s, C::kColDV, it > 0);
         mma_commit(bar(C::kBarDVDone));
-        if (!(ok = mbar_wait(bar(C::kBarDSFull), it & 1, ctl, kSiteDSFull))) break;
+        // dK_i needs dS^T_i in tensor memory only; dQ_i also needs its copy in
+        // shared memory, which the compute warps write while dK_i runs.
+        if (!(ok = mbar_wait(bar(C::kBarDSTmem), it & 1, ctl, kSiteDSTmem))) break;
         tc_fence_after();
         issue_tn(C::kColDP, q_s, C::kColDK, it > 0);
+        if (!(ok = mbar_wait(bar(C::kBarDSFull), it & 1, ctl, kSiteDSFull))) break;
         issue_dq(sbase + C::ds_off(s));
         mma_commit(bar(C::kBarDQFull));
         // With the transposed dQ the drain needs no shared memory: dQ_i was
@@ -460,8 +467,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const int s = it % C::kStages;
       const int i = i_first + it;
       const bool diag = p.causal && i == kt;
-      ok = mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull);
-      ok = ok && mbar_wait(bar(C::kBarSFull), it & 1, ctl, kSiteSFull);
+      // S^T_i complete implies Q_i landed: the compute warps read no stage data
+      ok = mbar_wait(bar(C::kBarSFull), it & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
 
@@ -550,8 +557,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int e = 0; e < 16; ++e) w[e] = dsw[ch * 16 + e];
         tmem_st16(lane_base + C::kColDP + wg * 64 + ch * 16, w);
       }
-      ok = mbar_wait(bar(C::kBarDVDone), it & 1, ctl, kSiteDVDone);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarDSTmem));
+      if constexpr (C::kDsInDO) {  // dV_i must be done reading dO_i
+        ok = mbar_wait(bar(C::kBarDVDone), it & 1, ctl, kSiteDVDone);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
       // dS tile laid out as an MN-major operand with 128B swizzle:
       // [query half][key row][64 queries], 16-byte chunk index XOR (key row
       // mod 8).
@@ -566,8 +578,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         *dst = make_uint4(dsw[4 * c8], dsw[4 * c8 + 1], dsw[4 * c8 + 2], dsw[4 * c8 + 3]);
       }
       fence_proxy_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
       mbar_arrive(bar(C::kBarDSFull));
     }
 
