@@ -238,6 +238,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.ln2 = 0.6931471805599453f;
   p.poly_per_octet = poly_per_octet();
   if (static_cast<long long>(p.n_qblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  p.n_items = p.n_qblk * BH;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (timing_record(0, true, s) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_fwd(p, d, s) != cudaSuccess) return FA_ERR_CUDA;

@@ -17,8 +17,12 @@
 // every 8 on the FMA pipe, so the default share is 0; the other shares stay
 // instantiated and selectable.
 //
-// CTA = two 128-row query tiles of one (batch, head); keys and values stream
-// through a ring of shared-memory slots (K_j and V_j alternate).
+// Persistent CTAs (one per SM) walk the work items; an item is two 128-row
+// query tiles of one (batch, head).  Keys and values stream through a ring of
+// shared-memory slots (K_j and V_j alternate, one running index across
+// items); the next item's Q tiles load as soon as the current item's last S
+// product has read the Q buffer, and its first S products run while the
+// softmax warpgroups write the current item's O.
 //
 // Warp roles (384 threads = three warpgroups):
 //   warps 0-3   softmax warpgroup for query tile 0 (thread = one query row)
@@ -27,7 +31,7 @@
 //   warp  9     tensor-memory allocator; lane 0 issues every MMA
 //   warps 10-11 idle
 // The CTA is launched with 168 registers per thread (12 warps, three per SM
-// sub-partition); the third warpgroup gives registers up (80) so that each
+// sub-partition); the third warpgroup gives registers up (88) so that each
 // softmax thread can hold a whole row of S (208).
 //
 // MMA order per key tile j (ping-pong: while one warpgroup computes the
@@ -49,7 +53,7 @@ struct FwdCfg {
   static constexpr int kThreads = 384;
   static constexpr int kLaunchRegs = 168;   // what ptxas must allocate (checked at launch)
   static constexpr int kSoftmaxRegs = 208;  // 2 x 128 threads
-  static constexpr int kOtherRegs = 80;     // 128 threads
+  static constexpr int kOtherRegs = 88;     // 128 threads (load, MMA): no spills
   static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
   static constexpr int kProducerWarp = 8;
@@ -60,11 +64,13 @@ struct FwdCfg {
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-  // barriers: q_full, full[kSlots], empty[kSlots], s_full[2], p_full[2], o_full[2], mma_done
+  // barriers: q_full, q_empty, full[kSlots], empty[kSlots], s_full[2],
+  // p_full[2], o_full[2], mma_done
   static constexpr int kBarQFull = 0;
-  static constexpr int kBarFull = 1;
-  static constexpr int kBarEmpty = 1 + kSlots;
-  static constexpr int kBarSFull = 1 + 2 * kSlots;
+  static constexpr int kBarQEmpty = 1;
+  static constexpr int kBarFull = 2;
+  static constexpr int kBarEmpty = 2 + kSlots;
+  static constexpr int kBarSFull = 2 + 2 * kSlots;
   static constexpr int kBarPFull = kBarSFull + 2;
   static constexpr int kBarOFull = kBarPFull + 2;
   static constexpr int kBarMmaDone = kBarOFull + 2;
@@ -87,7 +93,43 @@ enum : unsigned int {
   kSitePFull = 0x105,
   kSiteSFull = 0x106,
   kSiteOFull = 0x107,
+  kSiteQEmpty = 0x108,
 };
+
+// Work item w = two 128-row query tiles of one (batch, head).  Non-causal:
+// head-major, so that the query blocks of one head are processed together and
+// share its K and V in L2.  Causal: the heaviest blocks (the last query
+// blocks, which see the most keys) of every head first.
+struct FwdItem {
+  int bh;
+  int q0;
+  int nkv0, nkv1;  // key tiles seen by query tile 0 and 1 (0: tile past N)
+  int nmax;
+  __device__ __forceinline__ int nkv(int t) const { return t ? nkv1 : nkv0; }
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int w, int n_ktiles) {
+  FwdItem it;
+  it.bh = p.causal ? w % p.BH : w / p.n_qblk;
+  const int qblk = p.n_qblk - 1 - (p.causal ? w / p.BH : w % p.n_qblk);
+  it.q0 = qblk * 2 * kBlockM;
+  auto nkv_of = [&](int qs) {
+    return qs >= p.N ? 0 : (p.causal ? min(n_ktiles, qs / kBlockN + 1) : n_ktiles);
+  };
+  it.nkv0 = nkv_of(it.q0);
+  it.nkv1 = nkv_of(it.q0 + kBlockM);
+  it.nmax = max(it.nkv0, it.nkv1);
+  return it;
+}
+
+// The r-th item of this CTA: persistent CTAs walk the item list in rounds of
+// gridDim.x, alternating direction (0..G-1, then G-1..0), so that with the
+// heaviest items first every CTA gets a similar total.
+__device__ __forceinline__ int fwd_item_index(int r) {
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
+  return r * G + ((r & 1) ? G - 1 - c : c);
+}
 
 // POLY: of every 8 exponentials of the softmax, this many are evaluated by
 // exp2_poly on the FMA pipe, the rest by MUFU ex2.
@@ -106,28 +148,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   const int warp = warp_id();
   const int lane = lane_id();
-
-  // Work item.  Non-causal: head-major, so that the query blocks of one head
-  // run in the same wave and share its K and V in L2.  Causal: the heaviest
-  // blocks (the last query blocks, which see the most keys) of every head
-  // first, so that the short ones fill the tail.
-  const int blk = blockIdx.x;
-  const int bh = p.causal ? blk % p.BH : blk / p.n_qblk;
-  const int qblk = p.n_qblk - 1 - (p.causal ? blk / p.BH : blk % p.n_qblk);
-  const int q0 = qblk * 2 * kBlockM;
   const int n_ktiles = (p.N + kBlockN - 1) / kBlockN;
-  int nkv[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qs = q0 + t * kBlockM;
-    if (qs >= p.N) nkv[t] = 0;
-    else nkv[t] = p.causal ? min(n_ktiles, qs / kBlockN + 1) : n_ktiles;
-  }
-  const int nmax = max(nkv[0], nkv[1]);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(bar(C::kBarQFull), 1);
+    mbar_init(bar(C::kBarQEmpty), 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bar(C::kBarFull + s), 1);
       mbar_init(bar(C::kBarEmpty + s), 1);
@@ -150,32 +176,46 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
    regs_set<C::kOtherRegs, C::kLaunchRegs>();
    if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------- producer
+    // Per item: Q_0, Q_1 into the Q buffer once the previous item's last
+    // S product has read it, then K_j, V_j through the ring (one running
+    // load index across items).
     if (lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       const uint32_t q_smem = sbase + C::kQOff;
-      mbar_arrive_expect_tx(bar(C::kBarQFull), 2 * C::kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(q_smem + t * C::kTileBytes + h * C::kHalfBytes, &p.tm_q, bar(C::kBarQFull),
-                      h * 64, q0 + t * kBlockM, bh);
-      int issued = 0;
-      for (int idx = 0; idx < 2 * nmax; ++idx) {
-        const int slot = idx % C::kSlots;
-        const int use = idx / C::kSlots;
-        if (use > 0 && !mbar_wait(bar(C::kBarEmpty + slot), (use - 1) & 1, ctl, kSiteEmpty)) break;
-        const CUtensorMap* map = (idx & 1) ? &p.tm_v : &p.tm_k;
-        const int j = idx >> 1;
-        const uint32_t dst = sbase + C::kRingOff + slot * C::kTileBytes;
-        mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
-        for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(dst + h * C::kHalfBytes, map, bar(C::kBarFull + slot), h * 64, j * kBlockN, bh);
-        issued = idx + 1;
+      int gidx = 0, issued = 0, items_loaded = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int wi = fwd_item_index(round);
+        if (wi >= p.n_items) break;
+        const FwdItem item = fwd_item(p, wi, n_ktiles);
+        if (round > 0 && !(ok = mbar_wait(bar(C::kBarQEmpty), (round - 1) & 1, ctl, kSiteQEmpty)))
+          break;
+        mbar_arrive_expect_tx(bar(C::kBarQFull), 2 * C::kTileBytes);
+        for (int t = 0; t < 2; ++t)
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(q_smem + t * C::kTileBytes + h * C::kHalfBytes, &p.tm_q, bar(C::kBarQFull),
+                        h * 64, item.q0 + t * kBlockM, item.bh);
+        items_loaded = round + 1;
+        for (int idx = 0; idx < 2 * item.nmax; ++idx, ++gidx) {
+          const int slot = gidx % C::kSlots;
+          const int use = gidx / C::kSlots;
+          if (use > 0 && !(ok = mbar_wait(bar(C::kBarEmpty + slot), (use - 1) & 1, ctl, kSiteEmpty)))
+            break;
+          const CUtensorMap* map = (idx & 1) ? &p.tm_v : &p.tm_k;
+          const int j = idx >> 1;
+          const uint32_t dst = sbase + C::kRingOff + slot * C::kTileBytes;
+          mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(dst + h * C::kHalfBytes, map, bar(C::kBarFull + slot), h * 64, j * kBlockN,
+                        item.bh);
+          issued = gidx + 1;
+        }
       }
       // Let every copy this CTA started land before shared memory is released
       // (only waits on the give-up path; on the normal path all have landed).
-      mbar_wait_drain(bar(C::kBarQFull), 0);
+      if (items_loaded > 0) mbar_wait_drain(bar(C::kBarQFull), (items_loaded - 1) & 1);
       for (int idx = max(0, issued - C::kSlots); idx < issued; ++idx)
         mbar_wait_drain(bar(C::kBarFull + idx % C::kSlots), (idx / C::kSlots) & 1);
     }
@@ -217,45 +257,64 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
       };
 
-      bool ok = mbar_wait(bar(C::kBarQFull), 0, ctl, kSiteQFull);
-      if (ok) ok = mbar_wait(bar(C::kBarFull + slot_of(0)), parity_of(0), ctl, kSiteKFull);
-      if (ok) {
+      // Per item, with a running load index `base` and running P counts
+      // np0, np1 (the parity of the p_full barriers) across items:
+      //   S_0(0), S_1(0) | j: [P_0(j)] O_0 += P_0(j) V_j, S_0(j+1); [P_1(j)] ...
+      // The first O_t += P_t(0) V_0 of an item overwrites O_t: the softmax
+      // warpgroup has read O_t of the previous item (its epilogue) before it
+      // releases P_t(0).  S_t(0) of an item may run during that epilogue.
+      bool ok = true;
+      int base = 0;
+      int np0 = 0, np1 = 0;
+      for (int round = 0; ok; ++round) {
+        const int wi = fwd_item_index(round);
+        if (wi >= p.n_items) break;
+        const FwdItem item = fwd_item(p, wi, n_ktiles);
+        ok = mbar_wait(bar(C::kBarQFull), round & 1, ctl, kSiteQFull);
+        if (ok) ok = mbar_wait(bar(C::kBarFull + slot_of(base)), parity_of(base), ctl, kSiteKFull);
+        if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (nkv[t] > 0) {
-            issue_s(t, slot_of(0));
+          if (item.nkv(t) > 0) {
+            issue_s(t, slot_of(base));
             mma_commit(bar(C::kBarSFull + t));
           }
-        mma_commit(bar(C::kBarEmpty + slot_of(0)));
-      }
-      for (int j = 0; ok && j < nmax; ++j) {
-        const int vidx = 2 * j + 1, kidx = 2 * j + 2;
-        ok = mbar_wait(bar(C::kBarFull + slot_of(vidx)), parity_of(vidx), ctl, kSiteVFull);
-        if (!ok) break;
-        tc_fence_after();
-        bool k_next_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= nkv[t]) continue;
-          ok = mbar_wait(bar(C::kBarPFull + t), j & 1, ctl, kSitePFull);
+        if (item.nmax == 1) mma_commit(bar(C::kBarQEmpty));  // every S of the item issued
+        mma_commit(bar(C::kBarEmpty + slot_of(base)));
+        for (int j = 0; ok && j < item.nmax; ++j) {
+          const int vidx = base + 2 * j + 1, kidx = base + 2 * j + 2;
+          ok = mbar_wait(bar(C::kBarFull + slot_of(vidx)), parity_of(vidx), ctl, kSiteVFull);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(t, slot_of(vidx), j > 0);
-          if (j == nkv[t] - 1) {
-            mma_commit(bar(C::kBarOFull + t));
-          } else {
-            if (!k_next_ready) {
-              ok = mbar_wait(bar(C::kBarFull + slot_of(kidx)), parity_of(kidx), ctl, kSiteKFull);
-              if (!ok) break;
-              tc_fence_after();
-              k_next_ready = true;
+          bool k_next_ready = false;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!ok) break;
+            if (j >= item.nkv(t)) continue;
+            ok = mbar_wait(bar(C::kBarPFull + t), (t ? np1 : np0) & 1, ctl, kSitePFull);
+            if (!ok) break;
+            if (t) ++np1; else ++np0;
+            tc_fence_after();
+            issue_pv(t, slot_of(vidx), j > 0);
+            if (j == item.nkv(t) - 1) {
+              mma_commit(bar(C::kBarOFull + t));
+            } else {
+              if (!k_next_ready) {
+                ok = mbar_wait(bar(C::kBarFull + slot_of(kidx)), parity_of(kidx), ctl, kSiteKFull);
+                if (!ok) break;
+                tc_fence_after();
+                k_next_ready = true;
+              }
+              issue_s(t, slot_of(kidx));
+              mma_commit(bar(C::kBarSFull + t));
             }
-            issue_s(t, slot_of(kidx));
-            mma_commit(bar(C::kBarSFull + t));
           }
+          if (!ok) break;
+          if (j + 2 == item.nmax) mma_commit(bar(C::kBarQEmpty));  // the item's last S issued
+          mma_commit(bar(C::kBarEmpty + slot_of(vidx)));
+          if (k_next_ready) mma_commit(bar(C::kBarEmpty + slot_of(kidx)));
         }
-        if (!ok) break;
-        mma_commit(bar(C::kBarEmpty + slot_of(vidx)));
-        if (k_next_ready) mma_commit(bar(C::kBarEmpty + slot_of(kidx)));
+        base += 2 * item.nmax;
       }
       // Every MMA this thread issued must finish before tensor memory is freed.
       mma_commit(bar(C::kBarMmaDone));
@@ -268,150 +327,170 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const int t = warp >> 2;             // query tile of this warpgroup
     const int quarter = warp & 3;        // tensor-memory lane quarter
     const int row = quarter * 32 + lane;  // row within the query tile
-    const int qpos = q0 + t * kBlockM + row;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t t_s = lane_base + C::kSCol0 + t * 128;
     const uint32_t t_o = lane_base + C::kOCol0 + t * D;
     const float c = p.c;
     const f32x2 c2 = f2_pack(c, c);
     const bool ragged = (p.N % kBlockN) != 0;
-
-    float m_used = -INFINITY;  // running row max in log2 units (scores * c)
-    // row sum of exp2(x - m_used): four f32x2 accumulators (eight partial sums)
-    f32x2 l2[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
-                   f2_pack(0.0f, 0.0f)};
+    // Barrier phases across items: bit 0 = s_full (flips per S tile),
+    // bit 1 = o_full (flips per item).
+    uint32_t phase = 0;
     bool ok = true;
-    for (int j = 0; j < nkv[t]; ++j) {
-      ok = mbar_wait(bar(C::kBarSFull + t), j & 1, ctl, kSiteSFull);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      // The whole row of S (128 fp32) in registers: four loads, one wait.
-      uint32_t r[4][32];
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) tmem_ld32(t_s + ch * 32, r[ch]);
-      tmem_ld_wait(r[0]);
-      reg_fence(r[1]);
-      reg_fence(r[2]);
-      reg_fence(r[3]);
+    for (int round = 0; ok; ++round) {
+      const int wi = fwd_item_index(round);
+      if (wi >= p.n_items) break;
+      // Key tiles of this warpgroup's query tile.  Kept in a small array
+      // indexed by t (so in local memory, like a spill slot): one more live
+      // register in the tile loop below makes ptxas spill about 25 others.
+      const FwdItem itm = fwd_item(p, wi, n_ktiles);
+      int nkv_arr[2] = {itm.nkv0, itm.nkv1};
+      if (nkv_arr[t] == 0) continue;
 
-      const bool edge = (p.causal && j == nkv[t] - 1) || (ragged && j == n_ktiles - 1);
-      if (edge) {
-        const int kbase = j * kBlockN;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int kpos = kbase + ch * 32 + e;
-            if (kpos >= p.N || (p.causal && kpos > qpos)) r[ch][e] = __float_as_uint(-INFINITY);
-          }
-      }
-      // row max of the tile (raw scores; c > 0), eight independent chains
-      float mxa[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) mxa[a] = fmaxf(__uint_as_float(r[a >> 1][(a & 1) * 16]),
-                                                 __uint_as_float(r[a >> 1][(a & 1) * 16 + 1]));
-#pragma unroll
-      for (int a = 0; a < 8; ++a)
-#pragma unroll
-        for (int e = 2; e < 16; e += 2)
-          mxa[a] = fmax3(mxa[a], __uint_as_float(r[a >> 1][(a & 1) * 16 + e]),
-                         __uint_as_float(r[a >> 1][(a & 1) * 16 + e + 1]));
-      const float mx = fmaxf(fmax3(mxa[0], mxa[1], mxa[2]),
-                             fmaxf(fmax3(mxa[3], mxa[4], mxa[5]), fmax3(mxa[6], mxa[7], mxa[0])));
-      // Conditional rescale: move the reference max only when it grows by
-      // more than the threshold (always on the first tile, m_used = -inf).
-      const float m_new = fmaxf(m_used, mx * c);
-      const bool need = (m_new - m_used) > kRescaleThreshold;
-      if (__any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ex2_mufu(m_used - m_new) : 1.0f;
-        if (j > 0) {
-          const f32x2 a2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t o[32];
-            tmem_ld32(t_o + ch * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float lo, hi;
-              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
-              o[e] = __float_as_uint(lo);
-              o[e + 1] = __float_as_uint(hi);
-            }
-            tmem_st32(t_o + ch * 32, o);
-          }
-          tmem_st_wait();
-        }
-        if (need) {
-          const f32x2 a2 = f2_pack(alpha, alpha);
-#pragma unroll
-          for (int a = 0; a < 4; ++a) l2[a] = f2_mul(l2[a], a2);
-          m_used = m_new;
-        }
-      }
-
-      // P = exp2(x - m_used) -> bf16 into tensor memory over S.  Masked
-      // entries are -inf and give exact zeros from MUFU; edge tiles use MUFU
-      // only.
-      const f32x2 negm2 = f2_pack(-m_used, -m_used);
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float x0, x1, p0, p1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[ch][e]), __uint_as_float(r[ch][e + 1])), c2, negm2),
-                    x0, x1);
-          if (!edge && ((ch * 32 + e) & 7) < POLY) {
-            exp2_poly2(x0, x1, p0, p1);
-          } else {
-            p0 = ex2_mufu(x0);
-            p1 = ex2_mufu(x1);
-          }
-          w[e >> 1] = pack_bf16x2(p0, p1);
-          l2[(e >> 1) & 3] = f2_add(l2[(e >> 1) & 3], f2_pack(p0, p1));
-        }
-        tmem_st16(t_s + ch * 16, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarPFull + t));
-    }
-    float l;
-    {
-      float a, b;
-      f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])), a, b);
-      l = a + b;
-    }
-
-    // epilogue: O / l -> bf16, LSE = ln(2) * m_used + ln(l)
-    if (ok && nkv[t] > 0) {
-      ok = mbar_wait(bar(C::kBarOFull + t), 0, ctl, kSiteOFull);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
+      float m_used = -INFINITY;  // running row max in log2 units (scores * c)
+      // row sum of exp2(x - m_used): four f32x2 accumulators (eight partial sums)
+      f32x2 l2[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
+                     f2_pack(0.0f, 0.0f)};
+      for (int j = 0; j < nkv_arr[t]; ++j) {
+        ok = mbar_wait(bar(C::kBarSFull + t), phase & 1u, ctl, kSiteSFull);
+        phase ^= 1u;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
         tc_fence_after();
-        const float inv_l = 1.0f / l;
-        const bool in_range = qpos < p.N;
-        __nv_bfloat16* orow =
-            static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
+        // The whole row of S (128 fp32) in registers: four loads, one wait.
+        uint32_t r[4][32];
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) tmem_ld32(t_s + ch * 32, r[ch]);
+        tmem_ld_wait(r[0]);
+        reg_fence(r[1]);
+        reg_fence(r[2]);
+        reg_fence(r[3]);
+
+        const bool edge = (p.causal && j == nkv_arr[t] - 1) || (ragged && j == n_ktiles - 1);
+        if (edge) {
+          const int kbase = j * kBlockN;
+          const int qpos = fwd_item(p, wi, n_ktiles).q0 + t * kBlockM + row;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int kpos = kbase + ch * 32 + e;
+              if (kpos >= p.N || (p.causal && kpos > qpos)) r[ch][e] = __float_as_uint(-INFINITY);
+            }
+        }
+        // row max of the tile (raw scores; c > 0), eight independent chains
+        float mxa[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mxa[a] = fmaxf(__uint_as_float(r[a >> 1][(a & 1) * 16]),
+                                                   __uint_as_float(r[a >> 1][(a & 1) * 16 + 1]));
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+#pragma unroll
+          for (int e = 2; e < 16; e += 2)
+            mxa[a] = fmax3(mxa[a], __uint_as_float(r[a >> 1][(a & 1) * 16 + e]),
+                           __uint_as_float(r[a >> 1][(a & 1) * 16 + e + 1]));
+        const float mx = fmaxf(fmax3(mxa[0], mxa[1], mxa[2]),
+                               fmaxf(fmax3(mxa[3], mxa[4], mxa[5]), fmax3(mxa[6], mxa[7], mxa[0])));
+        // Conditional rescale: move the reference max only when it grows by
+        // more than the threshold (always on the first tile, m_used = -inf).
+        const float m_new = fmaxf(m_used, mx * c);
+        const bool need = (m_new - m_used) > kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2_mufu(m_used - m_new) : 1.0f;
+          if (j > 0) {
+            const f32x2 a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(t_o + ch * 32, r);
-          tmem_ld_wait(r);
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t o[32];
+              tmem_ld32(t_o + ch * 32, o);
+              tmem_ld_wait(o);
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                float lo, hi;
+                f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
+                o[e] = __float_as_uint(lo);
+                o[e + 1] = __float_as_uint(hi);
+              }
+              tmem_st32(t_o + ch * 32, o);
+            }
+            tmem_st_wait();
+          }
+          if (need) {
+            const f32x2 a2 = f2_pack(alpha, alpha);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) l2[a] = f2_mul(l2[a], a2);
+            m_used = m_new;
+          }
+        }
+
+        // P = exp2(x - m_used) -> bf16 into tensor memory over S.  Masked
+        // entries are -inf and give exact zeros from MUFU; edge tiles use MUFU
+        // only.
+        const f32x2 negm2 = f2_pack(-m_used, -m_used);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
           uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-          if (in_range) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+          for (int e = 0; e < 32; e += 2) {
+            float x0, x1, p0, p1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(r[ch][e]), __uint_as_float(r[ch][e + 1])), c2, negm2),
+                      x0, x1);
+            if (!edge && ((ch * 32 + e) & 7) < POLY) {
+              exp2_poly2(x0, x1, p0, p1);
+            } else {
+              p0 = ex2_mufu(x0);
+              p1 = ex2_mufu(x1);
+            }
+            w[e >> 1] = pack_bf16x2(p0, p1);
+            l2[(e >> 1) & 3] = f2_add(l2[(e >> 1) & 3], f2_pack(p0, p1));
           }
+          tmem_st16(t_s + ch * 16, w);
         }
-        if (in_range) p.lse[static_cast<size_t>(bh) * p.N + qpos] = m_used * p.ln2 + logf(l);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::kBarPFull + t));
+      }
+      float l;
+      {
+        float a, b;
+        f2_unpack(f2_add(f2_add(l2[0], l2[1]), f2_add(l2[2], l2[3])), a, b);
+        l = a + b;
+      }
+
+      // epilogue: O / l -> bf16, LSE = ln(2) * m_used + ln(l).  Reading O_t
+      // here, before P_t(0) of the next item is released, is what lets the
+      // next item's first P V overwrite O_t.
+      if (ok) {
+        ok = mbar_wait(bar(C::kBarOFull + t), (phase >> 1) & 1u, ctl, kSiteOFull);
+        phase ^= 2u;
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          tc_fence_after();
+          const float inv_l = 1.0f / l;
+          const FwdItem item = fwd_item(p, wi, n_ktiles);
+          const int bh = item.bh;
+          const int qpos = item.q0 + t * kBlockM + row;
+          const bool in_range = qpos < p.N;
+          __nv_bfloat16* orow =
+              static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld32(t_o + ch * 32, r);
+            tmem_ld_wait(r);
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+            if (in_range) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+            }
+          }
+          if (in_range) p.lse[static_cast<size_t>(bh) * p.N + qpos] = m_used * p.ln2 + logf(l);
+        }
       }
     }
   }
@@ -436,7 +515,13 @@ cudaError_t launch_fwd_dp(const FwdParams& p, cudaStream_t stream) {
   err = cudaFuncSetAttribute(fa_fwd_kernel<D, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
   if (err != cudaSuccess) return err;
-  const long long blocks = static_cast<long long>(p.n_qblk) * p.BH;
+  // Persistent CTAs: one per SM (the kernel holds all of tensor memory),
+  // each walking the work items (see fwd_item_index).
+  int dev = 0, sms = 0;
+  err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const int blocks = p.n_items < sms ? p.n_items : sms;
   fa_fwd_kernel<D, POLY><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

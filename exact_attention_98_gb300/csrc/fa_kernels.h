@@ -33,7 +33,8 @@ struct FwdParams {
   unsigned int* status;  // device status word
   int N;
   int BH;
-  int n_qblk;  // ceil(N / 256): each CTA takes two 128-row query tiles
+  int n_qblk;   // ceil(N / 256): a work item is two 128-row query tiles
+  int n_items;  // n_qblk * BH
   int causal;
   float c;          // scale * log2(e): scores enter exp2 in these units
   float ln2;        // ln(2), to turn the log2-unit row max into LSE
