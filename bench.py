@@ -62,8 +62,8 @@ def parse():
 # soon as any of them changes.
 NCU_TRAFFIC = {
     "kernel": "fa_bwd_kernel<128>",
-    "bytes": 202445056 + 85999360,
-    "sources_sha256": "d3202680892a9bad8f8aacee374909951af7cda1b0cc252673a4189f86cdc514",
+    "bytes": 202690048 + 84474880,
+    "sources_sha256": "82b4a08c39cc744ab66415e56580fad64e9d28fdda7a1956cef12a33c1aa2e02",
 }
 KERNEL_SOURCES = ("fa_bwd.cu", "fa_device.cuh", "fa_kernels.h", "exp2_poly_coeffs.h")
 
@@ -318,8 +318,26 @@ def native_arm(args):
         "bwd_main_tflops": cf_bwd / (statistics.median(c_bwd) * 1e-3) / 1e12,
     }
 
-    # end to end through the public API with pinned host buffers: H2D of
-    # q, k, v, dO, forward, backward, D2H of dQ, dK, dV every step
+    # The deterministic backward (all three of its kernels), same workload,
+    # L2 flushed before each launch; reported beside the headline.
+    ws_det = fa.workspace_for(qd, deterministic=True)
+    det_ms = []
+    for i in range(3 + 5):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fa.fa_bwd_deterministic(qd, kd, vd, o, lse, dod, dq, dk, dv, scale, False, ws_det)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            det_ms.append(e0.elapsed_time(e1))
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after the deterministic backward")
+    del ws_det
+    det_ms_med = statistics.median(det_ms)
+    deterministic_extra = {"bwd_tflops": f_bwd / (det_ms_med * 1e-3) / 1e12, "bwd_ms": det_ms_med,
+                           "note": "fa_bwd_deterministic, all kernels"}
+
     # End to end through the public calls: every step copies its own inputs
     # Q, K, V, dO from pinned host memory and its gradients dQ, dK, dV back.
     # Two forms are timed.  Serial: copies and kernels one after another on
@@ -449,6 +467,7 @@ def native_arm(args):
         "fwd_ms": fwd_med,
         "bwd_main_ms": bwd_med,
         "causal": causal_extra,
+        "deterministic": deterministic_extra,
         "roofline": {
             "kernel": "fa_bwd_kernel<128>",
             "bound": "tensor",

@@ -110,11 +110,13 @@ int poly_per_octet() {
 // fp32 dQ accumulator [BH, N, d] viewed as (d, N, BH); box 16 columns (64
 // bytes) x 128 rows x 1 head with 64-byte swizzle, for bulk reduce-adds.
 // Rows past N are dropped by the TMA unit.
-bool encode_dq_map(CUtensorMap* map, const float* base, int N, int BH, int d) {
+// fp32 [slices, N, d] with slices = BH (accumulator) or n_kblk * BH
+// (deterministic mode's per-key-tile contributions).
+bool encode_dq_map(CUtensorMap* map, const float* base, int N, long long slices, int d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(BH)};
+                              static_cast<cuuint64_t>(slices)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
                                  static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 4};
   const cuuint32_t box[3] = {16, 128, 1};
@@ -253,9 +255,20 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   return round_up(rows * sizeof(float)) + round_up(rows * d * sizeof(float));
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-           const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-           float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+size_t fa_bwd_deterministic_workspace_bytes(int B, int H, int N, int d) {
+  bool empty = false;
+  if (check_shape(B, H, N, d, 1.0f, &empty) != FA_OK || empty) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  const size_t n_kblk = (static_cast<size_t>(N) + kBlockN - 1) / kBlockN;
+  return round_up(rows * sizeof(float)) + round_up(n_kblk * rows * d * sizeof(float));
+}
+
+namespace {
+
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+             float scale, int causal, void* workspace, size_t workspace_bytes, void* stream,
+             bool deterministic) {
   bool empty = false;
   int rc = check_shape(B, H, N, d, scale, &empty);
   if (rc != FA_OK || empty) return rc;
@@ -264,32 +277,38 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
+  const size_t need = deterministic ? fa_bwd_deterministic_workspace_bytes(B, H, N, d)
+                                    : fa_bwd_workspace_bytes(B, H, N, d);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) != 0) return FA_ERR_WORKSPACE;
 
   const int BH = B * H;
   const long long rows = static_cast<long long>(BH) * N;
   float* dsum = static_cast<float*>(workspace);
-  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+  // After D: the dQ accumulator, or the per-key-tile contributions.
+  float* dq_buf = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                            round_up(static_cast<size_t>(rows) * sizeof(float)));
+  float* dq_acc = deterministic ? nullptr : dq_buf;
+  const int n_kblk = (N + kBlockN - 1) / kBlockN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   BwdParams p;
   if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
       !encode_tile_map(&p.tm_v, v, N, BH, d) || !encode_tile_map(&p.tm_do, dout, N, BH, d) ||
-      !encode_dq_map(&p.tm_dq, dq_acc, N, BH, d))
+      !encode_dq_map(&p.tm_dq, dq_buf, N,
+                     deterministic ? static_cast<long long>(n_kblk) * BH : BH, d))
     return FA_ERR_CUDA;
   p.lse = lse;
   p.dsum = dsum;
   p.dq_acc = dq_acc;
+  p.dq_part = deterministic ? dq_buf : nullptr;
   p.dk = dk;
   p.dv = dv;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   p.N = N;
   p.BH = BH;
-  p.n_kblk = (N + kBlockN - 1) / kBlockN;
+  p.n_kblk = n_kblk;
   p.causal = causal;
   p.c = scale * 1.4426950408889634f;
   p.scale = scale;
@@ -301,8 +320,30 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (timing_record(1, true, s) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_bwd_main(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
   if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
-  if (launch_bwd_post(dq_acc, dq, rows * d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (deterministic) {
+    if (launch_bwd_dq_reduce(dq_buf, dq, BH, N, d, n_kblk, causal, s) != cudaSuccess)
+      return FA_ERR_CUDA;
+  } else if (launch_bwd_post(dq_acc, dq, rows * d, s) != cudaSuccess) {
+    return FA_ERR_CUDA;
+  }
   return FA_OK;
+}
+
+}  // namespace
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                  workspace_bytes, stream, false);
+}
+
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                  workspace_bytes, stream, true);
 }
 
 int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,

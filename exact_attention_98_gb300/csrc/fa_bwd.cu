@@ -385,7 +385,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (!__all_sync(0xffffffffu, ok)) break;
         tc_fence_after();
         const int q0 = (i_first + it) * kBlockM;
-        float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.N + q0) * D + dcol;
+        const bool det = p.dq_part != nullptr;
+        float* acc = det ? p.dq_part + (static_cast<size_t>(kt * p.BH + bh) * p.N + q0) * D + dcol
+                         : p.dq_acc + (static_cast<size_t>(bh) * p.N + q0) * D + dcol;
         uint32_t r[4][32];
 #pragma unroll
         for (int b = 0; b < 4; ++b) tmem_ld32(t_dqt + b * 32, r[b]);
@@ -396,9 +398,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // dQ_i^T has left tensor memory: the MMA may write the columns again.
         tc_fence_before();
         mbar_arrive(bar(C::kBarDQEmpty));
+        if (det) {  // this key tile's contribution, summed later in key-tile order
 #pragma unroll
-        for (int qc = 0; qc < kBlockM; ++qc)
-          if (q0 + qc < p.N) atomicAdd(acc + static_cast<size_t>(qc) * D, __uint_as_float(r[qc >> 5][qc & 31]));
+          for (int qc = 0; qc < kBlockM; ++qc)
+            if (q0 + qc < p.N) acc[static_cast<size_t>(qc) * D] = __uint_as_float(r[qc >> 5][qc & 31]);
+        } else {
+#pragma unroll
+          for (int qc = 0; qc < kBlockM; ++qc)
+            if (q0 + qc < p.N)
+              atomicAdd(acc + static_cast<size_t>(qc) * D, __uint_as_float(r[qc >> 5][qc & 31]));
+        }
       }
     } else {
     for (int it = 0; it < n_iter; ++it) {
@@ -441,9 +450,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       named_bar_sync(C::kDrainBarrier, kBlockM);
       if (leader) {
         const int q0 = (i_first + it) * kBlockM;
+        if (p.dq_part != nullptr) {  // this key tile's contribution (see BwdParams)
 #pragma unroll 1
-        for (int ch = 0; ch < C::kDqChunks; ++ch)
-          tma_reduce_add_3d(&p.tm_dq, smem_u32(chunk_base(ch)), ch * C::kDqCols, q0, bh);
+          for (int ch = 0; ch < C::kDqChunks; ++ch)
+            tma_store_3d(&p.tm_dq, smem_u32(chunk_base(ch)), ch * C::kDqCols, q0, kt * p.BH + bh);
+        } else {
+#pragma unroll 1
+          for (int ch = 0; ch < C::kDqChunks; ++ch)
+            tma_reduce_add_3d(&p.tm_dq, smem_u32(chunk_base(ch)), ch * C::kDqCols, q0, bh);
+        }
         bulk_commit();
         bulk_wait_read<0>();  // the TMA has read the staged tile: stage s is free
         mbar_arrive(bar(C::kBarStEmpty + s));

@@ -3,6 +3,8 @@
 //   pre : D_i = sum_t dO_it * O_it  (fp32, from the bf16 O the forward wrote)
 //         and dQacc := 0
 //   post: dQ = dQacc -> bf16  (dS already carries the softmax scale)
+//   dq_reduce (deterministic mode): dQ = sum over key tiles, in key-tile
+//         order, of the per-key-tile contributions -> bf16
 //
 // D is the row term of dS = P * (dP - D): the softmax Jacobian applied to dP
 // (chain rule of the loss sum(O * dO) through P = softmax(S)).
@@ -41,9 +43,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       acc = fmaf(fa2.x, fb2.x, acc);
       acc = fmaf(fa2.y, fb2.y, acc);
     }
-    float4* z = reinterpret_cast<float4*>(dq_acc + row * D + col);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dq_acc != nullptr) {  // null in deterministic mode: nothing accumulates
+      float4* z = reinterpret_cast<float4*>(dq_acc + row * D + col);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 #pragma unroll
   for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
@@ -63,6 +67,37 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
     w.y = pack_bf16x2(a.z, a.w);
     w.z = pack_bf16x2(b.x, b.y);
     w.w = pack_bf16x2(b.z, b.w);
+    reinterpret_cast<uint4*>(dq)[i] = w;
+  }
+}
+
+// One thread per 8 consecutive d of one row: the contributions of key tiles
+// 0, 1, ... are added in that order (fp32), so the result does not depend on
+// the order in which the key tiles ran.
+__global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float* __restrict__ part,
+                                                            __nv_bfloat16* __restrict__ dq,
+                                                            int BH, int N, int d, int n_kblk,
+                                                            int causal, long long n8) {
+  const int per_row = d / 8;
+  const size_t slice = static_cast<size_t>(BH) * N * d;  // one key tile's contributions
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = i / per_row;  // (bh, q)
+    const int q = static_cast<int>(row % N);
+    const int nc = causal ? min(n_kblk, q / kBlockN + 1) : n_kblk;
+    const float* src = part + static_cast<size_t>(i) * 8;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int kt = 0; kt < nc; ++kt) {
+      const float4 x = reinterpret_cast<const float4*>(src + kt * slice)[0];
+      const float4 y = reinterpret_cast<const float4*>(src + kt * slice)[1];
+      a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+      a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+    }
+    uint4 w;
+    w.x = pack_bf16x2(a[0], a[1]);
+    w.y = pack_bf16x2(a[2], a[3]);
+    w.z = pack_bf16x2(a[4], a[5]);
+    w.w = pack_bf16x2(a[6], a[7]);
     reinterpret_cast<uint4*>(dq)[i] = w;
   }
 }
@@ -98,6 +133,14 @@ cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, cuda
   const long long n8 = elems / 8;  // d is a multiple of 8, so elems is too
   bwd_post_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
                                                          n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, int n_kblk,
+                                 int causal, cudaStream_t stream) {
+  const long long n8 = static_cast<long long>(BH) * N * d / 8;
+  bwd_dq_reduce_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(
+      dq_part, static_cast<__nv_bfloat16*>(dq), BH, N, d, n_kblk, causal, n8);
   return cudaGetLastError();
 }
 

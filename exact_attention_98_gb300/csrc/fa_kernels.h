@@ -51,10 +51,16 @@ struct BwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
-  CUtensorMap tm_dq;  // fp32 dQ accumulator [BH, N, d], box {16, 128, 1}, 64B swizzle
+  // fp32 dQ target, box {16, 128, 1}, 64B swizzle: the accumulator
+  // [BH, N, d], or in deterministic mode the partial sums [n_kblk * BH, N, d]
+  CUtensorMap tm_dq;
   const float* lse;   // fp32 [BH, N]
   const float* dsum;  // fp32 [BH, N]: D = rowsum(dO * O)
-  float* dq_acc;      // fp32 [BH, N, d], zeroed before the main kernel
+  float* dq_acc;      // fp32 [BH, N, d], zeroed before the main kernel (atomic mode)
+  // Deterministic mode (dq_part != nullptr): key tile kt of head bh writes
+  // its dQ contribution to dq_part[kt * BH + bh] (plain stores, no atomics);
+  // a second kernel adds the contributions in key-tile order.
+  float* dq_part;     // fp32 [n_kblk * BH, N, d]
   void* dk;           // bf16 [BH, N, d]
   void* dv;           // bf16 [BH, N, d]
   unsigned int* status;
@@ -78,5 +84,10 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* 
 cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
 // dQ = dQ accumulator -> bf16.
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, cudaStream_t stream);
+// Deterministic mode: dQ = sum over key tiles kt = 0, 1, ... (in that order)
+// of dq_part[kt] -> bf16.  Causal: query tile i has contributions from
+// kt <= i only.
+cudaError_t launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, int n_kblk,
+                                 int causal, cudaStream_t stream);
 
 }  // namespace fa

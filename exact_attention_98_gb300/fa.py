@@ -60,6 +60,11 @@ def _load() -> ctypes.CDLL:
     lib.fa_exp2_poly_eval.restype = i
     lib.fa_debug_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
     lib.fa_debug_bounded_wait.restype = i
+    lib.fa_bwd_deterministic_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_bwd_deterministic_workspace_bytes.restype = sz
+    lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp,
+                                         sz, vp]
+    lib.fa_bwd_deterministic.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_bwd_noalloc.restype = i
     lib.fa_timing_enable.argtypes = [i]
@@ -143,6 +148,25 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool, worksp
                       _ptr(workspace), ws_bytes, _stream(stream)), "fa_bwd")
 
 
+def fa_bwd_deterministic_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib.fa_bwd_deterministic_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool,
+                         workspace, stream=None) -> None:
+    """fa_bwd with run-to-run bit-identical results (no dQ atomics)."""
+    B, H, N, d = _shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
+    _check_tensor(lse, "lse", torch.float32, (B, H, N))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                    int(bool(causal)), _ptr(workspace), ws_bytes,
+                                    _stream(stream)), "fa_bwd_deterministic")
+
+
 def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool,
                    stream=None) -> None:
     """fa_bwd with the library's fixed scratch array instead of a caller
@@ -211,20 +235,23 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
     return o, lse
 
 
-def workspace_for(q):
+def workspace_for(q, deterministic: bool = False):
     B, H, N, d = _shape(q)
-    n = fa_bwd_workspace_bytes(B, H, N, d)
+    n = (fa_bwd_deterministic_workspace_bytes if deterministic else fa_bwd_workspace_bytes)(
+        B, H, N, d)
     # torch's caching allocator hands out 512-byte aligned blocks
     return torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
 
 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
-             workspace=None, stream=None):
-    """Returns (dq, dk, dv) freshly allocated on q's device."""
+             workspace=None, stream=None, deterministic: bool = False):
+    """Returns (dq, dk, dv) freshly allocated on q's device.  deterministic:
+    fa_bwd_deterministic (bit-identical from run to run) instead of fa_bwd."""
     B, H, N, d = _shape(q)
     scale = default_scale(d) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     if workspace is None:
-        workspace = workspace_for(q)
-    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale, causal, workspace, stream)
+        workspace = workspace_for(q, deterministic)
+    run = fa_bwd_deterministic if deterministic else fa_bwd
+    run(q, k, v, o, lse, dout, dq, dk, dv, scale, causal, workspace, stream)
     return dq, dk, dv

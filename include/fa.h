@@ -91,6 +91,32 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of device workspace fa_bwd_deterministic needs: fp32 D [B, H, N] and
+ * one fp32 dQ contribution per key tile, ceil(N / 128) x [B, H, N, d], each
+ * part 256-byte aligned (at B2 H16 N4096 d128 about 2.1 GB).  Returns 0 for
+ * empty or unsupported shapes.
+ */
+size_t fa_bwd_deterministic_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward with results that are bit-identical from run to run.  The pages
+ * single out the backward's dQ reduction (fp32 atomic adds from every key
+ * tile, whose order varies between runs) as a cost ("FlashAttention-3 и
+ * FlashAttention-4", section "Режим 2-CTA MMA"); here each key tile writes
+ * its dQ contribution with plain stores and a second kernel adds the
+ * contributions in key-tile order (causal: key tiles 0..i for query tile i).
+ * dK and dV are deterministic in both entry points (each key tile owns its
+ * rows and accumulates them in a fixed order).
+ * Same arguments, results and errors as fa_bwd; the workspace must hold
+ * fa_bwd_deterministic_workspace_bytes(B, H, N, d) bytes.  Slower than fa_bwd
+ * by the extra memory traffic of the contributions.
+ */
+int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * Backward without any allocation, for callers that cannot allocate device
  * memory: plugin hosts that hand a library its input and output buffers but
  * no allocator and no workspace, and latency-critical loops where a

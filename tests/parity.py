@@ -105,8 +105,9 @@ def compare_fwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_
     return worst_o, worst_l
 
 
-def run_bwd(B, H, N, d, causal, seed=0, stress=False, scale=None):
-    """GPU forward then backward; O and LSE come from this library's forward."""
+def run_bwd(B, H, N, d, causal, seed=0, stress=False, scale=None, deterministic=False):
+    """GPU forward then backward; O and LSE come from this library's forward.
+    deterministic: the backward runs through fa_bwd_deterministic."""
     from exact_attention_98_gb300 import fa
 
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -114,18 +115,19 @@ def run_bwd(B, H, N, d, causal, seed=0, stress=False, scale=None):
     dev = torch.device("cuda")
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     o, lse = fa.forward(qd, kd, vd, causal=causal, scale=scale)
-    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale,
+                             deterministic=deterministic)
     status = fa.fa_last_device_status()
     assert status == fa.FA_OK, fa.status_string(status)
     return (q, k, v, do), (to64(dq), to64(dk), to64(dv)), scale
 
 
 def compare_bwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_per_head=None,
-                kv_heads=()):
+                kv_heads=(), deterministic=False):
     """Backward parity.  Heads with index < full_heads (None = all) compare
     every row of dQ, dK, dV; other heads compare sampled dQ rows, and the
     heads listed in kv_heads also sampled dK/dV rows."""
-    inputs, grads, scale = run_bwd(B, H, N, d, causal, seed, stress)
+    inputs, grads, scale = run_bwd(B, H, N, d, causal, seed, stress, deterministic=deterministic)
     q64, k64, v64, do64 = (t.double().numpy() for t in inputs)
     dq, dk, dv = grads
     worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0}

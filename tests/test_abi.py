@@ -54,6 +54,11 @@ def test_workspace_bytes(lib):
     assert ws(1, 1, 1, 64) == 256 + 256
     assert ws(0, 1, 1, 64) == 0
     assert ws(1, 1, 1, 96) == 0  # unsupported head dim
+    det = lib.fa_bwd_deterministic_workspace_bytes
+    n_kblk = (N + 127) // 128
+    assert det(B, H, N, d) == up(4 * rows) + up(4 * rows * d * n_kblk)
+    assert det(1, 1, 129, 64) == up(4 * 129) + up(4 * 129 * 64 * 2)
+    assert det(0, 1, 1, 64) == 0
 
 
 P = ctypes.c_void_p
@@ -96,6 +101,18 @@ def test_bwd_validation(lib):
     assert bwd(lib, dq=0) == lib.FA_ERR_INVALID_ARG
     assert bwd(lib, scale=-1.0) == lib.FA_ERR_INVALID_ARG
     assert bwd(lib, N=0, dq=0, ws=0) == lib.FA_OK
+
+
+def test_bwd_deterministic_validation(lib):
+    a = P(0x1000)
+    need = lib.fa_bwd_deterministic_workspace_bytes(1, 1, 256, 64)
+    call = lambda ws, nbytes, d=64: lib.lib.fa_bwd_deterministic(
+        a, a, a, a, a, a, a, a, a, 1, 1, 256, d, 0.125, 0, P(ws), nbytes, None)
+    assert call(0, need) == lib.FA_ERR_WORKSPACE
+    assert call(0x10000, need - 1) == lib.FA_ERR_WORKSPACE
+    # the atomic backward's smaller workspace is not enough
+    assert call(0x10000, lib.fa_bwd_workspace_bytes(1, 1, 256, 64)) == lib.FA_ERR_WORKSPACE
+    assert call(0x10000, need, d=96) == lib.FA_ERR_UNSUPPORTED
 
 
 def test_diagnostics_validation(lib):
