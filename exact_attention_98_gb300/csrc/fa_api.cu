@@ -213,8 +213,40 @@ const char* fa_status_string(int status) {
   }
 }
 
+namespace {
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, float scale, int causal, int num_splits, void* workspace,
+             size_t workspace_bytes, void* stream);
+
+}  // namespace
+
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, float scale, int causal, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, 0, stream);
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
+  bool empty = false;
+  if (check_shape(B, H, N, d, 1.0f, &empty) != FA_OK || empty) return 0;
+  if (num_splits < 1) return 0;
+  if (num_splits == 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return round_up(num_splits * rows * d * sizeof(float)) + round_up(num_splits * rows * sizeof(float));
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, float scale, int causal, int num_splits, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,
+                  workspace_bytes, stream);
+}
+
+namespace {
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, float scale, int causal, int num_splits, void* workspace,
+             size_t workspace_bytes, void* stream) {
   bool empty = false;
   int rc = check_shape(B, H, N, d, scale, &empty);
   if (rc != FA_OK || empty) return rc;
@@ -222,14 +254,29 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
     return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  const int n_ktiles = (N + kBlockN - 1) / kBlockN;
+  if (num_splits < 1 || num_splits > n_ktiles) return FA_ERR_INVALID_ARG;
+  if (num_splits > 1) {
+    const size_t need = fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits);
+    if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) != 0) return FA_ERR_WORKSPACE;
+  }
 
   FwdParams p;
   const int BH = B * H;
   if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
       !encode_tile_map(&p.tm_v, v, N, BH, d))
     return FA_ERR_CUDA;
+  const long long rows = static_cast<long long>(BH) * N;
   p.o = o;
   p.lse = lse;
+  p.num_splits = num_splits;
+  p.o_part = num_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  p.lse_part = num_splits > 1
+                   ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                              round_up(static_cast<size_t>(num_splits) * rows * d *
+                                                       sizeof(float)))
+                   : nullptr;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   p.N = N;
@@ -239,14 +286,19 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.c = scale * 1.4426950408889634f;
   p.ln2 = 0.6931471805599453f;
   p.poly_per_octet = poly_per_octet();
-  if (static_cast<long long>(p.n_qblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  p.n_items = p.n_qblk * BH;
+  if (static_cast<long long>(p.n_qblk) * BH * num_splits > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  p.n_items = p.n_qblk * BH * num_splits;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (timing_record(0, true, s) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_fwd(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (num_splits > 1 &&
+      launch_fwd_merge(p.o_part, p.lse_part, o, lse, num_splits, rows, d, s) != cudaSuccess)
+    return FA_ERR_CUDA;
   if (timing_record(0, false, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
+
+}  // namespace
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   bool empty = false;

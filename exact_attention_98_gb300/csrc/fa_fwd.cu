@@ -96,28 +96,38 @@ enum : unsigned int {
   kSiteQEmpty = 0x108,
 };
 
-// Work item w = two 128-row query tiles of one (batch, head).  Non-causal:
-// head-major, so that the query blocks of one head are processed together and
-// share its K and V in L2.  Causal: the heaviest blocks (the last query
-// blocks, which see the most keys) of every head first.
+// Work item w = two 128-row query tiles of one (batch, head) and one of the
+// num_splits contiguous key-tile ranges (w = block * num_splits + split).
+// Blocks: non-causal head-major, so that the query blocks of one head are
+// processed together and share its K and V in L2; causal, the heaviest
+// blocks (the last query blocks, which see the most keys) of every head
+// first.  With num_splits = 1 an item sees all keys its rows may attend to.
 struct FwdItem {
   int bh;
   int q0;
-  int nkv0, nkv1;  // key tiles seen by query tile 0 and 1 (0: tile past N)
+  int kb;          // first key tile of the item's range
+  int nkv0, nkv1;  // key tiles of the range seen by query tile 0 and 1 (0: none)
   int nmax;
   __device__ __forceinline__ int nkv(int t) const { return t ? nkv1 : nkv0; }
 };
 
 __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int w, int n_ktiles) {
   FwdItem it;
-  it.bh = p.causal ? w % p.BH : w / p.n_qblk;
-  const int qblk = p.n_qblk - 1 - (p.causal ? w / p.BH : w % p.n_qblk);
+  const int split = w % p.num_splits;
+  const int blk = w / p.num_splits;
+  it.bh = p.causal ? blk % p.BH : blk / p.n_qblk;
+  const int qblk = p.n_qblk - 1 - (p.causal ? blk / p.BH : blk % p.n_qblk);
   it.q0 = qblk * 2 * kBlockM;
-  auto nkv_of = [&](int qs) {
+  // key tiles [0, end) a query tile starting at qs attends to
+  auto end_of = [&](int qs) {
     return qs >= p.N ? 0 : (p.causal ? min(n_ktiles, qs / kBlockN + 1) : n_ktiles);
   };
-  it.nkv0 = nkv_of(it.q0);
-  it.nkv1 = nkv_of(it.q0 + kBlockM);
+  const int end0 = end_of(it.q0);
+  const int end1 = end_of(it.q0 + kBlockM);
+  const int per = (max(end0, end1) + p.num_splits - 1) / p.num_splits;
+  it.kb = split * per;
+  it.nkv0 = max(0, min(end0 - it.kb, per));
+  it.nkv1 = max(0, min(end1 - it.kb, per));
   it.nmax = max(it.nkv0, it.nkv1);
   return it;
 }
@@ -184,20 +194,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
       const uint32_t q_smem = sbase + C::kQOff;
-      int gidx = 0, issued = 0, items_loaded = 0;
+      int gidx = 0, issued = 0, items_loaded = 0, q_items = 0;
       bool ok = true;
       for (int round = 0; ok; ++round) {
         const int wi = fwd_item_index(round);
         if (wi >= p.n_items) break;
         const FwdItem item = fwd_item(p, wi, n_ktiles);
-        if (round > 0 && !(ok = mbar_wait(bar(C::kBarQEmpty), (round - 1) & 1, ctl, kSiteQEmpty)))
+        if (item.nmax == 0) continue;  // a key range past every row's keys
+        if (q_items > 0 && !(ok = mbar_wait(bar(C::kBarQEmpty), (q_items - 1) & 1, ctl, kSiteQEmpty)))
           break;
         mbar_arrive_expect_tx(bar(C::kBarQFull), 2 * C::kTileBytes);
         for (int t = 0; t < 2; ++t)
           for (int h = 0; h < D / 64; ++h)
             tma_load_3d(q_smem + t * C::kTileBytes + h * C::kHalfBytes, &p.tm_q, bar(C::kBarQFull),
                         h * 64, item.q0 + t * kBlockM, item.bh);
-        items_loaded = round + 1;
+        items_loaded = ++q_items;
         for (int idx = 0; idx < 2 * item.nmax; ++idx, ++gidx) {
           const int slot = gidx % C::kSlots;
           const int use = gidx / C::kSlots;
@@ -208,8 +219,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           const uint32_t dst = sbase + C::kRingOff + slot * C::kTileBytes;
           mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
           for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(dst + h * C::kHalfBytes, map, bar(C::kBarFull + slot), h * 64, j * kBlockN,
-                        item.bh);
+            tma_load_3d(dst + h * C::kHalfBytes, map, bar(C::kBarFull + slot), h * 64,
+                        (item.kb + j) * kBlockN, item.bh);
           issued = gidx + 1;
         }
       }
@@ -264,13 +275,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // warpgroup has read O_t of the previous item (its epilogue) before it
       // releases P_t(0).  S_t(0) of an item may run during that epilogue.
       bool ok = true;
-      int base = 0;
+      int base = 0, q_items = 0;
       int np0 = 0, np1 = 0;
       for (int round = 0; ok; ++round) {
         const int wi = fwd_item_index(round);
         if (wi >= p.n_items) break;
         const FwdItem item = fwd_item(p, wi, n_ktiles);
-        ok = mbar_wait(bar(C::kBarQFull), round & 1, ctl, kSiteQFull);
+        if (item.nmax == 0) continue;
+        ok = mbar_wait(bar(C::kBarQFull), (q_items++) & 1, ctl, kSiteQFull);
         if (ok) ok = mbar_wait(bar(C::kBarFull + slot_of(base)), parity_of(base), ctl, kSiteKFull);
         if (!ok) break;
         tc_fence_after();
@@ -340,18 +352,32 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     for (int round = 0; ok; ++round) {
       const int wi = fwd_item_index(round);
       if (wi >= p.n_items) break;
-      // Key tiles of this warpgroup's query tile.  Kept in a small array
-      // indexed by t (so in local memory, like a spill slot): one more live
-      // register in the tile loop below makes ptxas spill about 25 others.
+      // Key tiles of this warpgroup's query tile in the item's range, the
+      // range's first key tile and the item's first diagonal key tile, kept
+      // in a small volatile array (so in local memory, like a spill slot):
+      // more live registers in the tile loop below make ptxas spill about 25
+      // others.
       const FwdItem itm = fwd_item(p, wi, n_ktiles);
-      int nkv_arr[2] = {itm.nkv0, itm.nkv1};
-      if (nkv_arr[t] == 0) continue;
-
+      volatile int iv[4] = {itm.nkv0, itm.nkv1, itm.kb, itm.q0 / kBlockN};
+      if (iv[t] == 0) {
+        // Split mode: an empty key range still leaves its partial result
+        // for the merge (weight exp(-inf) = 0).
+        const int qp = itm.q0 + t * kBlockM + row;
+        if (p.o_part != nullptr && qp < p.N) {
+          const size_t prow = static_cast<size_t>(wi % p.num_splits) * p.BH * p.N +
+                              static_cast<size_t>(itm.bh) * p.N + qp;
+          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll 1
+          for (int v4 = 0; v4 < D / 4; ++v4) dst[v4] = make_float4(0.f, 0.f, 0.f, 0.f);
+          p.lse_part[prow] = -INFINITY;
+        }
+        continue;
+      }
       float m_used = -INFINITY;  // running row max in log2 units (scores * c)
       // row sum of exp2(x - m_used): four f32x2 accumulators (eight partial sums)
       f32x2 l2[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
                      f2_pack(0.0f, 0.0f)};
-      for (int j = 0; j < nkv_arr[t]; ++j) {
+      for (int j = 0; j < iv[t]; ++j) {
         ok = mbar_wait(bar(C::kBarSFull + t), phase & 1u, ctl, kSiteSFull);
         phase ^= 1u;
         ok = __all_sync(0xffffffffu, ok);
@@ -366,9 +392,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         reg_fence(r[2]);
         reg_fence(r[3]);
 
-        const bool edge = (p.causal && j == nkv_arr[t] - 1) || (ragged && j == n_ktiles - 1);
+        const int jabs = iv[2] + j;  // key tile index
+        const bool edge = (p.causal && jabs == iv[3] + t) || (ragged && jabs == n_ktiles - 1);
         if (edge) {
-          const int kbase = j * kBlockN;
+          const int kbase = jabs * kBlockN;
           const int qpos = fwd_item(p, wi, n_ktiles).q0 + t * kBlockM + row;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch)
@@ -471,25 +498,51 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           const int bh = item.bh;
           const int qpos = item.q0 + t * kBlockM + row;
           const bool in_range = qpos < p.N;
-          __nv_bfloat16* orow =
-              static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
+          const float lse_row = m_used * p.ln2 + logf(l);
+          if (p.o_part == nullptr) {
+            __nv_bfloat16* orow =
+                static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
 #pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(t_o + ch * 32, r);
-            tmem_ld_wait(r);
-            uint32_t w[16];
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t r[32];
+              tmem_ld32(t_o + ch * 32, r);
+              tmem_ld_wait(r);
+              uint32_t w[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-            if (in_range) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+              for (int e = 0; e < 16; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
+                                   __uint_as_float(r[2 * e + 1]) * inv_l);
+              if (in_range) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
-              for (int v4 = 0; v4 < 4; ++v4)
-                dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                for (int v4 = 0; v4 < 4; ++v4)
+                  dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+              }
             }
+            if (in_range) p.lse[static_cast<size_t>(bh) * p.N + qpos] = lse_row;
+          } else {
+            // Split mode: this key range's O (normalised over the range) and
+            // LSE in fp32, for the merge.
+            const size_t prow = static_cast<size_t>(wi % p.num_splits) * p.BH * p.N +
+                                static_cast<size_t>(bh) * p.N + qpos;
+            float* orow = p.o_part + prow * D;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t r[32];
+              tmem_ld32(t_o + ch * 32, r);
+              tmem_ld_wait(r);
+              if (in_range) {
+                float4* dst = reinterpret_cast<float4*>(orow + ch * 32);
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4)
+                  dst[v4] = make_float4(__uint_as_float(r[4 * v4]) * inv_l,
+                                        __uint_as_float(r[4 * v4 + 1]) * inv_l,
+                                        __uint_as_float(r[4 * v4 + 2]) * inv_l,
+                                        __uint_as_float(r[4 * v4 + 3]) * inv_l);
+              }
+            }
+            if (in_range) p.lse_part[prow] = lse_row;
           }
-          if (in_range) p.lse[static_cast<size_t>(bh) * p.N + qpos] = m_used * p.ln2 + logf(l);
         }
       }
     }
@@ -543,6 +596,60 @@ cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
   if (d == 128) return launch_fwd_d<128>(p, stream);
   if (d == 64) return launch_fwd_d<64>(p, stream);
   return cudaErrorInvalidValue;
+}
+
+namespace {
+
+// Split-KV merge, one thread per 8 consecutive columns of one row: the
+// ranges' LSEs give the weights exp(LSE_s - max) (0 for an empty range),
+// their sum the row's LSE; O is the weighted mean of the ranges' O.
+__global__ void __launch_bounds__(256) fwd_merge_kernel(const float* __restrict__ o_part,
+                                                        const float* __restrict__ lse_part,
+                                                        __nv_bfloat16* __restrict__ o,
+                                                        float* __restrict__ lse, int num_splits,
+                                                        long long rows, int d) {
+  const int per_row = d / 8;
+  const long long n8 = rows * per_row;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = i / per_row;
+    const int col = static_cast<int>(i % per_row) * 8;
+    float m = -INFINITY;
+    for (int s = 0; s < num_splits; ++s) m = fmaxf(m, lse_part[s * rows + row]);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float wsum = 0.0f;
+    for (int s = 0; s < num_splits; ++s) {
+      const float ls = lse_part[s * rows + row];
+      if (ls == -INFINITY) continue;
+      const float w = expf(ls - m);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(o_part + (s * rows + row) * d + col);
+      const float4 x = src[0], y = src[1];
+      acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+      acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
+    }
+    const float inv = 1.0f / wsum;
+    uint4 out;
+    out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(o + row * d + col) = out;
+    if (col == 0) lse[row] = m + logf(wsum);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                             int num_splits, long long rows, int d, cudaStream_t stream) {
+  const long long n8 = rows * (d / 8);
+  long long blocks = (n8 + 255) / 256;
+  const long long cap = 152LL * 8;
+  if (blocks > cap) blocks = cap;
+  fwd_merge_kernel<<<static_cast<unsigned int>(blocks < 1 ? 1 : blocks), 256, 0, stream>>>(
+      o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, num_splits, rows, d);
+  return cudaGetLastError();
 }
 
 }  // namespace fa

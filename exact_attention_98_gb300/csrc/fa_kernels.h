@@ -34,7 +34,16 @@ struct FwdParams {
   int N;
   int BH;
   int n_qblk;   // ceil(N / 256): a work item is two 128-row query tiles
-  int n_items;  // n_qblk * BH
+  int n_items;  // n_qblk * BH * num_splits
+  // Split-KV: each query tile's key tiles are cut into num_splits contiguous
+  // ranges, one work item each.  With num_splits > 1 the kernel writes, per
+  // range, O normalised over the range and its LSE in fp32 to o_part
+  // [num_splits, BH, N, d] and lse_part [num_splits, BH, N]; a merge kernel
+  // combines them.  num_splits = 1: o_part = lse_part = nullptr, results go
+  // straight to o and lse.
+  int num_splits;
+  float* o_part;
+  float* lse_part;
   int causal;
   float c;          // scale * log2(e): scores enter exp2 in these units
   float ln2;        // ln(2), to turn the log2-unit row max into LSE
@@ -76,6 +85,10 @@ struct BwdParams {
 
 // Forward: one launch of the tcgen05 kernel for head dim d (64 or 128).
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
+// Split-KV merge: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s
+// -> bf16 O and fp32 LSE.
+cudaError_t launch_fwd_merge(const float* o_part, const float* lse_part, void* o, float* lse,
+                             int num_splits, long long rows, int d, cudaStream_t stream);
 
 // Backward: D = rowsum(dO * O) and dQ accumulator zeroing.
 cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* dq_acc,

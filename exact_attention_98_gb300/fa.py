@@ -46,6 +46,10 @@ def _load() -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_splitkv_workspace_bytes.restype = sz
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+    lib.fa_fwd_splitkv.restype = i
     lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
@@ -129,6 +133,22 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
     _check_tensor(lse, "lse", torch.float32, (B, H, N))
     _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
                       int(bool(causal)), _stream(stream)), "fa_fwd")
+
+
+def fa_fwd_splitkv_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int) -> int:
+    return int(lib.fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, scale: float, causal: bool, num_splits: int, workspace,
+                   stream=None) -> None:
+    B, H, N, d = _shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
+    _check_tensor(lse, "lse", torch.float32, (B, H, N))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                              float(scale), int(bool(causal)), int(num_splits), _ptr(workspace),
+                              ws_bytes, _stream(stream)), "fa_fwd_splitkv")
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
@@ -225,13 +245,20 @@ def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
-    """Returns (o, lse) freshly allocated on q's device."""
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None,
+            num_splits: int = 1):
+    """Returns (o, lse) freshly allocated on q's device.  num_splits > 1:
+    split-KV forward (fa_fwd_splitkv) with a freshly allocated workspace."""
     B, H, N, d = _shape(q)
     scale = default_scale(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    if num_splits == 1:
+        fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    else:
+        n = fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
+        fa_fwd_splitkv(q, k, v, o, lse, scale, causal, num_splits, ws, stream)
     return o, lse
 
 

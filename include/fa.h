@@ -64,6 +64,28 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int N, int d, float scale, int causal, void* stream);
 
 /*
+ * Split-KV forward: the same results as fa_fwd (within rounding), computed
+ * with each query tile's key tiles cut into num_splits contiguous ranges
+ * that run as separate work items, for problems with too few (batch, head,
+ * query-block) items to fill the GPU, such as long context with few heads.
+ * Each range leaves O normalised over the range and its LSE (fp32) in the
+ * workspace; a merge kernel combines them by log-sum-exp:
+ *   LSE = ln sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
+ * ("FlashAttention-4: Algorithm and Kernel Pipelining Co-Design", abstract:
+ * long-context attention; the merge is the online-softmax rescaling of the
+ * same pages applied across ranges).
+ *   num_splits: 1 .. ceil(N / 128); 1 runs fa_fwd (workspace unused).
+ *   workspace : at least fa_fwd_splitkv_workspace_bytes() bytes, 256-byte
+ *               aligned, owned by the caller, contents on entry irrelevant.
+ * Errors as fa_fwd, plus FA_ERR_INVALID_ARG for num_splits out of range and
+ * FA_ERR_WORKSPACE for a missing, short or misaligned workspace.
+ */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, float scale, int causal, int num_splits, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: fp32 D = rowsum(dO * O) [B, H, N]
  * and the fp32 dQ accumulator [B, H, N, d], each 256-byte aligned.
  * Returns 0 for empty or unsupported shapes.

@@ -72,22 +72,25 @@ def to64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def run_fwd(B, H, N, d, causal, seed=0, stress=False, scale=None):
+def run_fwd(B, H, N, d, causal, seed=0, stress=False, scale=None, num_splits=1):
     from exact_attention_98_gb300 import fa
 
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     q, k, v, _ = attention_inputs(B, H, N, d, seed=seed, stress=stress, with_dout=False)
     dev = torch.device("cuda")
-    o, lse = fa.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale)
+    o, lse = fa.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale,
+                        num_splits=num_splits)
     status = fa.fa_last_device_status()
     assert status == fa.FA_OK, fa.status_string(status)
     return (q, k, v), to64(o), to64(lse), scale
 
 
-def compare_fwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_per_head=None):
+def compare_fwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_per_head=None,
+                num_splits=1):
     """Forward parity.  full_heads: number of leading (b, h) slices compared on
-    every row (None = all); the others on sampled rows."""
-    (q, k, v), o, lse, scale = run_fwd(B, H, N, d, causal, seed, stress)
+    every row (None = all); the others on sampled rows.  num_splits > 1: the
+    split-KV forward."""
+    (q, k, v), o, lse, scale = run_fwd(B, H, N, d, causal, seed, stress, num_splits=num_splits)
     q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
     worst_o = worst_l = 0.0
     for b in range(B):

@@ -115,6 +115,29 @@ def test_bwd_deterministic_validation(lib):
     assert call(0x10000, need, d=96) == lib.FA_ERR_UNSUPPORTED
 
 
+def test_splitkv_workspace_bytes(lib):
+    ws = lib.fa_fwd_splitkv_workspace_bytes
+    up = lambda x: (x + 255) // 256 * 256
+    B, H, N, d = 1, 4, 16384, 128
+    rows = B * H * N
+    assert ws(B, H, N, d, 8) == up(8 * rows * d * 4) + up(8 * rows * 4)
+    assert ws(B, H, N, d, 1) == 0  # one range: fa_fwd, no workspace
+    assert ws(B, H, N, d, 0) == 0
+    assert ws(B, H, N, 96, 2) == 0
+
+
+def test_splitkv_validation(lib):
+    a = P(0x1000)
+    call = lambda splits, ws, nbytes: lib.lib.fa_fwd_splitkv(
+        a, a, a, a, a, 1, 1, 300, 64, 0.125, 0, splits, P(ws), nbytes, None)
+    need = lib.fa_fwd_splitkv_workspace_bytes(1, 1, 300, 64, 2)
+    assert call(0, 0x10000, need) == lib.FA_ERR_INVALID_ARG
+    assert call(4, 0x10000, need) == lib.FA_ERR_INVALID_ARG  # 3 key tiles
+    assert call(2, 0, need) == lib.FA_ERR_WORKSPACE
+    assert call(2, 0x10000, need - 1) == lib.FA_ERR_WORKSPACE
+    assert call(2, 0x10010, need) == lib.FA_ERR_WORKSPACE
+
+
 def test_diagnostics_validation(lib):
     assert lib.lib.fa_exp2_poly_eval(P(0), P(0), -1, None) == lib.FA_ERR_INVALID_ARG
     assert lib.lib.fa_exp2_poly_eval(P(0), P(0), 0, None) == lib.FA_OK
