@@ -96,6 +96,23 @@ bool encode_tile_map(CUtensorMap* map, const void* base, int N, int BH, int d) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 8-bit [slices, rows, cols] tensor, rows of `pitch` bytes, box 128 x 128:
+// one 128-byte swizzle row per tile row (the FP8 forward's e4m3 operands).
+bool encode_u8_map(CUtensorMap* map, const void* base, long long cols, long long rows,
+                   long long slices, long long pitch) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(slices)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch),
+                                 static_cast<cuuint64_t>(pitch) * static_cast<cuuint64_t>(rows)};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Share of the forward's exponentials on the FMA pipe, per 8 (env override).
 int poly_per_octet() {
   static std::once_flag once;
@@ -107,11 +124,11 @@ int poly_per_octet() {
   return value;
 }
 
-// fp32 dQ accumulator [BH, N, d] viewed as (d, N, BH); box 16 columns (64
-// bytes) x 128 rows x 1 head with 64-byte swizzle, for bulk reduce-adds.
-// Rows past N are dropped by the TMA unit.
-// fp32 [slices, N, d] with slices = BH (accumulator) or n_kblk * BH
-// (deterministic mode's per-key-tile contributions).
+// fp32 [slices, N, d] viewed as (d, N, slices), slices = BH (the dQ
+// accumulator) or n_kblk * BH (the deterministic mode's per-key-tile
+// contributions); box 16 columns (64 bytes) x 128 rows x 1 slice with 64-byte
+// swizzle, for bulk reduce-adds and stores.  Rows past N are dropped by the
+// TMA unit.
 bool encode_dq_map(CUtensorMap* map, const float* base, int N, long long slices, int d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -217,7 +234,7 @@ namespace {
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, float scale, int causal, int num_splits, void* workspace,
-             size_t workspace_bytes, void* stream);
+             size_t workspace_bytes, void* stream, int fp8 = 0, int rotate = 0);
 
 }  // namespace
 
@@ -235,6 +252,24 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits
   return round_up(num_splits * rows * d * sizeof(float)) + round_up(num_splits * rows * sizeof(float));
 }
 
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
+  bool empty = false;
+  if (check_shape(B, H, N, d, 1.0f, &empty) != FA_OK || empty || d != 128) return 0;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t rows = BH * N;
+  const size_t Np = (static_cast<size_t>(N) + 15) / 16 * 16;
+  return 2 * round_up(rows * 128) + round_up(BH * 128 * Np) + round_up(rows * sizeof(float)) +
+         round_up(2 * BH * sizeof(unsigned int));
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, int rotate, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  if (rotate != 0 && rotate != 1) return FA_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, 1, workspace, workspace_bytes, stream,
+                  1, rotate);
+}
+
 int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int N, int d, float scale, int causal, int num_splits, void* workspace,
                    size_t workspace_bytes, void* stream) {
@@ -246,7 +281,7 @@ namespace {
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, float scale, int causal, int num_splits, void* workspace,
-             size_t workspace_bytes, void* stream) {
+             size_t workspace_bytes, void* stream, int fp8, int rotate) {
   bool empty = false;
   int rc = check_shape(B, H, N, d, scale, &empty);
   if (rc != FA_OK || empty) return rc;
@@ -256,18 +291,48 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   const int n_ktiles = (N + kBlockN - 1) / kBlockN;
   if (num_splits < 1 || num_splits > n_ktiles) return FA_ERR_INVALID_ARG;
-  if (num_splits > 1) {
-    const size_t need = fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits);
+  if (fp8 && d != 128) return FA_ERR_UNSUPPORTED;
+  // the FP8 preparation launches one CTA per (head, 128-key block)
+  if (fp8 && static_cast<long long>(B) * H * ((N + 127) / 128) > 0x7fffffffLL)
+    return FA_ERR_UNSUPPORTED;
+  if (num_splits > 1 || fp8) {
+    const size_t need = fp8 ? fa_fwd_fp8_workspace_bytes(B, H, N, d)
+                            : fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits);
     if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) != 0) return FA_ERR_WORKSPACE;
   }
 
   FwdParams p;
   const int BH = B * H;
-  if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
-      !encode_tile_map(&p.tm_v, v, N, BH, d))
-    return FA_ERR_CUDA;
   const long long rows = static_cast<long long>(BH) * N;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  p.fp8 = fp8;
+  p.q_descale = nullptr;
+  p.fp8_amax = nullptr;
+  if (fp8) {
+    Fp8Buffers fb;
+    char* w = static_cast<char*>(workspace);
+    fb.Np = (N + 15) / 16 * 16;
+    fb.q8 = reinterpret_cast<uint8_t*>(w);
+    w += round_up(static_cast<size_t>(rows) * 128);
+    fb.k8 = reinterpret_cast<uint8_t*>(w);
+    w += round_up(static_cast<size_t>(rows) * 128);
+    fb.v8t = reinterpret_cast<uint8_t*>(w);
+    w += round_up(static_cast<size_t>(BH) * 128 * fb.Np);
+    fb.q_descale = reinterpret_cast<float*>(w);
+    w += round_up(static_cast<size_t>(rows) * sizeof(float));
+    fb.amax = reinterpret_cast<unsigned int*>(w);
+    if (!encode_u8_map(&p.tm_q, fb.q8, 128, N, BH, 128) ||
+        !encode_u8_map(&p.tm_k, fb.k8, 128, N, BH, 128) ||
+        !encode_u8_map(&p.tm_v, fb.v8t, fb.Np, 128, BH, fb.Np))
+      return FA_ERR_CUDA;
+    if (launch_fp8_prepare(q, k, v, fb, BH, N, rotate, s) != cudaSuccess) return FA_ERR_CUDA;
+    p.q_descale = fb.q_descale;
+    p.fp8_amax = fb.amax;
+  } else if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
+             !encode_tile_map(&p.tm_v, v, N, BH, d)) {
+    return FA_ERR_CUDA;
+  }
   p.o = o;
   p.lse = lse;
   p.num_splits = num_splits;
@@ -288,7 +353,6 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.poly_per_octet = poly_per_octet();
   if (static_cast<long long>(p.n_qblk) * BH * num_splits > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   p.n_items = p.n_qblk * BH * num_splits;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (timing_record(0, true, s) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_fwd(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
   if (num_splits > 1 &&

@@ -47,9 +47,13 @@
 namespace fa {
 namespace {
 
-template <int D>
+// FP8: Q, K and V^T arrive as e4m3 (rotated and scaled beforehand) and
+// both products run as kind::f8f6f4 MMAs (K = 32 per MMA); d = 128 only, so
+// a row of a tile is exactly one 128-byte swizzle row.
+template <int D, bool FP8 = false>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!FP8 || D == 128, "FP8 forward: d = 128");
   static constexpr int kThreads = 384;
   static constexpr int kLaunchRegs = 168;   // what ptxas must allocate (checked at launch)
   static constexpr int kSoftmaxRegs = 208;  // 2 x 128 threads
@@ -58,9 +62,9 @@ struct FwdCfg {
                 "register split exceeds the launch allocation");
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;
-  static constexpr int kTileBytes = kBlockM * D * 2;  // one Q, K or V tile (bf16)
-  static constexpr int kHalfBytes = kBlockM * 64 * 2;  // one 64-column swizzle block
-  static constexpr int kSlots = (D == 128) ? 5 : 6;
+  static constexpr int kTileBytes = kBlockM * D * (FP8 ? 1 : 2);  // one Q, K or V tile
+  static constexpr int kHalfBytes = kBlockM * 64 * 2;  // one 64-column bf16 swizzle block
+  static constexpr int kSlots = FP8 ? 10 : ((D == 128) ? 5 : 6);
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
@@ -143,10 +147,10 @@ __device__ __forceinline__ int fwd_item_index(int r) {
 
 // POLY: of every 8 exponentials of the softmax, this many are evaluated by
 // exp2_poly on the FMA pipe, the rest by MUFU ex2.
-template <int D, int POLY>
-__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+template <int D, int POLY, bool FP8>
+__global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
@@ -204,10 +208,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         if (q_items > 0 && !(ok = mbar_wait(bar(C::kBarQEmpty), (q_items - 1) & 1, ctl, kSiteQEmpty)))
           break;
         mbar_arrive_expect_tx(bar(C::kBarQFull), 2 * C::kTileBytes);
-        for (int t = 0; t < 2; ++t)
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(q_smem + t * C::kTileBytes + h * C::kHalfBytes, &p.tm_q, bar(C::kBarQFull),
-                        h * 64, item.q0 + t * kBlockM, item.bh);
+        for (int t = 0; t < 2; ++t) {
+          if constexpr (FP8) {
+            tma_load_3d(q_smem + t * C::kTileBytes, &p.tm_q, bar(C::kBarQFull), 0,
+                        item.q0 + t * kBlockM, item.bh);
+          } else {
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d(q_smem + t * C::kTileBytes + h * C::kHalfBytes, &p.tm_q,
+                          bar(C::kBarQFull), h * 64, item.q0 + t * kBlockM, item.bh);
+          }
+        }
         items_loaded = ++q_items;
         for (int idx = 0; idx < 2 * item.nmax; ++idx, ++gidx) {
           const int slot = gidx % C::kSlots;
@@ -218,9 +228,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           const int j = idx >> 1;
           const uint32_t dst = sbase + C::kRingOff + slot * C::kTileBytes;
           mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(dst + h * C::kHalfBytes, map, bar(C::kBarFull + slot), h * 64,
-                        (item.kb + j) * kBlockN, item.bh);
+          if constexpr (FP8) {
+            // K: [key][d] rows; V^T: [d][key] rows (keys along x)
+            if (idx & 1)
+              tma_load_3d(dst, map, bar(C::kBarFull + slot), (item.kb + j) * kBlockN, 0, item.bh);
+            else
+              tma_load_3d(dst, map, bar(C::kBarFull + slot), 0, (item.kb + j) * kBlockN, item.bh);
+          } else {
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d(dst + h * C::kHalfBytes, map, bar(C::kBarFull + slot), h * 64,
+                          (item.kb + j) * kBlockN, item.bh);
+          }
           issued = gidx + 1;
         }
       }
@@ -233,8 +251,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------- MMA issue
     if (lane == 0) {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlockM, D, false, true);
+      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kBlockM, kBlockN, false, false)
+                                       : idesc_bf16_f32(kBlockM, kBlockN, false, false);
+      // FP8: V^T is K-major ([d][key]); bf16: V is MN-major ([key][d]).
+      constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3_f32(kBlockM, D, false, false)
+                                        : idesc_bf16_f32(kBlockM, D, false, true);
       const uint32_t q_smem = sbase + C::kQOff;
       const uint32_t ring = sbase + C::kRingOff;
       auto slot_of = [](int idx) { return idx % C::kSlots; };
@@ -246,11 +267,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const uint32_t a0 = q_smem + t * C::kTileBytes;
         const uint32_t b0 = ring + kslot * C::kTileBytes;
         const uint32_t dcol = tmem_base + C::kSCol0 + t * 128;
+        if constexpr (FP8) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          mma_ss(dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), kIdescS,
-                 kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 32; ++kk)  // 32 e4m3 = 32 bytes of the 128-byte row
+            mma_ss_f8(dcol, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024),
+                      kIdescS, kk > 0 ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+            mma_ss(dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), kIdescS,
+                   kk > 0 ? 1u : 0u);
+          }
         }
       };
       // O_t += P_t V : M = 128, N = d, K = 128 keys.  P_t (bf16, two per
@@ -261,10 +289,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const uint32_t b0 = ring + vslot * C::kTileBytes;
         const uint32_t acol = tmem_base + C::kSCol0 + t * 128;
         const uint32_t dcol = tmem_base + C::kOCol0 + t * D;
+        if constexpr (FP8) {
+          // P_t as e4m3, four per 32-bit column: 32 keys = 8 columns per MMA;
+          // V^T rows of 128 keys, 32 keys = 32 bytes per MMA.
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          mma_ts(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024), kIdescPV,
-                 (accumulate || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBlockN / 32; ++kk)
+            mma_ts_f8(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 32, 16, 1024), kIdescPV,
+                      (accumulate || kk > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            mma_ts(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024), kIdescPV,
+                   (accumulate || kk > 0) ? 1u : 0u);
+          }
         }
       };
 
@@ -342,8 +379,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t t_s = lane_base + C::kSCol0 + t * 128;
     const uint32_t t_o = lane_base + C::kOCol0 + t * D;
-    const float c = p.c;
-    const f32x2 c2 = f2_pack(c, c);
+    float c = p.c;  // FP8: times the row's Q and the head's K descale, per item
+    f32x2 c2 = f2_pack(c, c);
     const bool ragged = (p.N % kBlockN) != 0;
     // Barrier phases across items: bit 0 = s_full (flips per S tile),
     // bit 1 = o_full (flips per item).
@@ -372,6 +409,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           p.lse_part[prow] = -INFINITY;
         }
         continue;
+      }
+      if constexpr (FP8) {
+        const int qp = itm.q0 + t * kBlockM + row;
+        const float qd = qp < p.N ? p.q_descale[static_cast<size_t>(itm.bh) * p.N + qp] : 1.0f;
+        const float ka = __uint_as_float(p.fp8_amax[itm.bh]);
+        c = p.c * qd * (ka > 0.0f ? ka * (1.0f / 448.0f) : 1.0f);
+        c2 = f2_pack(c, c);
       }
       float m_used = -INFINITY;  // running row max in log2 units (scores * c)
       // row sum of exp2(x - m_used): four f32x2 accumulators (eight partial sums)
@@ -452,8 +496,31 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
         // P = exp2(x - m_used) -> bf16 into tensor memory over S.  Masked
         // entries are -inf and give exact zeros from MUFU; edge tiles use MUFU
-        // only.
-        const f32x2 negm2 = f2_pack(-m_used, -m_used);
+        // only.  FP8: P * 64 (exp2(x - m_used + 6), so the row sum carries
+        // the same factor) -> e4m3, four per column, over the first 32
+        // columns of S.
+        const f32x2 negm2 = FP8 ? f2_pack(6.0f - m_used, 6.0f - m_used) : f2_pack(-m_used, -m_used);
+        if constexpr (FP8) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t w[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 16; ++q4) {
+              const int ch = 2 * half + (q4 >> 3), e = (q4 & 7) * 4;
+              float x0, x1, x2, x3;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(r[ch][e]), __uint_as_float(r[ch][e + 1])), c2,
+                               negm2),
+                        x0, x1);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(r[ch][e + 2]), __uint_as_float(r[ch][e + 3])),
+                               c2, negm2),
+                        x2, x3);
+              const float p0 = ex2_mufu(x0), p1 = ex2_mufu(x1), p2 = ex2_mufu(x2), p3 = ex2_mufu(x3);
+              w[q4] = pack_e4m3x4(p0, p1, p2, p3);
+              l2[q4 & 3] = f2_add(l2[q4 & 3], f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
+            }
+            tmem_st16(t_s + half * 16, w);
+          }
+        } else {
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           uint32_t w[16];
@@ -472,6 +539,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             l2[(e >> 1) & 3] = f2_add(l2[(e >> 1) & 3], f2_pack(p0, p1));
           }
           tmem_st16(t_s + ch * 16, w);
+        }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -493,12 +561,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
           tc_fence_after();
-          const float inv_l = 1.0f / l;
           const FwdItem item = fwd_item(p, wi, n_ktiles);
           const int bh = item.bh;
           const int qpos = item.q0 + t * kBlockM + row;
           const bool in_range = qpos < p.N;
-          const float lse_row = m_used * p.ln2 + logf(l);
+          float inv_l = 1.0f / l;
+          float lse_row = m_used * p.ln2 + logf(l);
+          if constexpr (FP8) {  // P carried a factor 64, V the head's scale
+            const float va = __uint_as_float(p.fp8_amax[p.BH + bh]);
+            inv_l *= va > 0.0f ? va * (1.0f / 448.0f) : 1.0f;
+            lse_row -= 6.0f * p.ln2;
+          }
           if (p.o_part == nullptr) {
             __nv_bfloat16* orow =
                 static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
@@ -556,16 +629,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, int POLY>
+template <int D, int POLY, bool FP8 = false>
 cudaError_t launch_fwd_dp(const FwdParams& p, cudaStream_t stream) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, FP8>;
   // The setmaxnreg split assumes the launch allocation; refuse to run a build
   // whose register count differs (an over-committed split would never finish).
   cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, fa_fwd_kernel<D, POLY>);
+  cudaError_t err = cudaFuncGetAttributes(&attr, fa_fwd_kernel<D, POLY, FP8>);
   if (err != cudaSuccess) return err;
   if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(fa_fwd_kernel<D, POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  err = cudaFuncSetAttribute(fa_fwd_kernel<D, POLY, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
   if (err != cudaSuccess) return err;
   // Persistent CTAs: one per SM (the kernel holds all of tensor memory),
@@ -575,7 +648,7 @@ cudaError_t launch_fwd_dp(const FwdParams& p, cudaStream_t stream) {
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
   const int blocks = p.n_items < sms ? p.n_items : sms;
-  fa_fwd_kernel<D, POLY><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
+  fa_fwd_kernel<D, POLY, FP8><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -593,6 +666,7 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
+  if (p.fp8) return d == 128 ? launch_fwd_dp<128, 0, true>(p, stream) : cudaErrorInvalidValue;
   if (d == 128) return launch_fwd_d<128>(p, stream);
   if (d == 64) return launch_fwd_d<64>(p, stream);
   return cudaErrorInvalidValue;

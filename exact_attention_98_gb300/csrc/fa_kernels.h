@@ -44,6 +44,12 @@ struct FwdParams {
   int num_splits;
   float* o_part;
   float* lse_part;
+  // FP8 inputs (fp8 != 0): tm_q, tm_k, tm_v map the e4m3 Q, K and V^T of
+  // Fp8Buffers; scores carry the row's Q and the head's K descale, O the
+  // head's V descale.
+  int fp8;
+  const float* q_descale;       // [BH, N]
+  const unsigned int* fp8_amax;  // [2 * BH]: K then V amax per head (fp32 bits)
   int causal;
   float c;          // scale * log2(e): scores enter exp2 in these units
   float ln2;        // ln(2), to turn the log2-unit row max into LSE
@@ -82,6 +88,19 @@ struct BwdParams {
   float inv_scale;  // 1 / scale: -LSE / scale is the bias in raw score units
   float log2e;
 };
+
+// FP8 forward inputs (d = 128), in the caller's workspace.
+struct Fp8Buffers {
+  uint8_t* q8;          // e4m3 [BH, N, 128], Q rotated, one scale per row
+  float* q_descale;     // [BH, N]: amax / 448 of each rotated Q row
+  uint8_t* k8;          // e4m3 [BH, N, 128], K rotated, one scale per head
+  uint8_t* v8t;         // e4m3 [BH, 128, Np], V transposed, one scale per head
+  unsigned int* amax;   // [2 * BH]: fp32 bits of the K amax per head, then V
+  int Np;               // N rounded up to a multiple of 16 (V^T row pitch)
+};
+// Rotation (optional) and quantisation of Q, K, V into `b`.
+cudaError_t launch_fp8_prepare(const void* q, const void* k, const void* v, const Fp8Buffers& b,
+                               int BH, int N, int rotate, cudaStream_t stream);
 
 // Forward: one launch of the tcgen05 kernel for head dim d (64 or 128).
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);

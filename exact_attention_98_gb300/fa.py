@@ -50,6 +50,10 @@ def _load() -> ctypes.CDLL:
     lib.fa_fwd_splitkv_workspace_bytes.restype = sz
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
     lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_fwd_fp8_workspace_bytes.restype = sz
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
+    lib.fa_fwd_fp8.restype = i
     lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.fa_bwd_workspace_bytes.restype = sz
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
@@ -149,6 +153,35 @@ def fa_fwd_splitkv(q, k, v, o, lse, scale: float, causal: bool, num_splits: int,
     _check(lib.fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
                               float(scale), int(bool(causal)), int(num_splits), _ptr(workspace),
                               ws_bytes, _stream(stream)), "fa_fwd_splitkv")
+
+
+def fa_fwd_fp8_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib.fa_fwd_fp8_workspace_bytes(B, H, N, d))
+
+
+def fa_fwd_fp8(q, k, v, o, lse, scale: float, causal: bool, rotate: bool, workspace,
+               stream=None) -> None:
+    B, H, N, d = _shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
+        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
+    _check_tensor(lse, "lse", torch.float32, (B, H, N))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+                          int(bool(causal)), int(bool(rotate)), _ptr(workspace), ws_bytes,
+                          _stream(stream)), "fa_fwd_fp8")
+
+
+def forward_fp8(q, k, v, causal: bool = False, scale: float | None = None, rotate: bool = True,
+                stream=None):
+    """FP8 forward (fa_fwd_fp8); returns (o, lse) freshly allocated."""
+    B, H, N, d = _shape(q)
+    scale = default_scale(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    ws = torch.empty(max(fa_fwd_fp8_workspace_bytes(B, H, N, d), 1), dtype=torch.uint8,
+                     device=q.device)
+    fa_fwd_fp8(q, k, v, o, lse, scale, causal, rotate, ws, stream)
+    return o, lse
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

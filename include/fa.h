@@ -86,6 +86,29 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 forward with incoherent processing ("FlashAttention-3 и
+ * FlashAttention-4", section "Поддержка FP8 с контролем ошибок": a cheap
+ * transform spreads outliers over the coordinates before quantisation).
+ * Inputs and outputs as fa_fwd (bf16 Q, K, V; bf16 O; fp32 LSE), d = 128.
+ * The call first rotates Q and K along the head dimension with the
+ * orthogonal R = diag(sigma) H / sqrt(128) (H Sylvester-Hadamard, sigma a
+ * fixed +-1 pattern) when rotate = 1, which leaves Q K^T unchanged, and
+ * quantises to e4m3 in the workspace (Q one scale per row, K and V one per
+ * (batch, head); V stored transposed); both products then run as e4m3
+ * tensor-core MMAs with fp32 accumulation, P quantised to e4m3 as well.
+ * The result approximates fa_fwd's to FP8 precision (about 5% relative
+ * Frobenius error on O for N(0,1) inputs).
+ *   rotate    : 1 = rotate Q and K (incoherent processing), 0 = plain FP8
+ *   workspace : fa_fwd_fp8_workspace_bytes() bytes, 256-byte aligned
+ * Returns FA_ERR_UNSUPPORTED for d != 128, FA_ERR_WORKSPACE for a missing,
+ * short or misaligned workspace, FA_ERR_INVALID_ARG for rotate not 0 or 1.
+ */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int N, int d, float scale, int causal, int rotate, void* workspace,
+               size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: fp32 D = rowsum(dO * O) [B, H, N]
  * and the fp32 dQ accumulator [B, H, N, d], each 256-byte aligned.
  * Returns 0 for empty or unsupported shapes.

@@ -138,6 +138,27 @@ def test_splitkv_validation(lib):
     assert call(2, 0x10010, need) == lib.FA_ERR_WORKSPACE
 
 
+def test_fp8_workspace_bytes(lib):
+    ws = lib.fa_fwd_fp8_workspace_bytes
+    up = lambda x: (x + 255) // 256 * 256
+    B, H, N = 2, 3, 300
+    rows, bh, np_ = B * H * N, B * H, 304
+    assert ws(B, H, N, 128) == 2 * up(rows * 128) + up(bh * 128 * np_) + up(rows * 4) + up(2 * bh * 4)
+    assert ws(B, H, N, 64) == 0  # d = 128 only
+    assert ws(0, H, N, 128) == 0
+
+
+def test_fp8_validation(lib):
+    a = P(0x1000)
+    call = lambda d, ws, nbytes, rotate=1: lib.lib.fa_fwd_fp8(
+        a, a, a, a, a, 1, 1, 256, d, 0.125, 0, rotate, P(ws), nbytes, None)
+    need = lib.fa_fwd_fp8_workspace_bytes(1, 1, 256, 128)
+    assert call(64, 0x10000, need) == lib.FA_ERR_UNSUPPORTED
+    assert call(128, 0, need) == lib.FA_ERR_WORKSPACE
+    assert call(128, 0x10000, need - 1) == lib.FA_ERR_WORKSPACE
+    assert call(128, 0x10000, need, rotate=2) == lib.FA_ERR_INVALID_ARG
+
+
 def test_diagnostics_validation(lib):
     assert lib.lib.fa_exp2_poly_eval(P(0), P(0), -1, None) == lib.FA_ERR_INVALID_ARG
     assert lib.lib.fa_exp2_poly_eval(P(0), P(0), 0, None) == lib.FA_OK
