@@ -338,6 +338,30 @@ def native_arm(args):
     deterministic_extra = {"bwd_tflops": f_bwd / (det_ms_med * 1e-3) / 1e12, "bwd_ms": det_ms_med,
                            "note": "fa_bwd_deterministic, all kernels"}
 
+    # The FP8 forward (rotation + e4m3 preparation, then the kernel), same
+    # workload; the kernel alone from the library's events.
+    ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    o8, lse8 = torch.empty_like(qd), torch.empty_like(lse)
+    call_ms, kern_ms = [], []
+    fa.fa_timing_enable(True)
+    for i in range(3 + 5):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fa.fa_fwd_fp8(qd, kd, vd, o8, lse8, scale, False, True, ws8)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            call_ms.append(e0.elapsed_time(e1))
+            kern_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
+    fa.fa_timing_enable(False)
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after the FP8 forward")
+    del ws8, o8, lse8
+    fp8_extra = {"call_tflops": f_fwd / (statistics.median(call_ms) * 1e-3) / 1e12,
+                 "kernel_tflops": f_fwd / (statistics.median(kern_ms) * 1e-3) / 1e12,
+                 "note": "fa_fwd_fp8 (rotate=1, e4m3): call = preparation + kernel"}
+
     # End to end through the public calls: every step copies its own inputs
     # Q, K, V, dO from pinned host memory and its gradients dQ, dK, dV back.
     # Two forms are timed.  Serial: copies and kernels one after another on
@@ -468,6 +492,7 @@ def native_arm(args):
         "bwd_main_ms": bwd_med,
         "causal": causal_extra,
         "deterministic": deterministic_extra,
+        "fp8_forward": fp8_extra,
         "roofline": {
             "kernel": "fa_bwd_kernel<128>",
             "bound": "tensor",
