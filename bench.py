@@ -62,8 +62,8 @@ def parse():
 # soon as any of them changes.
 NCU_TRAFFIC = {
     "kernel": "fa_bwd_kernel<128>",
-    "bytes": 202690048 + 84474880,
-    "sources_sha256": "82b4a08c39cc744ab66415e56580fad64e9d28fdda7a1956cef12a33c1aa2e02",
+    "bytes": 202439680 + 84786176,
+    "sources_sha256": "aaf2486709660a53644aa575c52f8edbb1be6ea829db651227f3f2fa52aa9c11",
 }
 KERNEL_SOURCES = ("fa_bwd.cu", "fa_device.cuh", "fa_kernels.h", "exp2_poly_coeffs.h")
 
