@@ -164,6 +164,43 @@ int check_shape(int B, int H, int N, int d, float scale, bool* empty) {
   return FA_OK;
 }
 
+// Number of SMs of the current device (the persistent forward's grid).
+int sm_count() {
+  static std::mutex mu;
+  static int counts[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (counts[dev] == 0 &&
+      cudaDeviceGetAttribute(&counts[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    counts[dev] = 0;
+  return counts[dev];
+}
+
+// A private stream-ordered memory pool per device for the forward's split
+// scratch: it keeps what it has reserved (release threshold at the maximum),
+// so that after the first call an allocation costs no driver mapping, and it
+// leaves the process's default pool untouched.
+cudaMemPool_t scratch_pool() {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[dev] = pool;
+  }
+  return pools[dev];
+}
+
 constexpr size_t kWsAlign = 256;
 size_t round_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 
@@ -243,13 +280,19 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, 0, stream);
 }
 
+// Partial buffers of `slots` split items of 256 rows: O (fp32, d columns),
+// then LSE.
+size_t split_scratch_bytes(size_t slots, int d) {
+  return round_up(slots * 2 * kBlockM * d * sizeof(float)) +
+         round_up(slots * 2 * kBlockM * sizeof(float));
+}
+
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
   bool empty = false;
   if (check_shape(B, H, N, d, 1.0f, &empty) != FA_OK || empty) return 0;
-  if (num_splits < 1) return 0;
-  if (num_splits == 1) return 0;
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  return round_up(num_splits * rows * d * sizeof(float)) + round_up(num_splits * rows * sizeof(float));
+  if (num_splits < 2) return 0;
+  const size_t blocks = static_cast<size_t>(B) * H * ((N + 2 * kBlockM - 1) / (2 * kBlockM));
+  return split_scratch_bytes(blocks * num_splits, d);
 }
 
 size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
@@ -335,13 +378,6 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   }
   p.o = o;
   p.lse = lse;
-  p.num_splits = num_splits;
-  p.o_part = num_splits > 1 ? static_cast<float*>(workspace) : nullptr;
-  p.lse_part = num_splits > 1
-                   ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                              round_up(static_cast<size_t>(num_splits) * rows * d *
-                                                       sizeof(float)))
-                   : nullptr;
   p.status = status_ptr();
   if (!p.status) return FA_ERR_CUDA;
   p.N = N;
@@ -352,14 +388,53 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.ln2 = 0.6931471805599453f;
   p.poly_per_octet = poly_per_octet();
   if (static_cast<long long>(p.n_qblk) * BH * num_splits > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  p.n_items = p.n_qblk * BH * num_splits;
-  if (timing_record(0, true, s) != cudaSuccess) return FA_ERR_CUDA;
-  if (launch_fwd(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
-  if (num_splits > 1 &&
-      launch_fwd_merge(p.o_part, p.lse_part, o, lse, num_splits, rows, d, s) != cudaSuccess)
-    return FA_ERR_CUDA;
-  if (timing_record(0, false, s) != cudaSuccess) return FA_ERR_CUDA;
-  return FA_OK;
+  const int blocks = p.n_qblk * BH;
+  // Which blocks are split: all of them (num_splits > 1, the caller's
+  // workspace), else the last partial round of the persistent grid
+  // (non-causal: its blocks all cost the same), into as many key ranges as
+  // fill the round, with scratch from the stream-ordered allocator.
+  void* scratch = nullptr;
+  p.split_from = blocks;
+  p.num_splits = 1;
+  p.o_part = p.lse_part = nullptr;
+  if (num_splits > 1) {
+    p.split_from = 0;
+    p.num_splits = num_splits;
+    scratch = workspace;
+  } else if (!causal) {
+    const int sms = sm_count();
+    const int tail = sms > 0 ? blocks % sms : 0;
+    const int ns = tail > 0 ? sms / tail : 0;
+    if (blocks > sms && ns >= 2 && n_ktiles >= 8 * ns) {  // ranges of at least 8 key tiles
+      void* mem = nullptr;
+      cudaMemPool_t pool = scratch_pool();
+      if (pool != nullptr &&
+          cudaMallocFromPoolAsync(&mem, split_scratch_bytes(static_cast<size_t>(tail) * ns, d), pool,
+                                  s) == cudaSuccess) {
+        p.split_from = blocks - tail;
+        p.num_splits = ns;
+        scratch = mem;
+      } else {
+        (void)cudaGetLastError();  // run unsplit
+      }
+    }
+  }
+  if (p.split_from < blocks) {
+    const size_t slots = static_cast<size_t>(blocks - p.split_from) * p.num_splits;
+    p.o_part = static_cast<float*>(scratch);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(scratch) +
+                                          round_up(slots * 2 * kBlockM * d * sizeof(float)));
+  }
+  p.n_items = p.split_from + (blocks - p.split_from) * p.num_splits;
+  cudaError_t err = timing_record(0, true, s);
+  if (err == cudaSuccess) err = launch_fwd(p, d, s);
+  if (err == cudaSuccess && p.split_from < blocks) err = launch_fwd_merge(p, o, lse, d, s);
+  if (err == cudaSuccess) err = timing_record(0, false, s);
+  if (scratch != nullptr && scratch != workspace) {
+    const cudaError_t ferr = cudaFreeAsync(scratch, s);
+    if (err == cudaSuccess) err = ferr;
+  }
+  return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace

@@ -100,35 +100,50 @@ enum : unsigned int {
   kSiteQEmpty = 0x108,
 };
 
-// Work item w = two 128-row query tiles of one (batch, head) and one of the
-// num_splits contiguous key-tile ranges (w = block * num_splits + split).
-// Blocks: non-causal head-major, so that the query blocks of one head are
-// processed together and share its K and V in L2; causal, the heaviest
-// blocks (the last query blocks, which see the most keys) of every head
-// first.  With num_splits = 1 an item sees all keys its rows may attend to.
+// Blocks: two 128-row query tiles of one (batch, head).  Non-causal:
+// head-major, so that the query blocks of one head are processed together and
+// share its K and V in L2; causal, the heaviest blocks (the last query
+// blocks, which see the most keys) of every head first.
+__device__ __forceinline__ void fwd_block(int blk, int causal, int BH, int n_qblk, int& bh,
+                                          int& q0) {
+  bh = causal ? blk % BH : blk / n_qblk;
+  const int qblk = n_qblk - 1 - (causal ? blk / BH : blk % n_qblk);
+  q0 = qblk * 2 * kBlockM;
+}
+
+// Work item w: blocks before split_from are whole items (every key their rows
+// attend to); from split_from on each block is cut into num_splits
+// contiguous key-tile ranges, one item each, whose results go to the
+// partial buffers at slot `part` (see FwdParams).
 struct FwdItem {
   int bh;
   int q0;
   int kb;          // first key tile of the item's range
   int nkv0, nkv1;  // key tiles of the range seen by query tile 0 and 1 (0: none)
   int nmax;
+  int part;        // partial slot ((block - split_from) * num_splits + range), -1: none
   __device__ __forceinline__ int nkv(int t) const { return t ? nkv1 : nkv0; }
 };
 
 __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int w, int n_ktiles) {
   FwdItem it;
-  const int split = w % p.num_splits;
-  const int blk = w / p.num_splits;
-  it.bh = p.causal ? blk % p.BH : blk / p.n_qblk;
-  const int qblk = p.n_qblk - 1 - (p.causal ? blk / p.BH : blk % p.n_qblk);
-  it.q0 = qblk * 2 * kBlockM;
+  int blk = w, split = 0, ns = 1;
+  it.part = -1;
+  if (w >= p.split_from) {
+    const int u = w - p.split_from;
+    blk = p.split_from + u / p.num_splits;
+    split = u % p.num_splits;
+    ns = p.num_splits;
+    it.part = u;
+  }
+  fwd_block(blk, p.causal, p.BH, p.n_qblk, it.bh, it.q0);
   // key tiles [0, end) a query tile starting at qs attends to
   auto end_of = [&](int qs) {
     return qs >= p.N ? 0 : (p.causal ? min(n_ktiles, qs / kBlockN + 1) : n_ktiles);
   };
   const int end0 = end_of(it.q0);
   const int end1 = end_of(it.q0 + kBlockM);
-  const int per = (max(end0, end1) + p.num_splits - 1) / p.num_splits;
+  const int per = (max(end0, end1) + ns - 1) / ns;
   it.kb = split * per;
   it.nkv0 = max(0, min(end0 - it.kb, per));
   it.nkv1 = max(0, min(end1 - it.kb, per));
@@ -400,9 +415,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         // Split mode: an empty key range still leaves its partial result
         // for the merge (weight exp(-inf) = 0).
         const int qp = itm.q0 + t * kBlockM + row;
-        if (p.o_part != nullptr && qp < p.N) {
-          const size_t prow = static_cast<size_t>(wi % p.num_splits) * p.BH * p.N +
-                              static_cast<size_t>(itm.bh) * p.N + qp;
+        if (itm.part >= 0 && qp < p.N) {
+          const size_t prow = static_cast<size_t>(itm.part) * 2 * kBlockM + t * kBlockM + row;
           float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
 #pragma unroll 1
           for (int v4 = 0; v4 < D / 4; ++v4) dst[v4] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -572,7 +586,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
             inv_l *= va > 0.0f ? va * (1.0f / 448.0f) : 1.0f;
             lse_row -= 6.0f * p.ln2;
           }
-          if (p.o_part == nullptr) {
+          if (item.part < 0) {
             __nv_bfloat16* orow =
                 static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
 #pragma unroll 1
@@ -596,8 +610,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
           } else {
             // Split mode: this key range's O (normalised over the range) and
             // LSE in fp32, for the merge.
-            const size_t prow = static_cast<size_t>(wi % p.num_splits) * p.BH * p.N +
-                                static_cast<size_t>(bh) * p.N + qpos;
+            const size_t prow = static_cast<size_t>(item.part) * 2 * kBlockM + t * kBlockM + row;
             float* orow = p.o_part + prow * D;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
@@ -674,30 +687,41 @@ cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
 
 namespace {
 
-// Split-KV merge, one thread per 8 consecutive columns of one row: the
-// ranges' LSEs give the weights exp(LSE_s - max) (0 for an empty range),
-// their sum the row's LSE; O is the weighted mean of the ranges' O.
+// Split-KV merge, one thread per 8 consecutive columns of one row of the
+// split blocks (block split_from + t, row r of its 256): the ranges' LSEs give
+// the weights exp(LSE_s - max) (0 for an empty range), their sum the row's
+// LSE; O is the weighted mean of the ranges' O.
 __global__ void __launch_bounds__(256) fwd_merge_kernel(const float* __restrict__ o_part,
                                                         const float* __restrict__ lse_part,
                                                         __nv_bfloat16* __restrict__ o,
                                                         float* __restrict__ lse, int num_splits,
-                                                        long long rows, int d) {
+                                                        int n_blocks, int split_from, int causal,
+                                                        int BH, int n_qblk, int N, int d) {
   const int per_row = d / 8;
-  const long long n8 = rows * per_row;
+  const long long n8 = static_cast<long long>(n_blocks) * 2 * kBlockM * per_row;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = i / per_row;
+    const long long prow0 = i / per_row;  // row over the split blocks
+    const int t = static_cast<int>(prow0 / (2 * kBlockM));
+    const int r = static_cast<int>(prow0 % (2 * kBlockM));
     const int col = static_cast<int>(i % per_row) * 8;
+    int bh, q0;
+    fwd_block(split_from + t, causal, BH, n_qblk, bh, q0);
+    const int q = q0 + r;
+    if (q >= N) continue;
+    auto prow = [&](int s) {
+      return (static_cast<size_t>(t) * num_splits + s) * 2 * kBlockM + r;
+    };
     float m = -INFINITY;
-    for (int s = 0; s < num_splits; ++s) m = fmaxf(m, lse_part[s * rows + row]);
+    for (int s = 0; s < num_splits; ++s) m = fmaxf(m, lse_part[prow(s)]);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float wsum = 0.0f;
     for (int s = 0; s < num_splits; ++s) {
-      const float ls = lse_part[s * rows + row];
+      const float ls = lse_part[prow(s)];
       if (ls == -INFINITY) continue;
       const float w = expf(ls - m);
       wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(o_part + (s * rows + row) * d + col);
+      const float4* src = reinterpret_cast<const float4*>(o_part + prow(s) * d + col);
       const float4 x = src[0], y = src[1];
       acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
       acc[4] += w * y.x; acc[5] += w * y.y; acc[6] += w * y.z; acc[7] += w * y.w;
@@ -708,21 +732,24 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const float* __restrict_
     out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
     out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
     out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(o + row * d + col) = out;
-    if (col == 0) lse[row] = m + logf(wsum);
+    const size_t orow = static_cast<size_t>(bh) * N + q;
+    *reinterpret_cast<uint4*>(o + orow * d + col) = out;
+    if (col == 0) lse[orow] = m + logf(wsum);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_merge(const float* o_part, const float* lse_part, void* o, float* lse,
-                             int num_splits, long long rows, int d, cudaStream_t stream) {
-  const long long n8 = rows * (d / 8);
+cudaError_t launch_fwd_merge(const FwdParams& p, void* o, float* lse, int d,
+                             cudaStream_t stream) {
+  const int n_blocks = (p.n_items - p.split_from) / p.num_splits;
+  const long long n8 = static_cast<long long>(n_blocks) * 2 * kBlockM * (d / 8);
   long long blocks = (n8 + 255) / 256;
   const long long cap = 152LL * 8;
   if (blocks > cap) blocks = cap;
   fwd_merge_kernel<<<static_cast<unsigned int>(blocks < 1 ? 1 : blocks), 256, 0, stream>>>(
-      o_part, lse_part, static_cast<__nv_bfloat16*>(o), lse, num_splits, rows, d);
+      p.o_part, p.lse_part, static_cast<__nv_bfloat16*>(o), lse, p.num_splits, n_blocks,
+      p.split_from, p.causal, p.BH, p.n_qblk, p.N, d);
   return cudaGetLastError();
 }
 

@@ -35,12 +35,13 @@ struct FwdParams {
   int BH;
   int n_qblk;   // ceil(N / 256): a work item is two 128-row query tiles
   int n_items;  // n_qblk * BH * num_splits
-  // Split-KV: each query tile's key tiles are cut into num_splits contiguous
-  // ranges, one work item each.  With num_splits > 1 the kernel writes, per
-  // range, O normalised over the range and its LSE in fp32 to o_part
-  // [num_splits, BH, N, d] and lse_part [num_splits, BH, N]; a merge kernel
-  // combines them.  num_splits = 1: o_part = lse_part = nullptr, results go
-  // straight to o and lse.
+  // Split-KV: work items from block split_from on cut their key tiles into
+  // num_splits contiguous ranges, one item each; such an item writes O
+  // normalised over its range and its LSE (fp32) to the partial buffers, slot
+  // part = (block - split_from) * num_splits + range, 256 rows per slot:
+  // o_part [slots, 256, d], lse_part [slots, 256].  A merge kernel combines
+  // the ranges.  split_from = number of blocks: no split, o_part unused.
+  int split_from;
   int num_splits;
   float* o_part;
   float* lse_part;
@@ -104,10 +105,9 @@ cudaError_t launch_fp8_prepare(const void* q, const void* k, const void* v, cons
 
 // Forward: one launch of the tcgen05 kernel for head dim d (64 or 128).
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
-// Split-KV merge: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s
-// -> bf16 O and fp32 LSE.
-cudaError_t launch_fwd_merge(const float* o_part, const float* lse_part, void* o, float* lse,
-                             int num_splits, long long rows, int d, cudaStream_t stream);
+// Split-KV merge of the split blocks of `p`: LSE = ln sum_s exp(LSE_s),
+// O = sum_s exp(LSE_s - LSE) O_s -> bf16 O and fp32 LSE.
+cudaError_t launch_fwd_merge(const FwdParams& p, void* o, float* lse, int d, cudaStream_t stream);
 
 // Backward: D = rowsum(dO * O) and dQ accumulator zeroing.
 cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* dq_acc,

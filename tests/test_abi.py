@@ -118,9 +118,9 @@ def test_bwd_deterministic_validation(lib):
 def test_splitkv_workspace_bytes(lib):
     ws = lib.fa_fwd_splitkv_workspace_bytes
     up = lambda x: (x + 255) // 256 * 256
-    B, H, N, d = 1, 4, 16384, 128
-    rows = B * H * N
-    assert ws(B, H, N, d, 8) == up(8 * rows * d * 4) + up(8 * rows * 4)
+    B, H, N, d = 1, 4, 16300, 128
+    slots = B * H * ((N + 255) // 256) * 8  # 256-row blocks x ranges
+    assert ws(B, H, N, d, 8) == up(slots * 256 * d * 4) + up(slots * 256 * 4)
     assert ws(B, H, N, d, 1) == 0  # one range: fa_fwd, no workspace
     assert ws(B, H, N, d, 0) == 0
     assert ws(B, H, N, 96, 2) == 0
