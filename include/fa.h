@@ -58,7 +58,14 @@ typedef enum {
  * Kernels: TMA-staged Q/K/V tiles, tcgen05 MMAs accumulating S and O in
  * tensor memory, warp-specialised load / MMA / softmax roles, polynomial exp2
  * mixed with the MUFU unit, O rescaled only when a row max grows past a
- * threshold (FlashAttention-4 abstract, items 1-3).
+ * threshold (FlashAttention-4 abstract, items 1-3).  One persistent CTA per
+ * SM walks the (batch, head, 256-query block) work items.  Non-causal, when
+ * the last round of items would leave SMs idle, those items are cut into key
+ * ranges merged by log-sum-exp (see fa_fwd_splitkv); their fp32 partials
+ * come from a library-private stream-ordered memory pool on `stream`
+ * (created on the device's first such call, kept for the process), so the
+ * call stays asynchronous and may be captured in a CUDA graph once that
+ * pool exists.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
            int N, int d, float scale, int causal, void* stream);

@@ -7,6 +7,8 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``attn_f64.c`` holds the plain definition (see its header for the formulas and
 the passages they follow); this module only marshals numpy arrays into it.
 ``attn_np.py`` is a NumPy restatement of the same definition for tiny inputs.
+``fp8.py`` restates the FP8 forward's recipe (rotation, e4m3 quantisation,
+attention on the quantised operands) step by step, for the FP8 tests.
 
 Arrays are float64, row-major.  Tensors of shape [B, H, N, d] are processed one
 (batch, head) slice at a time.
