@@ -134,7 +134,8 @@ struct BwdCfg {
   static constexpr uint32_t kColDP = 128;  // dP^T, dS^T, then dQ
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
-  [[maybe_unused]] static constexpr int kDrainBarrier = 1;  // named barrier of the d = 64 drain
+  static constexpr int kDrainBarrier = 1;  // named barrier of the d = 64 drain (0 is __syncthreads)
+  static_assert(kDrainBarrier > 0, "named barrier 0 is the CTA barrier");
   // Shared-memory offset of stage s's dS tile.
   static __device__ __forceinline__ int ds_off(int s) {
     return (D == 128) ? kDOOff + s * kTileBytes : kDsOff + s * kDsTileBytes;

@@ -63,7 +63,8 @@ struct FwdCfg {
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;
   static constexpr int kTileBytes = kBlockM * D * (FP8 ? 1 : 2);  // one Q, K or V tile
-  [[maybe_unused]] static constexpr int kHalfBytes = kBlockM * 64 * 2;  // one 64-column bf16 swizzle block
+  static constexpr int kHalfBytes = kBlockM * 64 * 2;  // one 64-column bf16 swizzle block
+  static_assert(FP8 || kTileBytes == (D / 64) * kHalfBytes, "bf16 tile = its swizzle blocks");
   static constexpr int kSlots = FP8 ? 10 : ((D == 128) ? 5 : 6);
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
