@@ -1,0 +1,79 @@
+"""Robustness of the public calls: CUDA-graph capture and replay of a
+training step, and edge shapes of the split and FP8 paths."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from parity import compare_fwd, run_fwd
+
+pytestmark = pytest.mark.gpu
+
+
+def test_cuda_graph_capture_of_a_step():
+    """fwd + bwd captured once and replayed: the replay equals an eager step
+    (O, LSE, dK, dV bit for bit; dQ up to the order of its fp32 additions).
+    B2 H16 N4096 non-causal also takes the forward's tail split, whose
+    scratch comes from a stream-ordered pool, inside the graph."""
+    from exact_attention_98_gb300 import fa
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    B, H, N, d = 2, 16, 4096, 128
+    q, k, v, do = (t.cuda() for t in attention_inputs(B, H, N, d, seed=21))
+    scale = 1 / math.sqrt(d)
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = fa.workspace_for(q)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # eager reference (also creates the library's pool)
+        fa.fa_fwd(q, k, v, o, lse, scale, False)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, False, ws)
+    s.synchronize()
+    ref = [t.clone() for t in (o, lse, dq, dk, dv)]
+    for t in (o, lse, dq, dk, dv):
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fa.fa_fwd(q, k, v, o, lse, scale, False)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, False, ws)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for got, want, name in zip((o, lse, dk, dv), (ref[0], ref[1], ref[3], ref[4]), ("o", "lse", "dk", "dv")):
+        assert torch.equal(got, want), name
+    rel = (dq.float() - ref[2].float()).norm() / ref[2].float().norm()
+    assert rel < 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tail_split_with_ragged_keys(causal):
+    """B2 H16 N4000: 512 work items, the last round's split in two key
+    ranges, the last key tile ragged; head 1 full, sampled rows elsewhere."""
+    compare_fwd(2, 16, 4000, 128, causal, full_heads=1, rows_per_head=128)
+
+
+@pytest.mark.parametrize("N", [1, 5, 129])
+def test_fp8_degenerate_lengths(N):
+    """FP8 forward on one key, a few keys and one key past a tile: V^T's
+    padded pitch and zero keys, within the FP8 bounds of the exact oracle."""
+    import oracle
+    from exact_attention_98_gb300 import fa
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    B, H, d = 1, 2, 128
+    q, k, v, _ = attention_inputs(B, H, N, d, seed=N, with_dout=False)
+    o, lse = fa.forward_fp8(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o, lse = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    for h in range(H):
+        q64, k64, v64 = (t[0, h].double().numpy() for t in (q, k, v))
+        o_ref, l_ref = oracle.fwd_head(q64, k64, v64, 1 / math.sqrt(d), True)
+        assert np.linalg.norm(o[0, h] - o_ref) / np.linalg.norm(o_ref) <= 0.08
+        assert np.abs(lse[0, h] - l_ref).max() <= 0.25
+
+
+def test_splitkv_single_key_tile():
+    """num_splits = 1 on a one-tile problem runs the plain forward."""
+    compare_fwd(1, 2, 100, 64, False, num_splits=1)
