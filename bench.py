@@ -111,10 +111,11 @@ def dist_env():
 # --------------------------------------------------------------------------- CPU oracle
 
 
-def oracle_sample(seconds_target: float, steps: int = 1):
+def oracle_sample(seconds_target: float, steps: int = 1, warmup: int = 0):
     """Times the fp64 oracle on a bounded sample of the workload: forward and
-    dQ/dK/dV-backward of R query rows of head 0 (R sized so one sample takes
-    about `seconds_target`).  Returns (TFLOP/s, threads, description)."""
+    dQ-rows backward of R query rows of head 0 (R sized so one sample takes
+    about `seconds_target`), `warmup` untimed samples then `steps` timed ones.
+    Returns (TFLOP/s, threads, description, per-step seconds, FLOPs per step)."""
     import numpy as np
 
     import oracle
@@ -137,6 +138,8 @@ def oracle_sample(seconds_target: float, steps: int = 1):
     per_row = (time.perf_counter() - t0) / 32
     R = int(max(16, min(N, seconds_target / max(per_row, 1e-9))))
     rows = list(range(R))
+    for _ in range(warmup):
+        run(rows)
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
@@ -156,10 +159,10 @@ def reference_arm(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    per_step = 4.0  # seconds of oracle work per step
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state; calibration runs inside oracle_sample
-    tf, threads, desc, times, f = oracle_sample(per_step, steps=args.steps)
+    # seconds of oracle work per step: the whole warm-up + timed run stays
+    # within about two and a half minutes
+    per_step = min(4.0, max(0.25, 150.0 / max(1, args.steps + args.warmup)))
+    tf, threads, desc, times, f = oracle_sample(per_step, steps=args.steps, warmup=args.warmup)
     ms = statistics.median(times) * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": args.gpus,
@@ -185,21 +188,36 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+        import torch
+
+        # nvidia-smi numbers GPUs without regard to CUDA_VISIBLE_DEVICES, so the
+        # sampled GPU is named by its UUID where torch reports one
+        uuid = getattr(torch.cuda.get_device_properties(gpu_index), "uuid", None)
+        uuid = None if uuid is None else str(uuid)
+        self.ids = [str(gpu_index)]
+        if uuid:
+            self.ids.insert(0, uuid if uuid.startswith("GPU-") else f"GPU-{uuid}")
+        self.gpu = None
         self.proc = None
         self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
 
     def __enter__(self):
-        try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
-        except Exception:
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        for gpu in self.ids:  # the UUID first; the index if nvidia-smi refuses it
+            try:
+                self.fh = open(self.path, "w")
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={gpu}", f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=self.fh, stderr=subprocess.DEVNULL)
+                time.sleep(0.3)
+            except Exception:
+                self.proc = None
+            if self.proc is not None and self.proc.poll() is None:
+                self.gpu = gpu
+                return self
             self.proc = None
+            self.fh.close()
         return self
 
     def __exit__(self, *exc):
@@ -230,7 +248,7 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "gpu": self.gpu}
 
 
 def native_arm(args):

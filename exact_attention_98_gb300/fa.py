@@ -116,9 +116,11 @@ def _shape(q):
     return tuple(int(x) for x in q.shape)
 
 
-def _check_tensor(t, name, dtype, shape):
+def _check_tensor(t, name, dtype, shape, device=None):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
@@ -127,14 +129,36 @@ def _check_tensor(t, name, dtype, shape):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_attention(q, names_and_tensors, lse):
+    """Shape, dtype, device and layout checks shared by the forward and
+    backward calls; every operand lives on q's device."""
+    B, H, N, d = _shape(q)
+    if q.is_cuda and q.device.index != torch.cuda.current_device():
+        raise ValueError(f"q is on {q.device}; the library launches on the current device "
+                         f"cuda:{torch.cuda.current_device()}")
+    for name, t in names_and_tensors:
+        _check_tensor(t, name, torch.bfloat16, (B, H, N, d), q.device)
+    _check_tensor(lse, "lse", torch.float32, (B, H, N), q.device)
+    return B, H, N, d
+
+
+def _workspace(ws, device):
+    """(pointer, bytes) of a caller workspace: None, or a contiguous CUDA
+    tensor on the operands' device (the library checks size and alignment)."""
+    if ws is None:
+        return None, 0
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or ws.device != device:
+        raise ValueError(f"workspace must be a CUDA tensor on {device}")
+    if not ws.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
 # --- the C entry points --------------------------------------------------------
 
 
 def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
-    B, H, N, d = _shape(q)
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
-        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
-    _check_tensor(lse, "lse", torch.float32, (B, H, N))
+    B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o)), lse)
     _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
                       int(bool(causal)), _stream(stream)), "fa_fwd")
 
@@ -145,13 +169,10 @@ def fa_fwd_splitkv_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: i
 
 def fa_fwd_splitkv(q, k, v, o, lse, scale: float, causal: bool, num_splits: int, workspace,
                    stream=None) -> None:
-    B, H, N, d = _shape(q)
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
-        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
-    _check_tensor(lse, "lse", torch.float32, (B, H, N))
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o)), lse)
+    ws_ptr, ws_bytes = _workspace(workspace, q.device)
     _check(lib.fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                              float(scale), int(bool(causal)), int(num_splits), _ptr(workspace),
+                              float(scale), int(bool(causal)), int(num_splits), ws_ptr,
                               ws_bytes, _stream(stream)), "fa_fwd_splitkv")
 
 
@@ -161,13 +182,10 @@ def fa_fwd_fp8_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def fa_fwd_fp8(q, k, v, o, lse, scale: float, causal: bool, rotate: bool, workspace,
                stream=None) -> None:
-    B, H, N, d = _shape(q)
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o)):
-        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
-    _check_tensor(lse, "lse", torch.float32, (B, H, N))
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o)), lse)
+    ws_ptr, ws_bytes = _workspace(workspace, q.device)
     _check(lib.fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
-                          int(bool(causal)), int(bool(rotate)), _ptr(workspace), ws_bytes,
+                          int(bool(causal)), int(bool(rotate)), ws_ptr, ws_bytes,
                           _stream(stream)), "fa_fwd_fp8")
 
 
@@ -190,15 +208,12 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool, workspace,
            stream=None) -> None:
-    B, H, N, d = _shape(q)
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq),
-                    ("dk", dk), ("dv", dv)):
-        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
-    _check_tensor(lse, "lse", torch.float32, (B, H, N))
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout),
+                                      ("dq", dq), ("dk", dk), ("dv", dv)), lse)
+    ws_ptr, ws_bytes = _workspace(workspace, q.device)
     _check(lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                       _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
-                      _ptr(workspace), ws_bytes, _stream(stream)), "fa_bwd")
+                      ws_ptr, ws_bytes, _stream(stream)), "fa_bwd")
 
 
 def fa_bwd_deterministic_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
@@ -208,15 +223,12 @@ def fa_bwd_deterministic_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 def fa_bwd_deterministic(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool,
                          workspace, stream=None) -> None:
     """fa_bwd with run-to-run bit-identical results (no dQ atomics)."""
-    B, H, N, d = _shape(q)
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq),
-                    ("dk", dk), ("dv", dv)):
-        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
-    _check_tensor(lse, "lse", torch.float32, (B, H, N))
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout),
+                                      ("dq", dq), ("dk", dk), ("dv", dv)), lse)
+    ws_ptr, ws_bytes = _workspace(workspace, q.device)
     _check(lib.fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
                                     _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
-                                    int(bool(causal)), _ptr(workspace), ws_bytes,
+                                    int(bool(causal)), ws_ptr, ws_bytes,
                                     _stream(stream)), "fa_bwd_deterministic")
 
 
@@ -224,11 +236,8 @@ def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool
                    stream=None) -> None:
     """fa_bwd with the library's fixed scratch array instead of a caller
     workspace: for callers that cannot allocate device memory."""
-    B, H, N, d = _shape(q)
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq),
-                    ("dk", dk), ("dv", dv)):
-        _check_tensor(t, name, torch.bfloat16, (B, H, N, d))
-    _check_tensor(lse, "lse", torch.float32, (B, H, N))
+    B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout),
+                                      ("dq", dq), ("dk", dk), ("dv", dv)), lse)
     _check(lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                               _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                               _stream(stream)), "fa_bwd_noalloc")

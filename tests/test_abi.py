@@ -168,3 +168,17 @@ def test_diagnostics_validation(lib):
 def test_binding_exposes_c_names(lib):
     for name in declared():
         assert hasattr(lib, name), name
+
+
+def test_binding_rejects_host_operands(lib):
+    """The binding refuses host tensors (operands or workspace) before any C
+    call: the library takes device pointers only."""
+    import torch
+
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 1, 8, dtype=torch.float32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lib.fa_fwd(q, q, q, q, lse, 0.125, False)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lib._workspace(torch.zeros(16, dtype=torch.uint8), torch.device("cuda", 0))
+    assert lib._workspace(None, torch.device("cuda", 0)) == (None, 0)
