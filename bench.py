@@ -298,6 +298,7 @@ def native_arm(args):
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         fwd_ms, bwd_ms = [], []
         barrier()
+        launches0 = fa.fa_launch_count()
         wall0 = time.perf_counter()
         for i in range(steps):
             flush.zero_()  # L2 flush between steps, outside the step's events
@@ -309,16 +310,18 @@ def native_arm(args):
                 bwd_ms.append(fa.fa_timing_last_ms(fa.KERNEL_BWD_MAIN))
         barrier()
         wall = time.perf_counter() - wall0
+        launches = fa.fa_launch_count() - launches0
         fa.fa_timing_enable(False)
         status = fa.fa_last_device_status()
         if status != fa.FA_OK:
             raise RuntimeError(f"device status {fa.status_string(status)}")
         step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-        return step_ms, fwd_ms, bwd_ms, wall
+        return step_ms, fwd_ms, bwd_ms, wall, launches
 
     # headline: non-causal, with per-kernel events and clocks sampled meanwhile
     with ClockSampler(local) as clocks:
-        step_ms, fwd_ms, bwd_ms, wall = timed(False, args.steps, args.warmup, kernel_times=True)
+        step_ms, fwd_ms, bwd_ms, wall, launches = timed(False, args.steps, args.warmup,
+                                                         kernel_times=True)
     clk = clocks.summary()
     mean_ms = max_over_ranks(statistics.mean(step_ms), dev)
     f_fwd, f_bwd = flops(B, H, N, d, False)
@@ -328,7 +331,7 @@ def native_arm(args):
     bwd_main_tf = f_bwd / (bwd_med * 1e-3) / 1e12
 
     # causal variant (extra)
-    c_ms, c_fwd, c_bwd, _ = timed(True, max(3, args.steps // 2), 2, kernel_times=True)
+    c_ms, c_fwd, c_bwd, _, _ = timed(True, max(3, args.steps // 2), 2, kernel_times=True)
     cf_fwd, cf_bwd = flops(B, H, N, d, True)
     causal_extra = {
         "step_tflops": (cf_fwd + cf_bwd) / (statistics.mean(c_ms) * 1e-3) / 1e12,
@@ -531,7 +534,9 @@ def native_arm(args):
                 "copies": "one stream per direction, overlapped with the kernels (double buffered)",
                 "steps": e2e_steps,
                 "serial": {"value": e2e_serial_value, "ms_per_step": e2e_serial_ms}},
-        "gpu_launches": 4 * args.steps,
+        # the library's own launch counter across the timed steps: fa_fwd
+        # (1, or 2 when it splits its last partial round) + fa_bwd (3)
+        "gpu_launches": launches,
         "wall_s_timed_region": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:

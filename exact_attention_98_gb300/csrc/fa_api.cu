@@ -3,6 +3,7 @@
 // and their argument conventions are documented in include/fa.h.
 #include <math.h>
 #include <stdlib.h>
+#include <atomic>
 #include <mutex>
 #include <stdint.h>
 
@@ -14,6 +15,15 @@ namespace fa {
 
 // The status word every kernel writes through a pointer (see fa_device.cuh).
 __device__ unsigned int g_status_word;
+
+// Kernels launched by this library since it was loaded (fa_launch_count).
+std::atomic<unsigned long long> g_launches{0};
+
+cudaError_t launched(unsigned int n) {
+  const cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess) g_launches.fetch_add(n, std::memory_order_relaxed);
+  return err;
+}
 
 namespace {
 
@@ -585,6 +595,8 @@ int fa_timing_last_ms(int kernel, float* ms) {
   return cudaEventElapsedTime(ms, start, stop) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+unsigned long long fa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
 int fa_exp2_poly_eval(const float* x, float* y, long long n, void* stream) {
   if (n < 0) return FA_ERR_INVALID_ARG;
   if (n == 0) return FA_OK;
@@ -592,7 +604,7 @@ int fa_exp2_poly_eval(const float* x, float* y, long long n, void* stream) {
   const long long blocks = (n + 255) / 256;
   exp2_poly_eval_kernel<<<static_cast<unsigned int>(blocks < 4096 ? blocks : 4096), 256, 0,
                           static_cast<cudaStream_t>(stream)>>>(x, y, n);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launched(1) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_debug_bounded_wait(unsigned long long limit_ns, void* stream) {
@@ -600,7 +612,7 @@ int fa_debug_bounded_wait(unsigned long long limit_ns, void* stream) {
   unsigned int* status = status_ptr();
   if (!status) return FA_ERR_CUDA;
   bounded_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return launched(1) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -646,7 +646,7 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(p.n_kblk) * p.BH;
   fa_bwd_kernel<D><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 }  // namespace

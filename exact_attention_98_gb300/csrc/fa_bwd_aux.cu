@@ -142,14 +142,14 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* 
                                                                               dq_acc, rows);
   else
     return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  return launched(1);
 }
 
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, cudaStream_t stream) {
   const long long n8 = elems / 8;  // d is a multiple of 8, so elems is too
   bwd_post_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
                                                          n8);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 cudaError_t launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, int n_kblk,
@@ -157,7 +157,7 @@ cudaError_t launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, 
   const long long n8 = static_cast<long long>(BH) * N * d / 8;
   bwd_dq_reduce_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(
       dq_part, static_cast<__nv_bfloat16*>(dq), BH, N, d, n_kblk, causal, n8);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 }  // namespace fa

@@ -253,7 +253,7 @@ cudaError_t launch_fp8_prepare(const void* q, const void* k, const void* v, cons
   const dim3 grid(static_cast<unsigned int>(BH) * ((b.Np + 127) / 128));
   fp8_v_transpose_kernel<<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(v), b.v8t,
                                                    b.amax + BH, N, b.Np);
-  return cudaGetLastError();
+  return launched(4);
 }
 
 }  // namespace fa

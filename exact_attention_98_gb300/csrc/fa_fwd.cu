@@ -663,7 +663,7 @@ cudaError_t launch_fwd_dp(const FwdParams& p, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const int blocks = p.n_items < sms ? p.n_items : sms;
   fa_fwd_kernel<D, POLY, FP8><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 template <int D>
@@ -751,7 +751,7 @@ cudaError_t launch_fwd_merge(const FwdParams& p, void* o, float* lse, int d,
   fwd_merge_kernel<<<static_cast<unsigned int>(blocks < 1 ? 1 : blocks), 256, 0, stream>>>(
       p.o_part, p.lse_part, static_cast<__nv_bfloat16*>(o), lse, p.num_splits, n_blocks,
       p.split_from, p.causal, p.BH, p.n_qblk, p.N, d);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 }  // namespace fa

@@ -103,6 +103,11 @@ struct Fp8Buffers {
 cudaError_t launch_fp8_prepare(const void* q, const void* k, const void* v, const Fp8Buffers& b,
                                int BH, int N, int rotate, cudaStream_t stream);
 
+// The launch wrappers end with `return launched(n)`: the launch error of the
+// n kernels just launched, which are added to the library's launch count
+// (fa_launch_count) when there is none.
+cudaError_t launched(unsigned int n);
+
 // Forward: one launch of the tcgen05 kernel for head dim d (64 or 128).
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream);
 // Split-KV merge of the split blocks of `p`: LSE = ln sum_s exp(LSE_s),

@@ -79,6 +79,8 @@ def _load() -> ctypes.CDLL:
     lib.fa_timing_enable.restype = i
     lib.fa_timing_last_ms.argtypes = [i, ctypes.POINTER(ctypes.c_float)]
     lib.fa_timing_last_ms.restype = i
+    lib.fa_launch_count.argtypes = []
+    lib.fa_launch_count.restype = ctypes.c_ulonglong
     return lib
 
 
@@ -88,7 +90,8 @@ lib = _load()
 def declared_functions() -> list[str]:
     """Names of the functions include/fa.h declares."""
     text = open(HEADER_PATH).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(fa_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^[ \t]*(?:const[ \t]+)?(?:\w+[ \t]+)*\w+[ \t]*\*?[ \t]*(fa_\w+)\s*\(",
+                                 text, re.M)))
 
 
 def status_string(code: int) -> str:
@@ -278,6 +281,10 @@ def fa_timing_last_ms(kernel: int) -> float:
     ms = ctypes.c_float(0.0)
     _check(lib.fa_timing_last_ms(int(kernel), ctypes.byref(ms)), "fa_timing_last_ms")
     return float(ms.value)
+
+
+def fa_launch_count() -> int:
+    return int(lib.fa_launch_count())
 
 
 # --- conveniences ----------------------------------------------------------------

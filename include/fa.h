@@ -239,6 +239,17 @@ int fa_debug_bounded_wait(unsigned long long limit_ns, void* stream);
 int fa_timing_enable(int enable);
 int fa_timing_last_ms(int kernel, float* ms);
 
+/*
+ * Number of kernels the library has launched since it was loaded, over all
+ * entry points, streams and threads (launches that CUDA refused are not
+ * counted).  The difference of two readings counts the launches in between,
+ * e.g. in a timed region: fa_fwd launches one kernel, or two when it splits
+ * its last partial round of work (the forward, then the merge); fa_bwd three;
+ * fa_bwd_deterministic three; fa_fwd_fp8 five (four preparation kernels and
+ * the forward); fa_fwd_splitkv two.
+ */
+unsigned long long fa_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -182,3 +182,11 @@ def test_binding_rejects_host_operands(lib):
     with pytest.raises(ValueError, match="CUDA tensor"):
         lib._workspace(torch.zeros(16, dtype=torch.uint8), torch.device("cuda", 0))
     assert lib._workspace(None, torch.device("cuda", 0)) == (None, 0)
+
+
+def test_launch_counter_without_launches(lib):
+    """Host-rejected calls launch nothing, so the counter does not move."""
+    before = lib.fa_launch_count()
+    assert lib.lib.fa_exp2_poly_eval(P(0), P(0), -1, None) == lib.FA_ERR_INVALID_ARG
+    assert lib.lib.fa_debug_bounded_wait(10, None) == lib.FA_ERR_INVALID_ARG
+    assert lib.fa_launch_count() == before

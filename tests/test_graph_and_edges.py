@@ -77,3 +77,36 @@ def test_fp8_degenerate_lengths(N):
 def test_splitkv_single_key_tile():
     """num_splits = 1 on a one-tile problem runs the plain forward."""
     compare_fwd(1, 2, 100, 64, False, num_splits=1)
+
+
+def test_launch_counter_per_call():
+    """fa_launch_count advances by the number of kernels each call launches
+    (the figure the benchmark reports as its launch count)."""
+    from exact_attention_98_gb300 import fa
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    B, H, N, d = 1, 2, 384, 128
+    q, k, v, do = (t.cuda() for t in attention_inputs(B, H, N, d, seed=5))
+    scale = 1 / math.sqrt(d)
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+
+    def count(call):
+        before = fa.fa_launch_count()
+        call()
+        torch.cuda.synchronize()
+        return fa.fa_launch_count() - before
+
+    # 2 query blocks of 256 rows x 2 heads: fewer than the SMs, never split
+    assert count(lambda: fa.fa_fwd(q, k, v, o, lse, scale, False)) == 1
+    ws = fa.workspace_for(q)
+    assert count(lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, False, ws)) == 3
+    wsd = fa.workspace_for(q, deterministic=True)
+    assert count(lambda: fa.fa_bwd_deterministic(q, k, v, o, lse, do, dq, dk, dv, scale, False,
+                                                 wsd)) == 3
+    ws2 = torch.empty(fa.fa_fwd_splitkv_workspace_bytes(B, H, N, d, 2), dtype=torch.uint8,
+                      device="cuda")
+    assert count(lambda: fa.fa_fwd_splitkv(q, k, v, o, lse, scale, False, 2, ws2)) == 2
+    ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+    assert count(lambda: fa.fa_fwd_fp8(q, k, v, o, lse, scale, False, True, ws8)) == 5
+    assert fa.fa_last_device_status() == fa.FA_OK
