@@ -378,10 +378,25 @@ def native_arm(args):
     fa.fa_timing_enable(False)
     if fa.fa_last_device_status() != fa.FA_OK:
         raise RuntimeError("device status after the FP8 forward")
-    del ws8, o8, lse8
+    del ws8
     fp8_extra = {"call_tflops": f_fwd / (statistics.median(call_ms) * 1e-3) / 1e12,
                  "kernel_tflops": f_fwd / (statistics.median(kern_ms) * 1e-3) / 1e12,
                  "note": "fa_fwd_fp8 (rotate=1, e4m3): call = preparation + kernel"}
+
+    # The CTA-pair forward (fa_fwd_2cta), same workload, kernel events.
+    pair_ms = []
+    fa.fa_timing_enable(True)
+    for i in range(3 + 5):
+        flush.zero_()
+        fa.fa_fwd_2cta(qd, kd, vd, o8, lse8, scale, False)
+        if i >= 3:
+            pair_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
+    fa.fa_timing_enable(False)
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after the CTA-pair forward")
+    del o8, lse8
+    two_cta_extra = {"kernel_tflops": f_fwd / (statistics.median(pair_ms) * 1e-3) / 1e12,
+                     "note": "fa_fwd_2cta: CTA pairs sharing M = 256 products"}
 
     # End to end through the public calls: every step copies its own inputs
     # Q, K, V, dO from pinned host memory and its gradients dQ, dK, dV back.
@@ -514,6 +529,7 @@ def native_arm(args):
         "causal": causal_extra,
         "deterministic": deterministic_extra,
         "fp8_forward": fp8_extra,
+        "two_cta_forward": two_cta_extra,
         "roofline": {
             "kernel": "fa_bwd_kernel<128>",
             "bound": "tensor",

@@ -89,16 +89,17 @@ EncodeTiledFn encode_fn() {
 }
 
 // bf16 [BH, N, d] viewed as a 3-D tensor (d, N, BH); the box is 64 columns
-// (128 bytes, one 128B-swizzle row) x 128 rows x 1 head.  Rows past N read
-// as zeros.
-bool encode_tile_map(CUtensorMap* map, const void* base, int N, int BH, int d) {
+// (128 bytes, one 128B-swizzle row) x box_rows rows x 1 head.  Rows past N
+// read as zeros.
+bool encode_tile_map(CUtensorMap* map, const void* base, int N, int BH, int d,
+                     unsigned int box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, box_rows, 1};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -281,13 +282,18 @@ namespace {
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, float scale, int causal, int num_splits, void* workspace,
-             size_t workspace_bytes, void* stream, int fp8 = 0, int rotate = 0);
+             size_t workspace_bytes, void* stream, int fp8 = 0, int rotate = 0, int pair = 0);
 
 }  // namespace
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            int d, float scale, int causal, void* stream) {
   return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, 0, stream);
+}
+
+int fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int N, int d, float scale, int causal, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, 0, stream, 0, 0, 1);
 }
 
 // Partial buffers of `slots` split items of 256 rows: O (fp32, d columns),
@@ -334,7 +340,7 @@ namespace {
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, float scale, int causal, int num_splits, void* workspace,
-             size_t workspace_bytes, void* stream, int fp8, int rotate) {
+             size_t workspace_bytes, void* stream, int fp8, int rotate, int pair) {
   bool empty = false;
   int rc = check_shape(B, H, N, d, scale, &empty);
   if (rc != FA_OK || empty) return rc;
@@ -344,7 +350,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   const int n_ktiles = (N + kBlockN - 1) / kBlockN;
   if (num_splits < 1 || num_splits > n_ktiles) return FA_ERR_INVALID_ARG;
-  if (fp8 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((fp8 || pair) && d != 128) return FA_ERR_UNSUPPORTED;
   // the FP8 preparation launches one CTA per (head, 128-key block)
   if (fp8 && static_cast<long long>(B) * H * ((N + 127) / 128) > 0x7fffffffLL)
     return FA_ERR_UNSUPPORTED;
@@ -382,7 +388,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (launch_fp8_prepare(q, k, v, fb, BH, N, rotate, s) != cudaSuccess) return FA_ERR_CUDA;
     p.q_descale = fb.q_descale;
     p.fp8_amax = fb.amax;
-  } else if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
+  } else if (!encode_tile_map(&p.tm_q, q, N, BH, d) ||
+             !encode_tile_map(&p.tm_k, k, N, BH, d, pair ? 64 : 128) ||
              !encode_tile_map(&p.tm_v, v, N, BH, d)) {
     return FA_ERR_CUDA;
   }
@@ -392,7 +399,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (!p.status) return FA_ERR_CUDA;
   p.N = N;
   p.BH = BH;
-  p.n_qblk = (N + 2 * kBlockM - 1) / (2 * kBlockM);
+  p.pair = pair;
+  const int item_rows = (pair ? 4 : 2) * kBlockM;
+  p.n_qblk = (N + item_rows - 1) / item_rows;
   p.causal = causal;
   p.c = scale * 1.4426950408889634f;
   p.ln2 = 0.6931471805599453f;
@@ -411,7 +420,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.split_from = 0;
     p.num_splits = num_splits;
     scratch = workspace;
-  } else if (!causal) {
+  } else if (!causal && !pair) {
     const int sms = sm_count();
     const int tail = sms > 0 ? blocks % sms : 0;
     const int ns = tail > 0 ? sms / tail : 0;

@@ -50,10 +50,15 @@ namespace {
 // FP8: Q, K and V^T arrive as e4m3 (rotated and scaled beforehand) and
 // both products run as kind::f8f6f4 MMAs (K = 32 per MMA); d = 128 only, so
 // a row of a tile is exactly one 128-byte swizzle row.
-template <int D, bool FP8 = false>
+// PAIR: two CTAs (a cluster of two) share every product as one M = 256
+// tcgen05 MMA (cta_group::2): each CTA keeps its own two query tiles, S, P and
+// O, and loads half of every K tile (64 of its keys) and half of every V tile
+// (64 of its d columns); bf16, d = 128 only.
+template <int D, bool FP8 = false, bool PAIR = false>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(!FP8 || D == 128, "FP8 forward: d = 128");
+  static_assert(!PAIR || (D == 128 && !FP8), "pair forward: bf16, d = 128");
   static constexpr int kThreads = 384;
   static constexpr int kLaunchRegs = 168;   // what ptxas must allocate (checked at launch)
   static constexpr int kSoftmaxRegs = 208;  // 2 x 128 threads
@@ -65,10 +70,15 @@ struct FwdCfg {
   static constexpr int kTileBytes = kBlockM * D * (FP8 ? 1 : 2);  // one Q, K or V tile
   static constexpr int kHalfBytes = kBlockM * 64 * 2;  // one 64-column bf16 swizzle block
   static_assert(FP8 || kTileBytes == (D / 64) * kHalfBytes, "bf16 tile = its swizzle blocks");
-  static constexpr int kSlots = FP8 ? 10 : ((D == 128) ? 5 : 6);
+  // one ring slot: a K or V tile, or in pair mode this CTA's half of one
+  static constexpr int kSlotBytes = PAIR ? kTileBytes / 2 : kTileBytes;
+  static constexpr int kSlots = FP8 ? 10 : PAIR ? 9 : ((D == 128) ? 5 : 6);
+  // pair mode: a pad of one slot after the ring, so that no operand
+  // read that starts in the last slot can leave the allocation
+  static constexpr int kRingPad = PAIR ? kSlotBytes : 0;
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kSlots * kSlotBytes + kRingPad;
   // barriers: q_full, q_empty, full[kSlots], empty[kSlots], s_full[2],
   // p_full[2], o_full[2], mma_done
   static constexpr int kBarQFull = 0;
@@ -84,6 +94,7 @@ struct FwdCfg {
   static constexpr int kAbortOff = kTmemSlotOff + 4;
   static constexpr int kSmemUsed = kAbortOff + 4;
   static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol0 = 0;    // S_t / P_t at t * 128
   static constexpr uint32_t kOCol0 = 256;  // O_t at 256 + t * D
@@ -101,15 +112,16 @@ enum : unsigned int {
   kSiteQEmpty = 0x108,
 };
 
-// Blocks: two 128-row query tiles of one (batch, head).  Non-causal:
-// head-major, so that the query blocks of one head are processed together and
-// share its K and V in L2; causal, the heaviest blocks (the last query
-// blocks, which see the most keys) of every head first.
+// Blocks: two 128-row query tiles of one (batch, head) (four for a CTA
+// pair: rows = 512).  Non-causal: head-major, so that the query blocks of one
+// head are processed together and share its K and V in L2; causal, the
+// heaviest blocks (the last query blocks, which see the most keys) of every
+// head first.
 __device__ __forceinline__ void fwd_block(int blk, int causal, int BH, int n_qblk, int& bh,
-                                          int& q0) {
+                                          int& q0, int rows = 2 * kBlockM) {
   bh = causal ? blk % BH : blk / n_qblk;
   const int qblk = n_qblk - 1 - (causal ? blk / BH : blk % n_qblk);
-  q0 = qblk * 2 * kBlockM;
+  q0 = qblk * rows;
 }
 
 // Work item w: blocks before split_from are whole items (every key their rows
@@ -152,21 +164,42 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int w, int n_kti
   return it;
 }
 
-// The r-th item of this CTA: persistent CTAs walk the item list in rounds of
-// gridDim.x, alternating direction (0..G-1, then G-1..0), so that with the
-// heaviest items first every CTA gets a similar total.
+// Pair work item w: 512 query rows of one (batch, head), never split.  Pair
+// tile t is query tile 2t (rank 0's tile t) and 2t + 1 (rank 1's tile t), so
+// that the two halves of one M = 256 product are adjacent query tiles; both
+// CTAs walk the key tiles the later one needs (causal: one more than the
+// earlier, which masks it whole).
+__device__ __forceinline__ FwdItem pair_item(const FwdParams& p, int w, int n_ktiles) {
+  FwdItem it;
+  it.part = -1;
+  it.kb = 0;
+  fwd_block(w, p.causal, p.BH, p.n_qblk, it.bh, it.q0, 4 * kBlockM);
+  auto end_of = [&](int qs) {
+    return qs >= p.N ? 0 : (p.causal ? min(n_ktiles, qs / kBlockN + 1) : n_ktiles);
+  };
+  it.nkv0 = max(end_of(it.q0), end_of(it.q0 + kBlockM));
+  it.nkv1 = max(end_of(it.q0 + 2 * kBlockM), end_of(it.q0 + 3 * kBlockM));
+  it.nmax = max(it.nkv0, it.nkv1);
+  return it;
+}
+
+// The r-th item of this CTA (of this pair): persistent CTAs (pairs) walk the
+// item list in rounds of G = gridDim.x (pairs: gridDim.x / 2), alternating
+// direction (0..G-1, then G-1..0), so that with the heaviest items first
+// every CTA gets a similar total.
+template <bool PAIR = false>
 __device__ __forceinline__ int fwd_item_index(int r) {
-  const int G = static_cast<int>(gridDim.x);
-  const int c = static_cast<int>(blockIdx.x);
+  const int G = static_cast<int>(gridDim.x) / (PAIR ? 2 : 1);
+  const int c = static_cast<int>(blockIdx.x) / (PAIR ? 2 : 1);
   return r * G + ((r & 1) ? G - 1 - c : c);
 }
 
 // POLY: of every 8 exponentials of the softmax, this many are evaluated by
 // exp2_poly on the FMA pipe, the rest by MUFU ex2.
-template <int D, int POLY, bool FP8>
-__global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
+template <int D, int POLY, bool FP8, bool PAIR = false>
+__global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D, FP8>;
+  using C = FwdCfg<D, FP8, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
@@ -179,6 +212,12 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
   const int warp = warp_id();
   const int lane = lane_id();
   const int n_ktiles = (p.N + kBlockN - 1) / kBlockN;
+  // pair mode: this CTA's rank in the pair (0 issues the MMAs)
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
+  auto item_of = [&](int wi) {
+    if constexpr (PAIR) return pair_item(p, wi, n_ktiles);
+    else return fwd_item(p, wi, n_ktiles);
+  };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -190,15 +229,22 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kBarSFull + t), 1);
-      mbar_init(bar(C::kBarPFull + t), kBlockM);
+      // pair mode: one arrival per softmax warp of both CTAs (on rank 0's)
+      mbar_init(bar(C::kBarPFull + t), PAIR ? 8 : kBlockM);
       mbar_init(bar(C::kBarOFull + t), 1);
     }
     mbar_init(bar(C::kBarMmaDone), 1);
     fence_mbar_init();
   }
-  if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  if (warp == C::kMmaWarp) {
+    if constexpr (PAIR) tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    else tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  }
   tc_fence_before();
-  __syncthreads();
+  // pair mode: both CTAs' barriers are initialised before either CTA's
+  // copies, commits or arrivals reach them
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -209,7 +255,65 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     // Per item: Q_0, Q_1 into the Q buffer once the previous item's last
     // S product has read it, then K_j, V_j through the ring (one running
     // load index across items).
-    if (lane == 0) {
+    if (PAIR && lane == 0) {
+      // Pair mode: this CTA's Q tiles and its halves of K_j and V_j, each
+      // copy counted on rank 0's barrier, where rank 0 expects both CTAs'
+      // bytes; the empty barriers are this CTA's own (the MMA commits reach
+      // both CTAs).
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      const uint32_t q_smem = sbase + C::kQOff;
+      int gidx = 0, issued = 0, items_loaded = 0, q_items = 0;
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int wi = fwd_item_index<PAIR>(round);
+        if (wi >= p.n_items) break;
+        const FwdItem item = pair_item(p, wi, n_ktiles);
+        if (item.nmax == 0) continue;
+        if (q_items > 0 && !(ok = mbar_wait(bar(C::kBarQEmpty), (q_items - 1) & 1, ctl, kSiteQEmpty)))
+          break;
+        if (rank == 0) mbar_arrive_expect_tx(bar(C::kBarQFull), 4 * C::kTileBytes);
+        const uint32_t qbar = cluster_smem(bar(C::kBarQFull), 0);
+        for (int t = 0; t < 2; ++t)
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d_pair(q_smem + t * C::kTileBytes + h * C::kHalfBytes, &p.tm_q, qbar, h * 64,
+                             item.q0 + (2 * t + static_cast<int>(rank)) * kBlockM, item.bh);
+        items_loaded = ++q_items;
+        for (int idx = 0; idx < 2 * item.nmax; ++idx, ++gidx) {
+          const int slot = gidx % C::kSlots;
+          const int use = gidx / C::kSlots;
+          if (use > 0 && !(ok = mbar_wait(bar(C::kBarEmpty + slot), (use - 1) & 1, ctl, kSiteEmpty)))
+            break;
+          const int key0 = (item.kb + (idx >> 1)) * kBlockN;
+          const uint32_t dst = sbase + C::kRingOff + slot * C::kSlotBytes;
+          const uint32_t fbar = cluster_smem(bar(C::kBarFull + slot), 0);
+          if (rank == 0) mbar_arrive_expect_tx(bar(C::kBarFull + slot), 2 * C::kSlotBytes);
+          if (idx & 1) {
+            // V_j: all 128 keys, this CTA's 64 of the d columns
+            tma_load_3d_pair(dst, &p.tm_v, fbar, static_cast<int>(rank) * 64, key0, item.bh);
+          } else {
+            // K_j: this CTA's 64 keys, all d columns (two 64-column blocks)
+            for (int h = 0; h < D / 64; ++h)
+              tma_load_3d_pair(dst + h * (C::kSlotBytes / 2), &p.tm_k, fbar, h * 64,
+                               key0 + static_cast<int>(rank) * 64, item.bh);
+          }
+          issued = gidx + 1;
+        }
+      }
+      if (rank == 0) {
+        // Rank 0's barriers count both CTAs' copies: waiting on them lets
+        // every copy of the pair land (only waits on the give-up path).
+        if (items_loaded > 0) mbar_wait_drain(bar(C::kBarQFull), (items_loaded - 1) & 1);
+        for (int idx = max(0, issued - C::kSlots); idx < issued; ++idx)
+          mbar_wait_drain(bar(C::kBarFull + idx % C::kSlots), (idx / C::kSlots) & 1);
+      } else if (!ok) {
+        // Give-up path of rank 1, whose copies complete on rank 0's barriers:
+        // a bounded pause for the copies in flight to land.
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) __nanosleep(1000);
+      }
+    } else if (!PAIR && lane == 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
@@ -266,22 +370,30 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------- MMA issue
-    if (lane == 0) {
-      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kBlockM, kBlockN, false, false)
-                                       : idesc_bf16_f32(kBlockM, kBlockN, false, false);
+    if (lane == 0 && rank == 0) {
+      // pair mode: M = 256 (this CTA's 128 query rows, then the other's)
+      constexpr int kM = PAIR ? 2 * kBlockM : kBlockM;
+      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kM, kBlockN, false, false)
+                                       : idesc_bf16_f32(kM, kBlockN, false, false);
       // FP8: V^T is K-major ([d][key]); bf16: V is MN-major ([key][d]).
-      constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3_f32(kBlockM, D, false, false)
-                                        : idesc_bf16_f32(kBlockM, D, false, true);
+      constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3_f32(kM, D, false, false)
+                                        : idesc_bf16_f32(kM, D, false, true);
+      // A commit reaches both CTAs of a pair.
+      auto commit = [&](int b) {
+        if constexpr (PAIR) mma_commit_pair(bar(b), 3);
+        else mma_commit(bar(b));
+      };
       const uint32_t q_smem = sbase + C::kQOff;
       const uint32_t ring = sbase + C::kRingOff;
       auto slot_of = [](int idx) { return idx % C::kSlots; };
       auto parity_of = [](int idx) { return static_cast<uint32_t>((idx / C::kSlots) & 1); };
 
       // S_t = Q_t K^T : M = 128 query rows, N = 128 keys, K = d (16 per MMA).
-      // Both operands K-major, 128B-swizzled: 64 columns per 16 KB block.
+      // Both operands K-major, 128B-swizzled: 64 columns per 16 KB block
+      // (pair mode: each CTA's K half is 64 keys, 64 columns per 8 KB block).
       auto issue_s = [&](int t, int kslot) {
         const uint32_t a0 = q_smem + t * C::kTileBytes;
-        const uint32_t b0 = ring + kslot * C::kTileBytes;
+        const uint32_t b0 = ring + kslot * C::kSlotBytes;
         const uint32_t dcol = tmem_base + C::kSCol0 + t * 128;
         if constexpr (FP8) {
 #pragma unroll
@@ -292,17 +404,23 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-            mma_ss(dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), kIdescS,
-                   kk > 0 ? 1u : 0u);
+            if constexpr (PAIR) {
+              const uint32_t boff = (kk >> 2) * (C::kSlotBytes / 2) + (kk & 3) * 32;
+              mma_ss_pair(dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + boff, 16, 1024),
+                          kIdescS, kk > 0 ? 1u : 0u);
+            } else {
+              mma_ss(dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), kIdescS,
+                     kk > 0 ? 1u : 0u);
+            }
           }
         }
       };
       // O_t += P_t V : M = 128, N = d, K = 128 keys.  P_t (bf16, two per
       // 32-bit column) sits in tensor memory over S_t; V is MN-major in shared
       // memory (d contiguous), 8-key groups 1024 B apart, 64-wide d blocks
-      // kHalfBytes apart.
+      // kHalfBytes apart (pair mode: one 64-wide block per CTA).
       auto issue_pv = [&](int t, int vslot, bool accumulate) {
-        const uint32_t b0 = ring + vslot * C::kTileBytes;
+        const uint32_t b0 = ring + vslot * C::kSlotBytes;
         const uint32_t acol = tmem_base + C::kSCol0 + t * 128;
         const uint32_t dcol = tmem_base + C::kOCol0 + t * D;
         if constexpr (FP8) {
@@ -315,8 +433,12 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         } else {
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            mma_ts(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024), kIdescPV,
-                   (accumulate || kk > 0) ? 1u : 0u);
+            if constexpr (PAIR)
+              mma_ts_pair(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024),
+                          kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+            else
+              mma_ts(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024), kIdescPV,
+                     (accumulate || kk > 0) ? 1u : 0u);
           }
         }
       };
@@ -331,24 +453,24 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       int base = 0, q_items = 0;
       int np0 = 0, np1 = 0;
       for (int round = 0; ok; ++round) {
-        const int wi = fwd_item_index(round);
+        const int wi = fwd_item_index<PAIR>(round);
         if (wi >= p.n_items) break;
-        const FwdItem item = fwd_item(p, wi, n_ktiles);
+        const FwdItem item = item_of(wi);
         if (item.nmax == 0) continue;
-        ok = mbar_wait(bar(C::kBarQFull), (q_items++) & 1, ctl, kSiteQFull);
-        if (ok) ok = mbar_wait(bar(C::kBarFull + slot_of(base)), parity_of(base), ctl, kSiteKFull);
+        ok = mbar_wait<PAIR>(bar(C::kBarQFull), (q_items++) & 1, ctl, kSiteQFull);
+        if (ok) ok = mbar_wait<PAIR>(bar(C::kBarFull + slot_of(base)), parity_of(base), ctl, kSiteKFull);
         if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
           if (item.nkv(t) > 0) {
             issue_s(t, slot_of(base));
-            mma_commit(bar(C::kBarSFull + t));
+            commit(C::kBarSFull + t);
           }
-        if (item.nmax == 1) mma_commit(bar(C::kBarQEmpty));  // every S of the item issued
-        mma_commit(bar(C::kBarEmpty + slot_of(base)));
+        if (item.nmax == 1) commit(C::kBarQEmpty);  // every S of the item issued
+        commit(C::kBarEmpty + slot_of(base));
         for (int j = 0; ok && j < item.nmax; ++j) {
           const int vidx = base + 2 * j + 1, kidx = base + 2 * j + 2;
-          ok = mbar_wait(bar(C::kBarFull + slot_of(vidx)), parity_of(vidx), ctl, kSiteVFull);
+          ok = mbar_wait<PAIR>(bar(C::kBarFull + slot_of(vidx)), parity_of(vidx), ctl, kSiteVFull);
           if (!ok) break;
           tc_fence_after();
           bool k_next_ready = false;
@@ -356,33 +478,34 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
           for (int t = 0; t < 2; ++t) {
             if (!ok) break;
             if (j >= item.nkv(t)) continue;
-            ok = mbar_wait(bar(C::kBarPFull + t), (t ? np1 : np0) & 1, ctl, kSitePFull);
+            ok = mbar_wait<PAIR>(bar(C::kBarPFull + t), (t ? np1 : np0) & 1, ctl, kSitePFull);
             if (!ok) break;
             if (t) ++np1; else ++np0;
             tc_fence_after();
             issue_pv(t, slot_of(vidx), j > 0);
             if (j == item.nkv(t) - 1) {
-              mma_commit(bar(C::kBarOFull + t));
+              commit(C::kBarOFull + t);
             } else {
               if (!k_next_ready) {
-                ok = mbar_wait(bar(C::kBarFull + slot_of(kidx)), parity_of(kidx), ctl, kSiteKFull);
+                ok = mbar_wait<PAIR>(bar(C::kBarFull + slot_of(kidx)), parity_of(kidx), ctl, kSiteKFull);
                 if (!ok) break;
                 tc_fence_after();
                 k_next_ready = true;
               }
               issue_s(t, slot_of(kidx));
-              mma_commit(bar(C::kBarSFull + t));
+              commit(C::kBarSFull + t);
             }
           }
           if (!ok) break;
-          if (j + 2 == item.nmax) mma_commit(bar(C::kBarQEmpty));  // the item's last S issued
-          mma_commit(bar(C::kBarEmpty + slot_of(vidx)));
-          if (k_next_ready) mma_commit(bar(C::kBarEmpty + slot_of(kidx)));
+          if (j + 2 == item.nmax) commit(C::kBarQEmpty);  // the item's last S issued
+          commit(C::kBarEmpty + slot_of(vidx));
+          if (k_next_ready) commit(C::kBarEmpty + slot_of(kidx));
         }
         base += 2 * item.nmax;
       }
       // Every MMA this thread issued must finish before tensor memory is freed.
-      mma_commit(bar(C::kBarMmaDone));
+      if constexpr (PAIR) mma_commit_pair(bar(C::kBarMmaDone), 1);
+      else mma_commit(bar(C::kBarMmaDone));
       mbar_wait_drain(bar(C::kBarMmaDone), 0);
     }
    }
@@ -392,6 +515,9 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     const int t = warp >> 2;             // query tile of this warpgroup
     const int quarter = warp & 3;        // tensor-memory lane quarter
     const int row = quarter * 32 + lane;  // row within the query tile
+    // first row of this warpgroup's query tile within the item (pair mode:
+    // query tile 2t + rank of the pair's 512 rows)
+    const int tile_row0 = PAIR ? (2 * t + static_cast<int>(rank)) * kBlockM : t * kBlockM;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t t_s = lane_base + C::kSCol0 + t * 128;
     const uint32_t t_o = lane_base + C::kOCol0 + t * D;
@@ -403,19 +529,19 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
-      const int wi = fwd_item_index(round);
+      const int wi = fwd_item_index<PAIR>(round);
       if (wi >= p.n_items) break;
       // Key tiles of this warpgroup's query tile in the item's range, the
-      // range's first key tile and the item's first diagonal key tile, kept
-      // in a small volatile array (so in local memory, like a spill slot):
-      // more live registers in the tile loop below make ptxas spill about 25
-      // others.
-      const FwdItem itm = fwd_item(p, wi, n_ktiles);
-      volatile int iv[4] = {itm.nkv0, itm.nkv1, itm.kb, itm.q0 / kBlockN};
+      // range's first key tile and the index of this warpgroup's query tile
+      // (its diagonal key tile), kept in a small volatile array (so in local
+      // memory, like a spill slot): more live registers in the tile loop
+      // below make ptxas spill about 25 others.
+      const FwdItem itm = item_of(wi);
+      volatile int iv[4] = {itm.nkv0, itm.nkv1, itm.kb, (itm.q0 + tile_row0) / kBlockN};
       if (iv[t] == 0) {
         // Split mode: an empty key range still leaves its partial result
         // for the merge (weight exp(-inf) = 0).
-        const int qp = itm.q0 + t * kBlockM + row;
+        const int qp = itm.q0 + tile_row0 + row;
         if (itm.part >= 0 && qp < p.N) {
           const size_t prow = static_cast<size_t>(itm.part) * 2 * kBlockM + t * kBlockM + row;
           float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
@@ -426,7 +552,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         continue;
       }
       if constexpr (FP8) {
-        const int qp = itm.q0 + t * kBlockM + row;
+        const int qp = itm.q0 + tile_row0 + row;
         const float qd = qp < p.N ? p.q_descale[static_cast<size_t>(itm.bh) * p.N + qp] : 1.0f;
         const float ka = __uint_as_float(p.fp8_amax[itm.bh]);
         c = p.c * qd * (ka > 0.0f ? ka * (1.0f / 448.0f) : 1.0f);
@@ -452,10 +578,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         reg_fence(r[3]);
 
         const int jabs = iv[2] + j;  // key tile index
-        const bool edge = (p.causal && jabs == iv[3] + t) || (ragged && jabs == n_ktiles - 1);
+        // causal: the diagonal tile (pair mode: and the tile after it, which
+        // the earlier CTA of the pair masks whole)
+        const bool edge = (p.causal && (PAIR ? jabs >= iv[3] : jabs == iv[3])) ||
+                          (ragged && jabs == n_ktiles - 1);
         if (edge) {
           const int kbase = jabs * kBlockN;
-          const int qpos = fwd_item(p, wi, n_ktiles).q0 + t * kBlockM + row;
+          const int qpos = iv[3] * kBlockN + row;
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
@@ -558,7 +687,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(C::kBarPFull + t));
+        if constexpr (PAIR) {
+          // one arrival per warp, on rank 0's barrier
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(cluster_smem(bar(C::kBarPFull + t), 0));
+        } else {
+          mbar_arrive(bar(C::kBarPFull + t));
+        }
       }
       float l;
       {
@@ -576,9 +711,9 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
           tc_fence_after();
-          const FwdItem item = fwd_item(p, wi, n_ktiles);
+          const FwdItem item = item_of(wi);
           const int bh = item.bh;
-          const int qpos = item.q0 + t * kBlockM + row;
+          const int qpos = item.q0 + tile_row0 + row;
           const bool in_range = qpos < p.N;
           float inv_l = 1.0f / l;
           float lse_row = m_used * p.ln2 + logf(l);
@@ -636,10 +771,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // pair mode: neither CTA frees tensor memory or leaves (its shared memory
+  // is an operand of rank 0's MMAs) before both are done
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   if (warp == C::kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
@@ -666,6 +805,40 @@ cudaError_t launch_fwd_dp(const FwdParams& p, cudaStream_t stream) {
   return launched(1);
 }
 
+// Pair mode: clusters of two CTAs, persistent (as many pairs as fit at
+// once, each walking the work items).
+cudaError_t launch_fwd_pair(const FwdParams& p, cudaStream_t stream) {
+  using C = FwdCfg<128, false, true>;
+  auto kernel = fa_fwd_kernel<128, 0, false, true>;
+  cudaFuncAttributes attr;
+  cudaError_t err = cudaFuncGetAttributes(&attr, kernel);
+  if (err != cudaSuccess) return err;
+  if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  int pairs = 0;
+  cfg.gridDim = dim3(2 * static_cast<unsigned int>(p.n_items));
+  err = cudaOccupancyMaxActiveClusters(&pairs, kernel, &cfg);
+  if (err != cudaSuccess) return err;
+  if (pairs < 1) return cudaErrorInvalidConfiguration;
+  if (pairs > p.n_items) pairs = p.n_items;
+  cfg.gridDim = dim3(2 * static_cast<unsigned int>(pairs));
+  err = cudaLaunchKernelEx(&cfg, kernel, p);
+  if (err != cudaSuccess) return err;
+  return launched(1);
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
   switch (p.poly_per_octet) {
@@ -680,6 +853,7 @@ cudaError_t launch_fwd_d(const FwdParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdParams& p, int d, cudaStream_t stream) {
+  if (p.pair) return (d == 128 && !p.fp8) ? launch_fwd_pair(p, stream) : cudaErrorInvalidValue;
   if (p.fp8) return d == 128 ? launch_fwd_dp<128, 0, true>(p, stream) : cudaErrorInvalidValue;
   if (d == 128) return launch_fwd_d<128>(p, stream);
   if (d == 64) return launch_fwd_d<64>(p, stream);

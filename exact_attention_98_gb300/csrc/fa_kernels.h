@@ -33,7 +33,7 @@ struct FwdParams {
   unsigned int* status;  // device status word
   int N;
   int BH;
-  int n_qblk;   // ceil(N / 256): a work item is two 128-row query tiles
+  int n_qblk;   // ceil(N / 256): a work item is two 128-row query tiles (pair: see below)
   int n_items;  // n_qblk * BH * num_splits
   // Split-KV: work items from block split_from on cut their key tiles into
   // num_splits contiguous ranges, one item each; such an item writes O
@@ -51,6 +51,11 @@ struct FwdParams {
   int fp8;
   const float* q_descale;       // [BH, N]
   const unsigned int* fp8_amax;  // [2 * BH]: K then V amax per head (fp32 bits)
+  // Pair mode (pair != 0; bf16, d = 128, no split): clusters of two CTAs
+  // share each product (M = 256); a work item is 512 query rows, n_qblk =
+  // ceil(N / 512), and tm_k's box is 64 rows (each CTA loads half of a K
+  // tile).
+  int pair;
   int causal;
   float c;          // scale * log2(e): scores enter exp2 in these units
   float ln2;        // ln(2), to turn the log2-unit row max into LSE

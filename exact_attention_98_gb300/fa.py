@@ -46,6 +46,8 @@ def _load() -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_2cta.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd_2cta.restype = i
     lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.fa_fwd_splitkv_workspace_bytes.restype = sz
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp, sz, vp]
@@ -164,6 +166,13 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
     B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o)), lse)
     _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
                       int(bool(causal)), _stream(stream)), "fa_fwd")
+
+
+def fa_fwd_2cta(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
+    """fa_fwd computed by CTA pairs sharing each M = 256 product (d = 128)."""
+    B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o)), lse)
+    _check(lib.fa_fwd_2cta(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+                           int(bool(causal)), _stream(stream)), "fa_fwd_2cta")
 
 
 def fa_fwd_splitkv_workspace_bytes(B: int, H: int, N: int, d: int, num_splits: int) -> int:
@@ -295,14 +304,19 @@ def default_scale(d: int) -> float:
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None,
-            num_splits: int = 1):
+            num_splits: int = 1, two_cta: bool = False):
     """Returns (o, lse) freshly allocated on q's device.  num_splits > 1:
-    split-KV forward (fa_fwd_splitkv) with a freshly allocated workspace."""
+    split-KV forward (fa_fwd_splitkv) with a freshly allocated workspace;
+    two_cta: the CTA-pair forward (fa_fwd_2cta)."""
     B, H, N, d = _shape(q)
     scale = default_scale(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if num_splits == 1:
+    if two_cta:
+        if num_splits != 1:
+            raise ValueError("the CTA-pair forward has no key-range split")
+        fa_fwd_2cta(q, k, v, o, lse, scale, causal, stream)
+    elif num_splits == 1:
         fa_fwd(q, k, v, o, lse, scale, causal, stream)
     else:
         n = fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits)

@@ -71,6 +71,25 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int N, int d, float scale, int causal, void* stream);
 
 /*
+ * 2-CTA forward: the same operation, arguments and errors as fa_fwd, computed
+ * by pairs of CTAs (a cluster of two on one TPC) that share every product as
+ * one M = 256 tcgen05 MMA (cta_group::2): each CTA keeps two of the pair's
+ * four 128-row query tiles with their S, P and O in its own tensor memory,
+ * and loads half of every K tile (64 keys) and half of every V tile (64 of
+ * the d columns), so each K/V tile crosses from L2 into the SM pair once.
+ * ("FlashAttention-3 и FlashAttention-4", section "Режим 2-CTA MMA": two
+ * CTAs on one matrix operation halve the shared-memory load; FlashAttention-4
+ * abstract, items 1 and 3: larger tiles, 2-CTA MMA.)  A work item is 512
+ * query rows of one (batch, head); there is no key-range split.  Only
+ * d = 128 (others return FA_ERR_UNSUPPORTED).  Results are bit-identical to
+ * fa_fwd's.  On GB300 it runs slower than fa_fwd (the forward is limited by
+ * the softmax, not by shared memory, and each P hand-off waits for both
+ * CTAs); it is kept as the measured variant.
+ */
+int fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int N, int d, float scale, int causal, void* stream);
+
+/*
  * Split-KV forward: the same results as fa_fwd (within rounding), computed
  * with each query tile's key tiles cut into num_splits contiguous ranges
  * that run as separate work items, for problems with too few (batch, head,
@@ -246,7 +265,7 @@ int fa_timing_last_ms(int kernel, float* ms);
  * e.g. in a timed region: fa_fwd launches one kernel, or two when it splits
  * its last partial round of work (the forward, then the merge); fa_bwd three;
  * fa_bwd_deterministic three; fa_fwd_fp8 five (four preparation kernels and
- * the forward); fa_fwd_splitkv two.
+ * the forward); fa_fwd_splitkv two; fa_fwd_2cta one.
  */
 unsigned long long fa_launch_count(void);
 

@@ -72,25 +72,26 @@ def to64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def run_fwd(B, H, N, d, causal, seed=0, stress=False, scale=None, num_splits=1):
+def run_fwd(B, H, N, d, causal, seed=0, stress=False, scale=None, num_splits=1, two_cta=False):
     from exact_attention_98_gb300 import fa
 
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     q, k, v, _ = attention_inputs(B, H, N, d, seed=seed, stress=stress, with_dout=False)
     dev = torch.device("cuda")
     o, lse = fa.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, scale=scale,
-                        num_splits=num_splits)
+                        num_splits=num_splits, two_cta=two_cta)
     status = fa.fa_last_device_status()
     assert status == fa.FA_OK, fa.status_string(status)
     return (q, k, v), to64(o), to64(lse), scale
 
 
 def compare_fwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_per_head=None,
-                num_splits=1):
+                num_splits=1, two_cta=False):
     """Forward parity.  full_heads: number of leading (b, h) slices compared on
     every row (None = all); the others on sampled rows.  num_splits > 1: the
-    split-KV forward."""
-    (q, k, v), o, lse, scale = run_fwd(B, H, N, d, causal, seed, stress, num_splits=num_splits)
+    split-KV forward; two_cta: the CTA-pair forward."""
+    (q, k, v), o, lse, scale = run_fwd(B, H, N, d, causal, seed, stress, num_splits=num_splits,
+                                       two_cta=two_cta)
     q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
     worst_o = worst_l = 0.0
     for b in range(B):

@@ -87,6 +87,19 @@ def test_fwd_validation(lib):
     assert fwd(lib, q=0, k=0, v=0, o=0, lse=0, B=0) == lib.FA_OK
 
 
+def test_fwd_2cta_validation(lib):
+    def fwd2(d=128, N=128, causal=0, q=0x1000, scale=0.125):
+        a = P(0x1000)
+        return lib.lib.fa_fwd_2cta(P(q), a, a, a, a, 1, 1, N, d, scale, causal, None)
+
+    assert fwd2(d=64) == lib.FA_ERR_UNSUPPORTED  # pairs are built for d = 128 only
+    assert fwd2(N=-1) == lib.FA_ERR_INVALID_ARG
+    assert fwd2(causal=3) == lib.FA_ERR_INVALID_ARG
+    assert fwd2(q=0) == lib.FA_ERR_INVALID_ARG
+    assert fwd2(scale=-1.0) == lib.FA_ERR_INVALID_ARG
+    assert fwd2(q=0, N=0) == lib.FA_OK
+
+
 def bwd(lib, ws=0x10000, ws_bytes=1 << 30, d=64, N=128, dq=0x1000, scale=0.125):
     a = P(0x1000)
     return lib.lib.fa_bwd(a, a, a, a, a, a, P(dq), a, a, 1, 1, N, d, scale, 0, P(ws), ws_bytes, None)
