@@ -318,7 +318,8 @@ size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
   const size_t rows = BH * N;
   const size_t Np = (static_cast<size_t>(N) + 15) / 16 * 16;
   return 2 * round_up(rows * 128) + round_up(BH * 128 * Np) + round_up(rows * sizeof(float)) +
-         round_up(2 * BH * sizeof(unsigned int));
+         round_up(2 * BH * sizeof(unsigned int)) +
+         round_up(fp8_amax_part_count(static_cast<int>(BH), N) * sizeof(float));
 }
 
 int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -351,8 +352,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   const int n_ktiles = (N + kBlockN - 1) / kBlockN;
   if (num_splits < 1 || num_splits > n_ktiles) return FA_ERR_INVALID_ARG;
   if ((fp8 || pair) && d != 128) return FA_ERR_UNSUPPORTED;
-  // the FP8 preparation launches one CTA per (head, 128-key block)
-  if (fp8 && static_cast<long long>(B) * H * ((N + 127) / 128) > 0x7fffffffLL)
+  // the FP8 preparation's second kernel launches one CTA per (head, 256-row
+  // chunk of K) and per (head, 128-key block of V) in one grid
+  if (fp8 && static_cast<long long>(B) * H * ((N + 255) / 256 + (N + 15) / 16 * 16 / 128 + 1) >
+                 0x7fffffffLL)
     return FA_ERR_UNSUPPORTED;
   if (num_splits > 1 || fp8) {
     const size_t need = fp8 ? fa_fwd_fp8_workspace_bytes(B, H, N, d)
@@ -381,6 +384,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     fb.q_descale = reinterpret_cast<float*>(w);
     w += round_up(static_cast<size_t>(rows) * sizeof(float));
     fb.amax = reinterpret_cast<unsigned int*>(w);
+    w += round_up(2 * static_cast<size_t>(BH) * sizeof(unsigned int));
+    fb.amax_part = reinterpret_cast<float*>(w);
     if (!encode_u8_map(&p.tm_q, fb.q8, 128, N, BH, 128) ||
         !encode_u8_map(&p.tm_k, fb.k8, 128, N, BH, 128) ||
         !encode_u8_map(&p.tm_v, fb.v8t, fb.Np, 128, BH, fb.Np))

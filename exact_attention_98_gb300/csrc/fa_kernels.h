@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace fa {
@@ -102,8 +103,11 @@ struct Fp8Buffers {
   uint8_t* k8;          // e4m3 [BH, N, 128], K rotated, one scale per head
   uint8_t* v8t;         // e4m3 [BH, 128, Np], V transposed, one scale per head
   unsigned int* amax;   // [2 * BH]: fp32 bits of the K amax per head, then V
+  float* amax_part;     // [2, BH, ceil(N / 256)]: K, then V amax of each 256-row chunk
   int Np;               // N rounded up to a multiple of 16 (V^T row pitch)
 };
+// Number of floats of Fp8Buffers::amax_part.
+size_t fp8_amax_part_count(int BH, int N);
 // Rotation (optional) and quantisation of Q, K, V into `b`.
 cudaError_t launch_fp8_prepare(const void* q, const void* k, const void* v, const Fp8Buffers& b,
                                int BH, int N, int rotate, cudaStream_t stream);

@@ -264,8 +264,9 @@ int fa_timing_last_ms(int kernel, float* ms);
  * counted).  The difference of two readings counts the launches in between,
  * e.g. in a timed region: fa_fwd launches one kernel, or two when it splits
  * its last partial round of work (the forward, then the merge); fa_bwd three;
- * fa_bwd_deterministic three; fa_fwd_fp8 five (four preparation kernels and
- * the forward); fa_fwd_splitkv two; fa_fwd_2cta one.
+ * fa_bwd_deterministic three; fa_fwd_fp8 three (two preparation kernels and
+ * the forward; four with the merge, as fa_fwd); fa_fwd_splitkv two;
+ * fa_fwd_2cta one.
  */
 unsigned long long fa_launch_count(void);
 

@@ -108,6 +108,6 @@ def test_launch_counter_per_call():
                       device="cuda")
     assert count(lambda: fa.fa_fwd_splitkv(q, k, v, o, lse, scale, False, 2, ws2)) == 2
     ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
-    assert count(lambda: fa.fa_fwd_fp8(q, k, v, o, lse, scale, False, True, ws8)) == 5
+    assert count(lambda: fa.fa_fwd_fp8(q, k, v, o, lse, scale, False, True, ws8)) == 3
     assert count(lambda: fa.fa_fwd_2cta(q, k, v, o, lse, scale, False)) == 1
     assert fa.fa_last_device_status() == fa.FA_OK
