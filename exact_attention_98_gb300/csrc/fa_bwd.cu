@@ -1,28 +1,31 @@
 // Backward exact attention for sm_103a: key/value-stationary CTAs, all five
 // GEMMs of a tile on tcgen05 with their accumulators in tensor memory, dQ
-// added into an fp32 accumulator by bulk TMA reductions.
+// added into an fp32 accumulator.
 //
 // The pages single out the backward pass as limited by shared-memory traffic
 // and by its reductions and atomic updates ("Pourquoi l'approche standard ne
 // fonctionne plus" of the French page; "Режим 2-CTA MMA" of "FlashAttention-3
 // и FlashAttention-4"; FlashAttention-4 abstract item 3).  This kernel keeps
 // every intermediate it can in tensor memory so that shared memory carries
-// only operands, and adds dQ tile by tile with bulk reductions instead of one
-// atomic per element:
+// only operands, and adds dQ tile by tile: at d = 128 from tensor memory with
+// warp-coalesced fp32 reductions (each warp instruction adds 32 consecutive
+// floats of one query row), at d = 64 through bulk TMA reduce-adds of a
+// staged fp32 tile:
 //
 //   tensor memory (512 columns x 128 lanes)
 //     [  0,128)  S^T = K Q_i^T (fp32, lane = key) -> P^T (bf16)
 //     [128,256)  dP^T = V dO_i^T (fp32, lane = key) -> dS^T (bf16)
-//                -> then dQ_i = dS K (fp32, lane = query, d columns)
+//                -> then dQ_i: d = 64, dQ_i = dS K (fp32, lane = query, d
+//                columns); d = 128, dQ_i^T = K^T dS^T (lane = d, 128 query
+//                columns)
 //     [256,256+d)      dV accumulator (lane = key)
 //     [256+d,256+2d)   dK accumulator (lane = key)
 //   Each compute warpgroup owns 64 query columns of S^T and dP^T and packs
 //   its bf16 P^T / dS^T into the first 32 of them, so neither warpgroup
-//   overwrites fp32 values the other has not read yet.  dQ_i = dS K has the
-//   query as its row, so its A operand is dS in shared memory (at d = 128
-//   written over the dO_i tile once dV has consumed it; at d = 64 in its own
-//   buffer).  dQ_i lands in the dP^T columns, so draining it overlaps the next
-//   tile's S^T product and softmax.
+//   overwrites fp32 values the other has not read yet.  The dQ product reads
+//   dS from shared memory (at d = 128 written over the dO_i tile once dV has
+//   consumed it; at d = 64 in its own buffer).  dQ_i lands in the dP^T
+//   columns, so draining it overlaps the next tile's S^T product and softmax.
 //
 // Per query tile i (MMA issue order):
 //   S^T = K Q_i^T ; [dQ_{i-1} drained] dP^T = V dO_i^T ;
@@ -37,28 +40,23 @@
 // zeros elsewhere.  The compute warps then need no per-query loads at all:
 // P = exp2(c S'^T) and dS = scale P dP'^T.
 //
-// The per-query terms -LSE_i / scale and -D_i enter through the tensor core
-// as a rank-1 bias: one more K = 16 MMA adds ones(128 x 16) * b^T onto S^T
-// (and onto dP^T), where column k of b holds the query's value split into
-// bf16 hi + lo parts (about 16 significant bits) in its first two entries and
-// zeros elsewhere.  The compute warps then need no per-query loads at all:
-// P = exp2(c S'^T) and dS = scale P dP'^T.
-//
 // Warp roles (512 threads = four warpgroups):
 //   warps 0-7   compute: two warpgroups, thread = key row, warpgroup w takes
 //               query columns [64w, 64w + 64); at the end warpgroup 0 writes
 //               dV, warpgroup 1 dK
-//   warps 8-11  dQ drain: thread = query row; tensor memory -> registers (in
-//               two batches, after which the columns are free again) ->
-//               swizzled 16-column fp32 chunks in the Q_i and dO_i buffers
-//               (dead once dQ_i is computed: together exactly one fp32 dQ
-//               tile) -> TMA reduce-adds; the stage goes back to the loader
-//               when the TMA has read it
+//   warps 8-11  dQ drain.  d = 128: thread = d index of dQ_i^T; the whole
+//               tile leaves tensor memory in one batch (after which the
+//               columns are free again), then coalesced fp32 reductions into
+//               the accumulator.  d = 64: thread = query row; tensor memory ->
+//               registers -> swizzled 16-column fp32 chunks in the Q_i and
+//               dO_i buffers (dead once dQ_i is computed: together exactly one
+//               fp32 dQ tile) -> TMA reduce-adds; the stage goes back to the
+//               loader when the TMA has read it
 //   warp  12    loads: K, V once; Q_i, dO_i by TMA; LSE_i, D_i by plain loads
 //   warp  13    tensor-memory allocator; lane 0 issues every MMA
 //   warps 14-15 idle
 // Launched with 128 registers per thread; the warpgroups then re-split them
-// (compute 144, drain 144, load/MMA 64).
+// (compute 144, drain 144, load/MMA 80).
 #include "fa_device.cuh"
 #include "fa_kernels.h"
 
