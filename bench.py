@@ -78,6 +78,36 @@ def kernel_sources_sha256() -> str:
     return h.hexdigest()
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as lscpu or /proc/cpuinfo give it ("" if
+    neither does)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return ""
+
+
+def oracle_fields(tf: float, threads: int, desc: str) -> dict:
+    """The cpu_baseline object: the oracle's rate on its sample, the host it
+    ran on and the time the whole fwd+bwd step of the workload would take at
+    that rate."""
+    B, H, N, d = WORKLOAD["B"], WORKLOAD["H"], WORKLOAD["N"], WORKLOAD["d"]
+    f_fwd, f_bwd = flops(B, H, N, d, False)
+    return {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc,
+            "cpu_model": cpu_model(), "nproc": os.cpu_count(),
+            "projected_full_step_s": (f_fwd + f_bwd) / (tf * 1e12) if tf > 0 else None}
+
+
 def replica_seed(rank: int) -> int:
     """Seed of rank `rank`'s replica batch: each rank works on its own batch."""
     return rank
@@ -170,8 +200,7 @@ def reference_arm(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "attention fwd+bwd B2 H16 N4096 d128 non-causal bf16 inputs",
                    "sample": desc},
-        "cpu_baseline": {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": oracle_fields(tf, threads, desc),
         "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -521,6 +550,9 @@ def native_arm(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": mean_ms,
+        # this rank's step times (the headline uses the mean, max over ranks)
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms),
+                    "max": max(step_ms)},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -566,8 +598,7 @@ def native_arm(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         tf, threads, desc, _, _ = oracle_sample(12.0, steps=1)
-        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                                "sample": desc}
+        line["cpu_baseline"] = oracle_fields(tf, threads, desc)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
