@@ -14,6 +14,10 @@ Recipe (all on the CPU with ``torch.Generator().manual_seed(seed)``):
     and the conditional rescale.
   * Sampled rows of head (b, h): sorted(randperm(N, seed 1 + b*H + h)[:k])
     together with rows 0 and N-1.
+  * Problems too large to draw on the host (tens of GB) are drawn one head at
+    a time on the device: Q, K, V, dO of head h as ``randn`` fp32 [4, N, d]
+    from a generator of that device seeded with seed * 1000003 + h, rounded
+    to bf16 (same distribution, a different stream).
 """
 from __future__ import annotations
 
@@ -49,3 +53,11 @@ def sampled_rows(N: int, k: int, b: int, h: int, H: int):
     rows = set(int(x) for x in pick.tolist())
     rows.update({0, N - 1})
     return sorted(rows)
+
+
+def device_head_inputs(N: int, d: int, seed: int, head: int, device):
+    """Returns (q, k, v, dout) of one head, each a bf16 [N, d] tensor on
+    ``device``, drawn there (see the module docstring)."""
+    g = torch.Generator(device=device).manual_seed(int(seed) * 1000003 + int(head))
+    x = torch.randn((4, N, d), generator=g, device=device, dtype=torch.float32)
+    return tuple(x[i].to(torch.bfloat16) for i in range(4))
