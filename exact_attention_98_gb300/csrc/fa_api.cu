@@ -352,10 +352,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   const int n_ktiles = (N + kBlockN - 1) / kBlockN;
   if (num_splits < 1 || num_splits > n_ktiles) return FA_ERR_INVALID_ARG;
   if ((fp8 || pair) && d != 128) return FA_ERR_UNSUPPORTED;
-  // the FP8 preparation's second kernel launches one CTA per (head, 256-row
-  // chunk of K) and per (head, 128-key block of V) in one grid
-  if (fp8 && static_cast<long long>(B) * H * ((N + 255) / 256 + (N + 15) / 16 * 16 / 128 + 1) >
-                 0x7fffffffLL)
+  // the FP8 preparation counts its work units (three per 128-row block of a
+  // head) in int
+  if (fp8 && static_cast<long long>(B) * H * (3LL * ((N + 127) / 128) + 1) > 0x7fffffffLL)
     return FA_ERR_UNSUPPORTED;
   if (num_splits > 1 || fp8) {
     const size_t need = fp8 ? fa_fwd_fp8_workspace_bytes(B, H, N, d)
@@ -390,7 +389,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
         !encode_u8_map(&p.tm_k, fb.k8, 128, N, BH, 128) ||
         !encode_u8_map(&p.tm_v, fb.v8t, fb.Np, 128, BH, fb.Np))
       return FA_ERR_CUDA;
-    if (launch_fp8_prepare(q, k, v, fb, BH, N, rotate, s) != cudaSuccess) return FA_ERR_CUDA;
+    Fp8Maps maps;
+    if (!encode_tile_map(&maps.q, q, N, BH, d) || !encode_tile_map(&maps.k, k, N, BH, d) ||
+        !encode_tile_map(&maps.v, v, N, BH, d))
+      return FA_ERR_CUDA;
+    unsigned int* status = status_ptr();
+    if (!status) return FA_ERR_CUDA;
+    if (launch_fp8_prepare(maps, fb, BH, N, rotate, status, s) != cudaSuccess) return FA_ERR_CUDA;
     p.q_descale = fb.q_descale;
     p.fp8_amax = fb.amax;
   } else if (!encode_tile_map(&p.tm_q, q, N, BH, d) ||

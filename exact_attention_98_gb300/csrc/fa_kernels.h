@@ -103,14 +103,22 @@ struct Fp8Buffers {
   uint8_t* k8;          // e4m3 [BH, N, 128], K rotated, one scale per head
   uint8_t* v8t;         // e4m3 [BH, 128, Np], V transposed, one scale per head
   unsigned int* amax;   // [2 * BH]: fp32 bits of the K amax per head, then V
-  float* amax_part;     // [2, BH, ceil(N / 256)]: K, then V amax of each 256-row chunk
+  float* amax_part;     // [2, BH, ceil(N / 128)]: K, then V amax of each 128-row block
   int Np;               // N rounded up to a multiple of 16 (V^T row pitch)
 };
 // Number of floats of Fp8Buffers::amax_part.
 size_t fp8_amax_part_count(int BH, int N);
-// Rotation (optional) and quantisation of Q, K, V into `b`.
-cudaError_t launch_fp8_prepare(const void* q, const void* k, const void* v, const Fp8Buffers& b,
-                               int BH, int N, int rotate, cudaStream_t stream);
+// The bf16 inputs of the FP8 preparation: [BH, N, d] maps as the forward's
+// (box {64, 128, 1}, 128-byte swizzle).
+struct Fp8Maps {
+  CUtensorMap q;
+  CUtensorMap k;
+  CUtensorMap v;
+};
+// Rotation (optional) and quantisation of Q, K, V into `b`; bounded waits
+// report through `status`.
+cudaError_t launch_fp8_prepare(const Fp8Maps& maps, const Fp8Buffers& b, int BH, int N, int rotate,
+                               unsigned int* status, cudaStream_t stream);
 
 // The launch wrappers end with `return launched(n)`: the launch error of the
 // n kernels just launched, which are added to the library's launch count

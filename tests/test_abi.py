@@ -156,9 +156,9 @@ def test_fp8_workspace_bytes(lib):
     up = lambda x: (x + 255) // 256 * 256
     B, H, N = 2, 3, 300
     rows, bh, np_ = B * H * N, B * H, 304
-    chunks = (N + 255) // 256  # per-chunk amax slots of K and V
+    blocks = (N + 127) // 128  # per-block amax slots of K and V
     assert ws(B, H, N, 128) == (2 * up(rows * 128) + up(bh * 128 * np_) + up(rows * 4) +
-                                up(2 * bh * 4) + up(2 * bh * chunks * 4))
+                                up(2 * bh * 4) + up(2 * bh * blocks * 4))
     assert ws(B, H, N, 64) == 0  # d = 128 only
     assert ws(0, H, N, 128) == 0
 
