@@ -218,6 +218,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // D and the zeroed dQ accumulator come from the kernel before this one;
+  // the inputs and outputs may belong to earlier work in the stream
+  grid_dependency_wait();
 
   if (warp >= C::kProducerWarp) {
     regs_set<C::kOtherRegs, C::kLaunchRegs>();
@@ -643,7 +646,9 @@ cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
                              C::kSmemBytes);
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(p.n_kblk) * p.BH;
-  fa_bwd_kernel<D><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
+  err = launch_dependent(fa_bwd_kernel<D>, dim3(static_cast<unsigned int>(blocks)), dim3(C::kThreads),
+                         C::kSmemBytes, stream, p);
+  if (err != cudaSuccess) return err;
   return launched(1);
 }
 

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   constexpr int kVec = 8;               // bf16 per 16-byte load
   constexpr int kLanesPerRow = D / kVec;  // 16 (d=128) or 8 (d=64)
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  grid_dependency_wait();  // O from the forward; dQacc may still be read by earlier work
   const long long warp_global = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long row = warp_global * kRowsPerWarp + lane / kLanesPerRow;
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ dq_acc,
                                                        __nv_bfloat16* __restrict__ dq,
                                                        long long n8) {
+  grid_dependency_wait();  // the accumulator of the main kernel before it
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i0 < n8;
        i0 += 4 * stride) {
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float* __restr
                                                             __nv_bfloat16* __restrict__ dq,
                                                             int BH, int N, int d, int n_kblk,
                                                             int causal, long long n8) {
+  grid_dependency_wait();  // the contributions of the main kernel before it
   const int per_row = d / 8;
   const size_t slice = static_cast<size_t>(BH) * N * d;  // one key tile's contributions
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
@@ -134,29 +137,29 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* 
   const long long rows_per_block = (256 / 32) * (32 / (d / 8));
   const long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (d == 128)
-    bwd_pre_kernel<128><<<static_cast<unsigned int>(blocks), 256, 0, stream>>>(o16, do16, dsum,
-                                                                               dq_acc, rows);
-  else if (d == 64)
-    bwd_pre_kernel<64><<<static_cast<unsigned int>(blocks), 256, 0, stream>>>(o16, do16, dsum,
-                                                                              dq_acc, rows);
-  else
-    return cudaErrorInvalidValue;
+  if (d != 128 && d != 64) return cudaErrorInvalidValue;
+  const cudaError_t err = launch_dependent(d == 128 ? bwd_pre_kernel<128> : bwd_pre_kernel<64>,
+                                           dim3(static_cast<unsigned int>(blocks)), dim3(256), 0,
+                                           stream, o16, do16, dsum, dq_acc, rows);
+  if (err != cudaSuccess) return err;
   return launched(1);
 }
 
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, cudaStream_t stream) {
   const long long n8 = elems / 8;  // d is a multiple of 8, so elems is too
-  bwd_post_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
-                                                         n8);
+  const cudaError_t err = launch_dependent(bwd_post_kernel, dim3(grid_for(n8, 256)), dim3(256), 0,
+                                           stream, dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
+  if (err != cudaSuccess) return err;
   return launched(1);
 }
 
 cudaError_t launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, int n_kblk,
                                  int causal, cudaStream_t stream) {
   const long long n8 = static_cast<long long>(BH) * N * d / 8;
-  bwd_dq_reduce_kernel<<<grid_for(n8, 256), 256, 0, stream>>>(
-      dq_part, static_cast<__nv_bfloat16*>(dq), BH, N, d, n_kblk, causal, n8);
+  const cudaError_t err = launch_dependent(bwd_dq_reduce_kernel, dim3(grid_for(n8, 256)), dim3(256),
+                                           0, stream, dq_part, static_cast<__nv_bfloat16*>(dq), BH,
+                                           N, d, n_kblk, causal, n8);
+  if (err != cudaSuccess) return err;
   return launched(1);
 }
 

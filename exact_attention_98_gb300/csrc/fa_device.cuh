@@ -137,6 +137,14 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// Programmatic dependent launch: blocks until the kernels this grid depends
+// on (the stream's earlier work) have completed and their memory operations
+// are visible.  Every kernel launched by launch_dependent() calls it before
+// its first access to data that earlier work produces or may still read.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // CTA pairs: a cluster of two CTAs on one TPC that share each MMA
 // (tcgen05 cta_group::2).  Rank 0 issues the MMAs; operands and accumulators

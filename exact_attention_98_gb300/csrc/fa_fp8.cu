@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(256, 2) fp8_pass1_kernel(const __grid_constant
                                                            int BH, int rotate,
                                                            unsigned int* status) {
   using L = PrepSmem<kPass1Stages>;
+  grid_dependency_wait();  // Q, K, V and the workspace may belong to earlier work in the stream
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -256,6 +257,7 @@ __global__ void __launch_bounds__(256, 2) fp8_quant_kernel(const __grid_constant
                                                            int N, int Np, int BH, int rotate,
                                                            unsigned int* status) {
   using L = PrepSmem<kQuantStages>;
+  grid_dependency_wait();  // the amax slots of pass 1
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -386,10 +388,14 @@ cudaError_t launch_fp8_prepare(const Fp8Maps& maps, const Fp8Buffers& b, int BH,
   if (err != cudaSuccess) return err;
   const long long resident = 2LL * (sms > 0 ? sms : 1);
   const long long units1 = 3LL * BH * nb, units2 = BH * (nb + tiles);
-  fp8_pass1_kernel<<<static_cast<unsigned int>(units1 < resident ? units1 : resident), 256, kSmem1,
-                     stream>>>(maps, b.q8, b.q_descale, b.amax_part, N, BH, rotate, status);
-  fp8_quant_kernel<<<static_cast<unsigned int>(units2 < resident ? units2 : resident), 256, kSmem2,
-                     stream>>>(maps, b.k8, b.v8t, b.amax_part, b.amax, N, b.Np, BH, rotate, status);
+  err = launch_dependent(fp8_pass1_kernel, dim3(static_cast<unsigned int>(units1 < resident ? units1 : resident)),
+                         dim3(256), kSmem1, stream, maps, b.q8, b.q_descale, b.amax_part, N, BH, rotate,
+                         status);
+  if (err != cudaSuccess) return err;
+  err = launch_dependent(fp8_quant_kernel, dim3(static_cast<unsigned int>(units2 < resident ? units2 : resident)),
+                         dim3(256), kSmem2, stream, maps, b.k8, b.v8t,
+                         static_cast<const float*>(b.amax_part), b.amax, N, b.Np, BH, rotate, status);
+  if (err != cudaSuccess) return err;
   return launched(2);
 }
 

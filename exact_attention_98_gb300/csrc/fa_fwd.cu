@@ -247,6 +247,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Q, K, V and the outputs may belong to the stream's earlier work
+  grid_dependency_wait();
 
   if (warp >= 8) {
    regs_set<C::kOtherRegs, C::kLaunchRegs>();
@@ -801,7 +803,9 @@ cudaError_t launch_fwd_dp(const FwdParams& p, cudaStream_t stream) {
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
   const int blocks = p.n_items < sms ? p.n_items : sms;
-  fa_fwd_kernel<D, POLY, FP8><<<static_cast<unsigned int>(blocks), C::kThreads, C::kSmemBytes, stream>>>(p);
+  err = launch_dependent(fa_fwd_kernel<D, POLY, FP8>, dim3(static_cast<unsigned int>(blocks)),
+                         dim3(C::kThreads), C::kSmemBytes, stream, p);
+  if (err != cudaSuccess) return err;
   return launched(1);
 }
 
@@ -817,16 +821,18 @@ cudaError_t launch_fwd_pair(const FwdParams& p, cudaStream_t stream) {
   err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = 2;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // as launch_dependent
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
   int pairs = 0;
   cfg.gridDim = dim3(2 * static_cast<unsigned int>(p.n_items));
   err = cudaOccupancyMaxActiveClusters(&pairs, kernel, &cfg);
@@ -834,6 +840,7 @@ cudaError_t launch_fwd_pair(const FwdParams& p, cudaStream_t stream) {
   if (pairs < 1) return cudaErrorInvalidConfiguration;
   if (pairs > p.n_items) pairs = p.n_items;
   cfg.gridDim = dim3(2 * static_cast<unsigned int>(pairs));
+  cfg.numAttrs = 2;
   err = cudaLaunchKernelEx(&cfg, kernel, p);
   if (err != cudaSuccess) return err;
   return launched(1);
@@ -872,6 +879,7 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const float* __restrict_
                                                         float* __restrict__ lse, int num_splits,
                                                         int n_blocks, int split_from, int causal,
                                                         int BH, int n_qblk, int N, int d) {
+  grid_dependency_wait();  // the partial results of the forward before it
   const int per_row = d / 8;
   const long long n8 = static_cast<long long>(n_blocks) * 2 * kBlockM * per_row;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
@@ -922,9 +930,12 @@ cudaError_t launch_fwd_merge(const FwdParams& p, void* o, float* lse, int d,
   long long blocks = (n8 + 255) / 256;
   const long long cap = 152LL * 8;
   if (blocks > cap) blocks = cap;
-  fwd_merge_kernel<<<static_cast<unsigned int>(blocks < 1 ? 1 : blocks), 256, 0, stream>>>(
-      p.o_part, p.lse_part, static_cast<__nv_bfloat16*>(o), lse, p.num_splits, n_blocks,
-      p.split_from, p.causal, p.BH, p.n_qblk, p.N, d);
+  const cudaError_t err = launch_dependent(
+      fwd_merge_kernel, dim3(static_cast<unsigned int>(blocks < 1 ? 1 : blocks)), dim3(256), 0,
+      stream, static_cast<const float*>(p.o_part), static_cast<const float*>(p.lse_part),
+      static_cast<__nv_bfloat16*>(o), lse, p.num_splits, n_blocks, p.split_from, p.causal, p.BH,
+      p.n_qblk, p.N, d);
+  if (err != cudaSuccess) return err;
   return launched(1);
 }
 

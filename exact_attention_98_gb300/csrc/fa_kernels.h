@@ -8,6 +8,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace fa {
 
 // Tile shape shared by the forward and backward kernels: 128 query rows x 128
@@ -119,6 +121,27 @@ struct Fp8Maps {
 // report through `status`.
 cudaError_t launch_fp8_prepare(const Fp8Maps& maps, const Fp8Buffers& b, int BH, int N, int rotate,
                                unsigned int* status, cudaStream_t stream);
+
+// Launches `kernel` on `stream` as a programmatic dependent launch: it may
+// start (allocate, initialise its barriers, set up tensor memory) while the
+// kernel before it in the stream is finishing, and it calls
+// grid_dependency_wait() before it reads or writes anything that kernel, or
+// any earlier work in the stream, produces or consumes.
+template <typename... P, typename... A>
+cudaError_t launch_dependent(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // The launch wrappers end with `return launched(n)`: the launch error of the
 // n kernels just launched, which are added to the library's launch count
