@@ -11,11 +11,14 @@
 //   * exponentials partly on the FMA pipe (exp2_poly) and partly on MUFU;
 //   * conditional rescaling: O_t and the row sum are rescaled only when a row
 //     max grows by more than kRescaleThreshold (log2 units).
-// On GB300 the MUFU unit is not what limits this softmax (its issue slots
-// are): measured on B2 H16 N4096 d128, the forward ran at 1073 TFLOP/s with
-// every exponential on MUFU and at 861 / 859 / 699 TFLOP/s with 1 / 2 / 3 of
-// every 8 on the FMA pipe, so the default share is 0; the other shares stay
-// instantiated and selectable.
+// On GB300 the MUFU unit is not what limits this kernel: in steady state a
+// softmax warpgroup needs ~1250 cycles per key tile, less than the ~1600
+// cycles of products the other warpgroup keeps the tensor pipe busy with,
+// and the tensor pipe sets the pace.  Exponentials moved to the FMA pipe
+// lengthen the softmax past that budget: measured on B2 H16 N4096 d128, the
+// forward ran at 1073 TFLOP/s with every exponential on MUFU and at 861 /
+// 859 / 699 TFLOP/s with 1 / 2 / 3 of every 8 on the FMA pipe, so the
+// default share is 0; the other shares stay instantiated and selectable.
 //
 // Persistent CTAs (one per SM) walk the work items; an item is two 128-row
 // query tiles of one (batch, head).  Keys and values stream through a ring of

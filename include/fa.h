@@ -82,9 +82,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  * abstract, items 1 and 3: larger tiles, 2-CTA MMA.)  A work item is 512
  * query rows of one (batch, head); there is no key-range split.  Only
  * d = 128 (others return FA_ERR_UNSUPPORTED).  Results are bit-identical to
- * fa_fwd's.  On GB300 it runs slower than fa_fwd (the forward is limited by
- * the softmax, not by shared memory, and each P hand-off waits for both
- * CTAs); it is kept as the measured variant.
+ * fa_fwd's.  On GB300 it runs slower than fa_fwd (shared memory is not what
+ * limits the forward, and every product of the pair waits on operands and P
+ * of both CTAs); it is kept as the measured variant.
  */
 int fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int N, int d, float scale, int causal, void* stream);
