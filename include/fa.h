@@ -19,12 +19,20 @@
  *   - d must be 64 or 128.  Any N >= 0 is accepted; a ragged last tile is
  *     masked.  B, H, N of 0 are a no-op that returns FA_OK.
  *   - Queries and keys have the same length N, so "causal" is unambiguous.
- *   - The caller owns every buffer; the library allocates no device memory.
+ *   - The caller owns every input, output and workspace buffer.  The only
+ *     device memory the library takes on its own is fa_fwd's scratch for its
+ *     split last round (from a private stream-ordered pool, see fa_fwd) and
+ *     fa_bwd_noalloc's fixed scratch array.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  The return value reports argument validation and
  *     launch errors only.  A kernel that gives up on a bounded wait records
  *     FA_ERR_TIMEOUT in a device status word instead of hanging; read it
- *     with fa_last_device_status().
+ *     with fa_last_device_status().  There is one status word per device,
+ *     shared by every stream and host thread: after work on several
+ *     streams, a timeout is reported to whichever caller reads it first.
+ *   - Each kernel is launched so that it may start while the previous
+ *     kernel in `stream` finishes (programmatic dependent launch); it waits
+ *     for that work before touching any buffer.
  *   - Input and output buffers must not overlap.
  */
 #ifndef FA_H_
