@@ -396,26 +396,27 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       // S_t = Q_t K^T : M = 128 query rows, N = 128 keys, K = d (16 per MMA).
       // Both operands K-major, 128B-swizzled: 64 columns per 16 KB block
       // (pair mode: each CTA's K half is 64 keys, 64 columns per 8 KB block).
+      // Descriptors are built once per group and stepped by adding the byte
+      // offset >> 4 to the start-address field: every address here is below
+      // 256 KB, so the 14-bit field never carries into the next one.
+      auto step = [](uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); };
       auto issue_s = [&](int t, int kslot) {
-        const uint32_t a0 = q_smem + t * C::kTileBytes;
-        const uint32_t b0 = ring + kslot * C::kSlotBytes;
+        const uint64_t a0 = sdesc_sw128(q_smem + t * C::kTileBytes, 16, 1024);
+        const uint64_t b0 = sdesc_sw128(ring + kslot * C::kSlotBytes, 16, 1024);
         const uint32_t dcol = tmem_base + C::kSCol0 + t * 128;
         if constexpr (FP8) {
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)  // 32 e4m3 = 32 bytes of the 128-byte row
-            mma_ss_f8(dcol, sdesc_sw128(a0 + kk * 32, 16, 1024), sdesc_sw128(b0 + kk * 32, 16, 1024),
-                      kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss_f8(dcol, step(a0, kk * 32), step(b0, kk * 32), kIdescS, kk > 0 ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
             if constexpr (PAIR) {
               const uint32_t boff = (kk >> 2) * (C::kSlotBytes / 2) + (kk & 3) * 32;
-              mma_ss_pair(dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + boff, 16, 1024),
-                          kIdescS, kk > 0 ? 1u : 0u);
+              mma_ss_pair(dcol, step(a0, off), step(b0, boff), kIdescS, kk > 0 ? 1u : 0u);
             } else {
-              mma_ss(dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), kIdescS,
-                     kk > 0 ? 1u : 0u);
+              mma_ss(dcol, step(a0, off), step(b0, off), kIdescS, kk > 0 ? 1u : 0u);
             }
           }
         }
@@ -425,24 +426,25 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       // memory (d contiguous), 8-key groups 1024 B apart, 64-wide d blocks
       // kHalfBytes apart (pair mode: one 64-wide block per CTA).
       auto issue_pv = [&](int t, int vslot, bool accumulate) {
-        const uint32_t b0 = ring + vslot * C::kSlotBytes;
         const uint32_t acol = tmem_base + C::kSCol0 + t * 128;
         const uint32_t dcol = tmem_base + C::kOCol0 + t * D;
         if constexpr (FP8) {
           // P_t as e4m3, four per 32-bit column: 32 keys = 8 columns per MMA;
           // V^T rows of 128 keys, 32 keys = 32 bytes per MMA.
+          const uint64_t b0 = sdesc_sw128(ring + vslot * C::kSlotBytes, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 32; ++kk)
-            mma_ts_f8(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 32, 16, 1024), kIdescPV,
+            mma_ts_f8(dcol, acol + kk * 8, step(b0, kk * 32), kIdescPV,
                       (accumulate || kk > 0) ? 1u : 0u);
         } else {
+          const uint64_t b0 = sdesc_sw128(ring + vslot * C::kSlotBytes, C::kHalfBytes, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk) {
             if constexpr (PAIR)
-              mma_ts_pair(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024),
-                          kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+              mma_ts_pair(dcol, acol + kk * 8, step(b0, kk * 2048), kIdescPV,
+                          (accumulate || kk > 0) ? 1u : 0u);
             else
-              mma_ts(dcol, acol + kk * 8, sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024), kIdescPV,
+              mma_ts(dcol, acol + kk * 8, step(b0, kk * 2048), kIdescPV,
                      (accumulate || kk > 0) ? 1u : 0u);
           }
         }
