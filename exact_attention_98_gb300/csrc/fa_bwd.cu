@@ -292,12 +292,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const uint32_t v_smem = sbase + C::kVOff;
       // X^T = A B^T with A = K or V (key rows, K-major over d) and
       // B = Q_i or dO_i (query rows, K-major over d): M = keys, N = queries.
+      // Descriptors are built once per product and stepped by adding the
+      // byte offset >> 4 to the start-address field: every address here is
+      // below 256 KB, so the 14-bit field never carries into the next one.
+      // Each base goes through an empty asm so that it is rebuilt per product
+      // instead of being held in a register across the tile loop.
+      auto base = [](uint64_t desc) {
+        asm volatile("" : "+l"(desc));
+        return desc;
+      };
+      auto step = [](uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); };
       auto issue_nt = [&](uint32_t a0, uint32_t b0, uint32_t dcol) {
+        const uint64_t ad = base(sdesc_sw128(a0, 16, 1024));
+        const uint64_t bd = base(sdesc_sw128(b0, 16, 1024));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem_base + dcol, sdesc_sw128(a0 + off, 16, 1024),
-                 sdesc_sw128(b0 + off, 16, 1024), kIdescSq, kk > 0 ? 1u : 0u);
+          mma_ss(tmem_base + dcol, step(ad, off), step(bd, off), kIdescSq, kk > 0 ? 1u : 0u);
         }
       };
       // X^T += ones b^T: the rank-1 bias of tile `which` (stage-major: LSE, D)
@@ -309,10 +320,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // acc += X^T Y with X^T (keys x queries, bf16) in tensor memory and Y =
       // dO_i or Q_i in shared memory as an MN-major B (d contiguous).
       auto issue_tn = [&](uint32_t acol, uint32_t b0, uint32_t dcol, bool accumulate) {
+        const uint64_t bd = base(sdesc_sw128(b0, C::kHalfBytes, 1024));
 #pragma unroll
         for (int kk = 0; kk < kBlockM / 16; ++kk)
-          mma_ts(tmem_base + dcol, tmem_base + acol + C::packed_col(kk),
-                 sdesc_sw128(b0 + kk * 2048, C::kHalfBytes, 1024), kIdescKV,
+          mma_ts(tmem_base + dcol, tmem_base + acol + C::packed_col(kk), step(bd, kk * 2048), kIdescKV,
                  (accumulate || kk > 0) ? 1u : 0u);
       };
       // dQ_i = dS K: A = dS (queries x keys) MN-major (64-query blocks 16 KB
@@ -323,10 +334,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // d index, column = query, so the drain adds whole query rows of the
       // accumulator with warp-coalesced reductions.
       auto issue_dq = [&](uint32_t ds0) {
+        const uint64_t dsd = base(sdesc_sw128(ds0, kBlockN * 128, 1024));
+        const uint64_t kd = base(sdesc_sw128(k_smem, C::kHalfBytes, 1024));
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          const uint64_t ds_desc = sdesc_sw128(ds0 + kk * 2048, kBlockN * 128, 1024);
-          const uint64_t k_desc = sdesc_sw128(k_smem + kk * 2048, C::kHalfBytes, 1024);
+          const uint64_t ds_desc = step(dsd, kk * 2048);
+          const uint64_t k_desc = step(kd, kk * 2048);
           if (C::kDqTransposed)
             mma_ss(tmem_base + C::kColDP, k_desc, ds_desc, kIdescQ, kk > 0 ? 1u : 0u);
           else
