@@ -398,11 +398,17 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       // (pair mode: each CTA's K half is 64 keys, 64 columns per 8 KB block).
       // Descriptors are built once per group and stepped by adding the byte
       // offset >> 4 to the start-address field: every address here is below
-      // 256 KB, so the 14-bit field never carries into the next one.
+      // 256 KB, so the 14-bit field never carries into the next one.  Each
+      // base goes through an empty asm so that it is rebuilt per group
+      // instead of being held in a register across the loops.
+      auto opaque = [](uint64_t desc) {
+        asm volatile("" : "+l"(desc));
+        return desc;
+      };
       auto step = [](uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); };
       auto issue_s = [&](int t, int kslot) {
-        const uint64_t a0 = sdesc_sw128(q_smem + t * C::kTileBytes, 16, 1024);
-        const uint64_t b0 = sdesc_sw128(ring + kslot * C::kSlotBytes, 16, 1024);
+        const uint64_t a0 = opaque(sdesc_sw128(q_smem + t * C::kTileBytes, 16, 1024));
+        const uint64_t b0 = opaque(sdesc_sw128(ring + kslot * C::kSlotBytes, 16, 1024));
         const uint32_t dcol = tmem_base + C::kSCol0 + t * 128;
         if constexpr (FP8) {
 #pragma unroll
@@ -431,13 +437,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         if constexpr (FP8) {
           // P_t as e4m3, four per 32-bit column: 32 keys = 8 columns per MMA;
           // V^T rows of 128 keys, 32 keys = 32 bytes per MMA.
-          const uint64_t b0 = sdesc_sw128(ring + vslot * C::kSlotBytes, 16, 1024);
+          const uint64_t b0 = opaque(sdesc_sw128(ring + vslot * C::kSlotBytes, 16, 1024));
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 32; ++kk)
             mma_ts_f8(dcol, acol + kk * 8, step(b0, kk * 32), kIdescPV,
                       (accumulate || kk > 0) ? 1u : 0u);
         } else {
-          const uint64_t b0 = sdesc_sw128(ring + vslot * C::kSlotBytes, C::kHalfBytes, 1024);
+          const uint64_t b0 = opaque(sdesc_sw128(ring + vslot * C::kSlotBytes, C::kHalfBytes, 1024));
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk) {
             if constexpr (PAIR)
