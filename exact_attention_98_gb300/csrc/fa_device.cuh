@@ -126,6 +126,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// mbar_wait for a whole converged warp: every lane waits and the result is
+// made warp-uniform, so that a warp whose lanes run the same loop (the MMA
+// issuers, whose tcgen05 instructions are issued by one elected lane) stays
+// converged even on the give-up path.
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
+                                               unsigned int site,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
+  return __all_sync(0xffffffffu, mbar_wait<kCluster>(bar, parity, ctl, site, limit_ns));
+}
+
 // Clean-up wait on the give-up path: ignores the abort flag, bounded by
 // kDrainLimitNs, records nothing.  Used to let this CTA's own TMA copies and
 // MMAs finish before it frees tensor memory and exits.
@@ -419,88 +430,103 @@ __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Every MMA and commit form below comes in two flavours.  kWarp = false: the
+// calling thread issues it.  kWarp = true: a whole converged warp executes the
+// call and elect.sync picks the one lane that issues it (the same lane every
+// time, so its commits track its own MMAs); the warp's loop, waits and
+// operand arithmetic then run as ordinary warp-uniform code.
+#define FA_MMA_ASM(kWarp, INSTR, ...)                                                  \
+  do {                                                                                 \
+    if constexpr (kWarp)                                                               \
+      asm volatile("{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\t"          \
+                   "setp.ne.b32 p, %4, 0;\n\t@e " INSTR "\n\t}" ::__VA_ARGS__          \
+                   : "memory");                                                        \
+    else                                                                               \
+      asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t" INSTR "\n\t}" ::__VA_ARGS__ \
+                   : "memory");                                                        \
+  } while (0)
+
 // D[tmem] (+)= A[smem] * B[smem]
+template <bool kWarp = false>
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  FA_MMA_ASM(kWarp, "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;", "r"(d_tmem),
+             "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]
+template <bool kWarp = false>
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  FA_MMA_ASM(kWarp, "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;", "r"(d_tmem),
+             "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Pair forms (cta_group::2, issued by rank 0): M = 256 rows, 128 from each
 // CTA's A (shared or tensor memory at the same address in both) into each
 // CTA's D; B is split along N, the first N/2 columns in rank 0's shared
 // memory and the rest in rank 1's, both at the descriptor's address.
+template <bool kWarp = false>
 __device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  FA_MMA_ASM(kWarp, "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;", "r"(d_tmem),
+             "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
+template <bool kWarp = false>
 __device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  FA_MMA_ASM(kWarp, "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;", "r"(d_tmem),
+             "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // The same two forms for 8-bit operands (kind::f8f6f4: K = 32 per MMA).
+template <bool kWarp = false>
 __device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  FA_MMA_ASM(kWarp, "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;", "r"(d_tmem),
+             "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
+template <bool kWarp = false>
 __device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  FA_MMA_ASM(kWarp, "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;", "r"(d_tmem),
+             "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
+#undef FA_MMA_ASM
 
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
+template <bool kWarp = false>
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
+  if constexpr (kWarp)
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
 }
 
 // Pair form: arrives once on the barrier at `bar` (this CTA's address) in
 // every CTA of `cta_mask` (bit r = rank r) when the pair MMAs this thread
 // issued so far have completed.
+template <bool kWarp = false>
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
+  if constexpr (kWarp)
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // ---------------------------------------------------------------------------

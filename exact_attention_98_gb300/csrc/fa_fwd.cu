@@ -11,11 +11,12 @@
 //   * exponentials partly on the FMA pipe (exp2_poly) and partly on MUFU;
 //   * conditional rescaling: O_t and the row sum are rescaled only when a row
 //     max grows by more than kRescaleThreshold (log2 units).
-// On GB300 the MUFU unit is not what limits this kernel: in steady state a
-// softmax warpgroup needs ~1250 cycles per key tile, less than the ~1600
-// cycles of products the other warpgroup keeps the tensor pipe busy with,
-// and the tensor pipe sets the pace.  Exponentials moved to the FMA pipe
-// lengthen the softmax past that budget: measured on B2 H16 N4096 d128, the
+// On GB300 the MUFU unit is not what limits this kernel.  The pace is set by
+// the MMA-issuing warp: between its groups of products it waits, commits
+// and does its own arithmetic while sharing a warp scheduler with two
+// softmax warps, and in steady state the tensor pipe runs at about 70% of
+// its rate.  Exponentials moved to the FMA pipe add softmax instructions to
+// that competition: measured on B2 H16 N4096 d128, the
 // forward ran at 1073 TFLOP/s with every exponential on MUFU and at 861 /
 // 859 / 699 TFLOP/s with 1 / 2 / 3 of every 8 on the FMA pipe, so the
 // default share is 0; the other shares stay instantiated and selectable.
@@ -31,7 +32,8 @@
 //   warps 0-3   softmax warpgroup for query tile 0 (thread = one query row)
 //   warps 4-7   softmax warpgroup for query tile 1
 //   warp  8     TMA producer
-//   warp  9     tensor-memory allocator; lane 0 issues every MMA
+//   warp  9     tensor-memory allocator and MMA issuer (the warp runs the
+//               loop and one elected lane issues each MMA; pair mode: lane 0)
 //   warps 10-11 idle
 // The CTA is launched with 168 registers per thread (12 warps, three per SM
 // sub-partition); the third warpgroup gives registers up (88) so that each
@@ -375,7 +377,17 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
     }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------- MMA issue
-    if (lane == 0 && rank == 0) {
+    // One CTA: the whole warp runs this loop and one elected lane issues each
+    // MMA and commit (the forms with kWarp = true), so the loop's own
+    // arithmetic and waits are warp-uniform code (measured 0.5-4% faster
+    // than lane 0 alone).  Pair mode: lane 0 alone (the warp-wide loop
+    // measured 7% slower there at N = 32768).
+    constexpr bool kWarpIssue = !PAIR;
+    if (rank == 0 && (kWarpIssue || lane == 0)) {
+      auto wait = [&](uint32_t b, uint32_t parity, unsigned int site) {
+        if constexpr (kWarpIssue) return mbar_wait_warp<PAIR>(b, parity, ctl, site);
+        else return mbar_wait<PAIR>(b, parity, ctl, site);
+      };
       // pair mode: M = 256 (this CTA's 128 query rows, then the other's)
       constexpr int kM = PAIR ? 2 * kBlockM : kBlockM;
       constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(kM, kBlockN, false, false)
@@ -385,8 +397,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
                                         : idesc_bf16_f32(kM, D, false, true);
       // A commit reaches both CTAs of a pair.
       auto commit = [&](int b) {
-        if constexpr (PAIR) mma_commit_pair(bar(b), 3);
-        else mma_commit(bar(b));
+        if constexpr (PAIR) mma_commit_pair<kWarpIssue>(bar(b), 3);
+        else mma_commit<kWarpIssue>(bar(b));
       };
       const uint32_t q_smem = sbase + C::kQOff;
       const uint32_t ring = sbase + C::kRingOff;
@@ -413,16 +425,16 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         if constexpr (FP8) {
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)  // 32 e4m3 = 32 bytes of the 128-byte row
-            mma_ss_f8(dcol, step(a0, kk * 32), step(b0, kk * 32), kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss_f8<kWarpIssue>(dcol, step(a0, kk * 32), step(b0, kk * 32), kIdescS, kk > 0 ? 1u : 0u);
         } else {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
             if constexpr (PAIR) {
               const uint32_t boff = (kk >> 2) * (C::kSlotBytes / 2) + (kk & 3) * 32;
-              mma_ss_pair(dcol, step(a0, off), step(b0, boff), kIdescS, kk > 0 ? 1u : 0u);
+              mma_ss_pair<kWarpIssue>(dcol, step(a0, off), step(b0, boff), kIdescS, kk > 0 ? 1u : 0u);
             } else {
-              mma_ss(dcol, step(a0, off), step(b0, off), kIdescS, kk > 0 ? 1u : 0u);
+              mma_ss<kWarpIssue>(dcol, step(a0, off), step(b0, off), kIdescS, kk > 0 ? 1u : 0u);
             }
           }
         }
@@ -440,17 +452,17 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
           const uint64_t b0 = opaque(sdesc_sw128(ring + vslot * C::kSlotBytes, 16, 1024));
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 32; ++kk)
-            mma_ts_f8(dcol, acol + kk * 8, step(b0, kk * 32), kIdescPV,
+            mma_ts_f8<kWarpIssue>(dcol, acol + kk * 8, step(b0, kk * 32), kIdescPV,
                       (accumulate || kk > 0) ? 1u : 0u);
         } else {
           const uint64_t b0 = opaque(sdesc_sw128(ring + vslot * C::kSlotBytes, C::kHalfBytes, 1024));
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk) {
             if constexpr (PAIR)
-              mma_ts_pair(dcol, acol + kk * 8, step(b0, kk * 2048), kIdescPV,
+              mma_ts_pair<kWarpIssue>(dcol, acol + kk * 8, step(b0, kk * 2048), kIdescPV,
                           (accumulate || kk > 0) ? 1u : 0u);
             else
-              mma_ts(dcol, acol + kk * 8, step(b0, kk * 2048), kIdescPV,
+              mma_ts<kWarpIssue>(dcol, acol + kk * 8, step(b0, kk * 2048), kIdescPV,
                      (accumulate || kk > 0) ? 1u : 0u);
           }
         }
@@ -470,8 +482,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         if (wi >= p.n_items) break;
         const FwdItem item = item_of(wi);
         if (item.nmax == 0) continue;
-        ok = mbar_wait<PAIR>(bar(C::kBarQFull), (q_items++) & 1, ctl, kSiteQFull);
-        if (ok) ok = mbar_wait<PAIR>(bar(C::kBarFull + slot_of(base)), parity_of(base), ctl, kSiteKFull);
+        ok = wait(bar(C::kBarQFull), (q_items++) & 1, kSiteQFull);
+        if (ok) ok = wait(bar(C::kBarFull + slot_of(base)), parity_of(base), kSiteKFull);
         if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
@@ -483,7 +495,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         commit(C::kBarEmpty + slot_of(base));
         for (int j = 0; ok && j < item.nmax; ++j) {
           const int vidx = base + 2 * j + 1, kidx = base + 2 * j + 2;
-          ok = mbar_wait<PAIR>(bar(C::kBarFull + slot_of(vidx)), parity_of(vidx), ctl, kSiteVFull);
+          ok = wait(bar(C::kBarFull + slot_of(vidx)), parity_of(vidx), kSiteVFull);
           if (!ok) break;
           tc_fence_after();
           bool k_next_ready = false;
@@ -491,7 +503,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
           for (int t = 0; t < 2; ++t) {
             if (!ok) break;
             if (j >= item.nkv(t)) continue;
-            ok = mbar_wait<PAIR>(bar(C::kBarPFull + t), (t ? np1 : np0) & 1, ctl, kSitePFull);
+            ok = wait(bar(C::kBarPFull + t), (t ? np1 : np0) & 1, kSitePFull);
             if (!ok) break;
             if (t) ++np1; else ++np0;
             tc_fence_after();
@@ -500,7 +512,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
               commit(C::kBarOFull + t);
             } else {
               if (!k_next_ready) {
-                ok = mbar_wait<PAIR>(bar(C::kBarFull + slot_of(kidx)), parity_of(kidx), ctl, kSiteKFull);
+                ok = wait(bar(C::kBarFull + slot_of(kidx)), parity_of(kidx), kSiteKFull);
                 if (!ok) break;
                 tc_fence_after();
                 k_next_ready = true;
@@ -517,8 +529,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         base += 2 * item.nmax;
       }
       // Every MMA this thread issued must finish before tensor memory is freed.
-      if constexpr (PAIR) mma_commit_pair(bar(C::kBarMmaDone), 1);
-      else mma_commit(bar(C::kBarMmaDone));
+      if constexpr (PAIR) mma_commit_pair<kWarpIssue>(bar(C::kBarMmaDone), 1);
+      else mma_commit<kWarpIssue>(bar(C::kBarMmaDone));
       mbar_wait_drain(bar(C::kBarMmaDone), 0);
     }
    }
