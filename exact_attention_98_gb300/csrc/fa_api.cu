@@ -221,7 +221,10 @@ __global__ void exp2_poly_eval_kernel(const float* x, float* y, long long n) {
     y[i] = exp2_poly(x[i]);
 }
 
-// One mbarrier that nothing arrives on; the bounded wait must give up.
+// One mbarrier that nothing arrives on; the bounded wait must give up.  One
+// warp waits in the warp-uniform form the forward's MMA-issuing warp uses
+// (every lane waits, the result is voted), so its give-up path is the one
+// exercised.
 __global__ void bounded_wait_kernel(unsigned int* status, unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t mbar;
   __shared__ int abort_flag;
@@ -232,7 +235,7 @@ __global__ void bounded_wait_kernel(unsigned int* status, unsigned long long lim
   }
   __syncthreads();
   const WaitCtl ctl{&abort_flag, status};
-  mbar_wait(smem_u32(&mbar), 0, ctl, 0x0F0, limit_ns);
+  mbar_wait_warp(smem_u32(&mbar), 0, ctl, 0x0F0, limit_ns);
   __syncthreads();
 }
 
