@@ -4,7 +4,7 @@
 // What the pages ask of the forward (FlashAttention-4 abstract, items 1-3;
 // "Les capacités de Blackwell qui l'ont rendu possible" of the French page):
 //   * pipelines where the tensor cores, the exponential units and memory
-//     overlap -> one load warp, one MMA-issuing thread, two softmax
+//     overlap -> one load warp, one MMA-issuing warp, two softmax
 //     warpgroups working on two query tiles in ping-pong;
 //   * accumulators and intermediates in tensor memory -> S_t, O_t and P_t
 //     (P written in place of S) for both query tiles: 2 x (128 + d) columns;
