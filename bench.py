@@ -3,10 +3,14 @@ over one batch of synthetic bf16 inputs, through the C ABI.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
-Default workload: B=2, H=16, N=4096, d=128, bf16, non-causal, scale 1/sqrt(d)
-(the B2 H16 N4096 d128 configuration; the causal variant is reported as an
-extra).  Algorithmic FLOPs: forward 4*B*H*N^2*d (halved when causal),
-backward 2.5x that.
+Default workload: B=1, H=16, N=32768, d=128, bf16, non-causal, scale
+1/sqrt(d): the largest configuration of the fixed-token sweep (B*N = 32768)
+and the long-context shape.  Reported beside it, each with its own kernel
+rates: the causal variant of the same shape (its forward is the B1 H16 N32768
+causal long-context forward), the B2 H16 N8192 causal backward, and the
+B2 H16 N4096 step with the other entry points (deterministic backward, FP8
+and CTA-pair forwards).  Algorithmic FLOPs: forward 4*B*H*N^2*d (halved when
+causal), backward 2.5x that.
 
 Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its
 own replica on its own GPU (independent batches, no collective on the data
@@ -24,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -31,7 +36,10 @@ sys.path.insert(0, ROOT)
 
 PAGES_PEAK_TFLOPS = 2250.0  # dense BF16 peak the pages quote for the GPU generation
 METRIC = "attention fwd/bwd TFLOPs/s (bf16, d=128) and % of 2.25 PF dense BF16 peak"
-WORKLOAD = dict(B=2, H=16, N=4096, d=128)
+WORKLOAD = dict(B=1, H=16, N=32768, d=128)
+WORKLOAD_NAME = "attention fwd+bwd B1 H16 N32768 d128 non-causal"
+BWD_CAUSAL = dict(B=2, H=16, N=8192, d=128)  # the B2 H16 N8192 causal backward
+SMALL = dict(B=2, H=16, N=4096, d=128)  # the B2 H16 N4096 step and the other entry points
 
 
 def flops(B, H, N, d, causal):
@@ -62,8 +70,9 @@ def parse():
 # soon as any of them changes.
 NCU_TRAFFIC = {
     "kernel": "fa_bwd_kernel<128>",
-    "bytes": 202454272 + 85904640,
-    "sources_sha256": "760b9151c41f631ff6f5c2fdbbf86ff53efd27e02a05e736abb1aeac3a9c8014",
+    "workload": WORKLOAD_NAME,
+    "bytes": None,
+    "sources_sha256": "",
 }
 KERNEL_SOURCES = ("fa_bwd.cu", "fa_device.cuh", "fa_kernels.h", "exp2_poly_coeffs.h")
 
@@ -181,7 +190,7 @@ def oracle_sample(seconds_target: float, steps: int = 1, warmup: int = 0):
     f = 10.0 * R * N * d
     tf = f / statistics.median(times) / 1e12
     desc = (f"forward + dQ rows of the backward for {R} of {N} query rows of one head "
-            f"(B2 H16 N{N} d{d} non-causal workload), fp64, {oracle.num_threads()} threads")
+            f"({WORKLOAD_NAME} workload), fp64, {oracle.num_threads()} threads")
     return tf, oracle.num_threads(), desc, times, f
 
 
@@ -198,8 +207,7 @@ def reference_arm(args):
         "impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "attention fwd+bwd B2 H16 N4096 d128 non-causal bf16 inputs",
-                   "sample": desc},
+        "config": {"workload": WORKLOAD_NAME + " (bf16 inputs)", "sample": desc},
         "cpu_baseline": oracle_fields(tf, threads, desc),
         "e2e": {"value": tf, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -228,7 +236,8 @@ class ClockSampler:
             self.ids.insert(0, uuid if uuid.startswith("GPU-") else f"GPU-{uuid}")
         self.gpu = None
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        fd, self.path = tempfile.mkstemp(prefix=f"fa_clocks_{gpu_index}_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         return self.start()
@@ -237,7 +246,6 @@ class ClockSampler:
         self.stop()
 
     def start(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
         for gpu in self.ids:  # the UUID first; the index if nvidia-smi refuses it
             try:
                 self.fh = open(self.path, "w")
@@ -282,8 +290,53 @@ class ClockSampler:
             for name, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm), "gpu": self.gpu}
+
+
+def kernel_rates(fa, shape, causal, flush, stream, reps=5, warmup=2, fwd=True, bwd=True):
+    """Median forward-kernel and backward-main-kernel times (the library's
+    CUDA events on the launch stream, L2 flushed before every step) of one
+    shape; the step each rep runs is fa_fwd (with its workspace) then fa_bwd.
+    Returns dict of ms and TFLOP/s."""
+    import torch
+
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    B, H, N, d = shape["B"], shape["H"], shape["N"], shape["d"]
+    dev = flush.device
+    scale = 1.0 / math.sqrt(d)
+    q, k, v, do = (t.to(dev) for t in attention_inputs(B, H, N, d, seed=1))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = fa.workspace_for(q)
+    wsf = fa.fwd_workspace_for(q, causal)
+    f_fwd, f_bwd = flops(B, H, N, d, causal)
+    fwd_ms, bwd_ms = [], []
+    for i in range(warmup + reps):
+        flush.zero_()
+        fa.fa_timing_enable(i >= warmup)
+        fa.fa_fwd(q, k, v, o, lse, scale, causal, wsf)
+        fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, ws)
+        if i >= warmup:
+            fwd_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
+            bwd_ms.append(fa.fa_timing_last_ms(fa.KERNEL_BWD_MAIN))
+    fa.fa_timing_enable(False)
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status")
+    fm, bm = statistics.median(fwd_ms), statistics.median(bwd_ms)
+    out = {"workload": f"B{B} H{H} N{N} d{d} {'causal' if causal else 'non-causal'}"}
+    if fwd:
+        out.update(fwd_ms=fm, fwd_tflops=f_fwd / fm / 1e9)
+    if bwd:
+        out.update(bwd_main_ms=bm, bwd_main_tflops=f_bwd / bm / 1e9)
+    del q, k, v, do, o, lse, dq, dk, dv, ws, wsf
+    return out
 
 
 def native_arm(args):
@@ -316,11 +369,12 @@ def native_arm(args):
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
     ws = fa.workspace_for(qd)
+    wsf = {c: fa.fwd_workspace_for(qd, c) for c in (False, True)}
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 129 MB L2
     stream = torch.cuda.current_stream()
 
     def step(causal):
-        fa.fa_fwd(qd, kd, vd, o, lse, scale, causal)
+        fa.fa_fwd(qd, kd, vd, o, lse, scale, causal, wsf[causal])
         fa.fa_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, scale, causal, ws)
 
     def timed(causal, steps, warmup, kernel_times=False):
@@ -354,8 +408,7 @@ def native_arm(args):
         return step_ms, fwd_ms, bwd_ms, wall, launches
 
     # headline: non-causal, with per-kernel events.  Clocks are sampled from
-    # here to the end of the last GPU leg (the headline's own timed region is
-    # tens of milliseconds, shorter than the sampling interval).
+    # here to the end of the last GPU leg.
     clocks = ClockSampler(local).start()
     step_ms, fwd_ms, bwd_ms, wall, launches = timed(False, args.steps, args.warmup,
                                                      kernel_times=True)
@@ -366,73 +419,18 @@ def native_arm(args):
     fwd_tf = f_fwd / (fwd_med * 1e-3) / 1e12
     bwd_main_tf = f_bwd / (bwd_med * 1e-3) / 1e12
 
-    # causal variant (extra)
+    # causal variant of the same shape: its forward is the B1 H16 N32768
+    # causal long-context forward
     c_ms, c_fwd, c_bwd, _, _ = timed(True, max(3, args.steps // 2), 2, kernel_times=True)
     cf_fwd, cf_bwd = flops(B, H, N, d, True)
     causal_extra = {
+        "workload": "attention fwd+bwd B1 H16 N32768 d128 causal",
         "step_tflops": (cf_fwd + cf_bwd) / (statistics.mean(c_ms) * 1e-3) / 1e12,
         "fwd_tflops": cf_fwd / (statistics.median(c_fwd) * 1e-3) / 1e12,
+        "fwd_ms": statistics.median(c_fwd),
         "bwd_main_tflops": cf_bwd / (statistics.median(c_bwd) * 1e-3) / 1e12,
+        "bwd_main_ms": statistics.median(c_bwd),
     }
-
-    # The deterministic backward (all three of its kernels), same workload,
-    # L2 flushed before each launch; reported beside the headline.
-    ws_det = fa.workspace_for(qd, deterministic=True)
-    det_ms = []
-    for i in range(3 + 5):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        fa.fa_bwd_deterministic(qd, kd, vd, o, lse, dod, dq, dk, dv, scale, False, ws_det)
-        e1.record(stream)
-        e1.synchronize()
-        if i >= 3:
-            det_ms.append(e0.elapsed_time(e1))
-    if fa.fa_last_device_status() != fa.FA_OK:
-        raise RuntimeError("device status after the deterministic backward")
-    del ws_det
-    det_ms_med = statistics.median(det_ms)
-    deterministic_extra = {"bwd_tflops": f_bwd / (det_ms_med * 1e-3) / 1e12, "bwd_ms": det_ms_med,
-                           "note": "fa_bwd_deterministic, all kernels"}
-
-    # The FP8 forward (rotation + e4m3 preparation, then the kernel), same
-    # workload; the kernel alone from the library's events.
-    ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
-    o8, lse8 = torch.empty_like(qd), torch.empty_like(lse)
-    call_ms, kern_ms = [], []
-    fa.fa_timing_enable(True)
-    for i in range(3 + 5):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        fa.fa_fwd_fp8(qd, kd, vd, o8, lse8, scale, False, True, ws8)
-        e1.record(stream)
-        e1.synchronize()
-        if i >= 3:
-            call_ms.append(e0.elapsed_time(e1))
-            kern_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
-    fa.fa_timing_enable(False)
-    if fa.fa_last_device_status() != fa.FA_OK:
-        raise RuntimeError("device status after the FP8 forward")
-    del ws8
-    fp8_extra = {"call_tflops": f_fwd / (statistics.median(call_ms) * 1e-3) / 1e12,
-                 "kernel_tflops": f_fwd / (statistics.median(kern_ms) * 1e-3) / 1e12,
-                 "note": "fa_fwd_fp8 (rotate=1, e4m3): call = preparation + kernel"}
-
-    # The CTA-pair forward (fa_fwd_2cta), same workload, kernel events.
-    pair_ms = []
-    fa.fa_timing_enable(True)
-    for i in range(3 + 5):
-        flush.zero_()
-        fa.fa_fwd_2cta(qd, kd, vd, o8, lse8, scale, False)
-        if i >= 3:
-            pair_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
-    fa.fa_timing_enable(False)
-    if fa.fa_last_device_status() != fa.FA_OK:
-        raise RuntimeError("device status after the CTA-pair forward")
-    del o8, lse8
-    two_cta_extra = {"kernel_tflops": f_fwd / (statistics.median(pair_ms) * 1e-3) / 1e12,
-                     "note": "fa_fwd_2cta: CTA pairs sharing M = 256 products"}
 
     # End to end through the public calls: every step copies its own inputs
     # Q, K, V, dO from pinned host memory and its gradients dQ, dK, dV back.
@@ -502,7 +500,7 @@ def native_arm(args):
         if sl["used"]:
             for ev in sl["out_free"]:
                 stream.wait_event(ev)
-        fa.fa_fwd(sl["q"], sl["k"], sl["v"], o, lse, scale, False)
+        fa.fa_fwd(sl["q"], sl["k"], sl["v"], o, lse, scale, False, wsf[False])
         fa.fa_bwd(sl["q"], sl["k"], sl["v"], o, lse, sl["do"], sl["dq"], sl["dk"], sl["dv"], scale,
                   False, ws)
         sl["in_free"].record(stream)
@@ -528,9 +526,85 @@ def native_arm(args):
     e2e_ms = timed_e2e(pipelined_step, pipelined_prepare, pipelined_finish)
     e2e_value = job_tflops(f_fwd + f_bwd, world, e2e_ms)
     e2e_serial_value = job_tflops(f_fwd + f_bwd, world, e2e_serial_ms)
+    tensor_bytes = q.numel() * q.element_size()
+    del slots, hq, hk, hv, hdo, hdq, hdk, hdv, qd, kd, vd, dod, o, lse, dq, dk, dv, ws, wsf
+    torch.cuda.empty_cache()
+
+    # The B2 H16 N8192 causal backward, kernel events.
+    bwd_causal = kernel_rates(fa, BWD_CAUSAL, True, flush, stream, fwd=False)
+    # The B2 H16 N4096 step (non-causal) and the other entry points on it.
+    small = kernel_rates(fa, SMALL, False, flush, stream)
+    sB, sH, sN, sd = SMALL["B"], SMALL["H"], SMALL["N"], SMALL["d"]
+    s_fwd, s_bwd = flops(sB, sH, sN, sd, False)
+    sq, sk, sv, sdo = (t.to(dev) for t in attention_inputs(sB, sH, sN, sd, seed=2))
+    so, slse = torch.empty_like(sq), torch.empty((sB, sH, sN), dtype=torch.float32, device=dev)
+    sdq, sdk, sdv = torch.empty_like(sq), torch.empty_like(sq), torch.empty_like(sq)
+    fa.fa_fwd(sq, sk, sv, so, slse, 1.0 / math.sqrt(sd), False, fa.fwd_workspace_for(sq, False))
+
+    # The deterministic backward (all three of its kernels), L2 flushed
+    # before each launch.
+    ws_det = fa.workspace_for(sq, deterministic=True)
+    det_ms = []
+    for i in range(3 + 5):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fa.fa_bwd_deterministic(sq, sk, sv, so, slse, sdo, sdq, sdk, sdv, 1.0 / math.sqrt(sd),
+                                False, ws_det)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            det_ms.append(e0.elapsed_time(e1))
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after the deterministic backward")
+    del ws_det
+    det_ms_med = statistics.median(det_ms)
+    deterministic_extra = {"bwd_tflops": s_bwd / (det_ms_med * 1e-3) / 1e12, "bwd_ms": det_ms_med,
+                           "workload": "B2 H16 N4096 d128 non-causal",
+                           "note": "fa_bwd_deterministic, all kernels"}
+
+    # The FP8 forward (rotation + e4m3 preparation, then the kernel); the
+    # kernel alone from the library's events.
+    ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(sB, sH, sN, sd), dtype=torch.uint8, device=dev)
+    o8, lse8 = torch.empty_like(sq), torch.empty_like(slse)
+    call_ms, kern_ms = [], []
+    fa.fa_timing_enable(True)
+    for i in range(3 + 5):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fa.fa_fwd_fp8(sq, sk, sv, o8, lse8, 1.0 / math.sqrt(sd), False, True, ws8)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            call_ms.append(e0.elapsed_time(e1))
+            kern_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
+    fa.fa_timing_enable(False)
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after the FP8 forward")
+    del ws8
+    fp8_extra = {"call_tflops": s_fwd / (statistics.median(call_ms) * 1e-3) / 1e12,
+                 "kernel_tflops": s_fwd / (statistics.median(kern_ms) * 1e-3) / 1e12,
+                 "workload": "B2 H16 N4096 d128 non-causal",
+                 "note": "fa_fwd_fp8 (rotate=1, e4m3): call = preparation + kernel"}
+
+    # The CTA-pair forward (fa_fwd_2cta), kernel events.
+    pair_ms = []
+    fa.fa_timing_enable(True)
+    for i in range(3 + 5):
+        flush.zero_()
+        fa.fa_fwd_2cta(sq, sk, sv, o8, lse8, 1.0 / math.sqrt(sd), False)
+        if i >= 3:
+            pair_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
+    fa.fa_timing_enable(False)
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after the CTA-pair forward")
+    two_cta_extra = {"kernel_tflops": s_fwd / (statistics.median(pair_ms) * 1e-3) / 1e12,
+                     "workload": "B2 H16 N4096 d128 non-causal",
+                     "note": "fa_fwd_2cta: CTA pairs sharing M = 256 products"}
+    del sq, sk, sv, sdo, so, slse, sdq, sdk, sdv, o8, lse8
     clocks.stop()
     clk = clocks.summary()
-    tensor_bytes = q.numel() * q.element_size()
 
     peaks = {}
     try:
@@ -542,6 +616,12 @@ def native_arm(args):
     if peak is None:
         peak, peak_note = 1900.0, "fallback 1.9 PFLOP/s bf16"
 
+    def roofline(kernel, achieved, **extra):
+        return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_note, **extra}
+
+    traffic_ok = (NCU_TRAFFIC["bytes"] is not None and
+                  kernel_sources_sha256() == NCU_TRAFFIC["sources_sha256"])
     line = {
         "metric": METRIC,
         "value": value,
@@ -558,33 +638,34 @@ def native_arm(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "attention fwd+bwd B2 H16 N4096 d128 non-causal", "B": B, "H": H,
-                   "N": N, "d": d, "causal": False, "global_batch": B * world, "seq_len": N,
+        "config": {"workload": WORKLOAD_NAME, "B": B, "H": H, "N": N, "d": d, "causal": False,
+                   "global_batch": B * world, "seq_len": N,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between steps (256 MiB write outside the step events)"},
+                   "l2": "flushed between steps (256 MiB write outside the step events); "
+                         "each input tensor (134 MB) is also larger than L2"},
         "pct_of_2250_tflops": 100.0 * value / PAGES_PEAK_TFLOPS,
         "fwd_tflops": fwd_tf,
         "bwd_main_tflops": bwd_main_tf,
         "fwd_ms": fwd_med,
         "bwd_main_ms": bwd_med,
+        "fwd_pct_of_2250_tflops": 100.0 * fwd_tf / PAGES_PEAK_TFLOPS,
+        "bwd_main_pct_of_2250_tflops": 100.0 * bwd_main_tf / PAGES_PEAK_TFLOPS,
         "causal": causal_extra,
+        "bwd_b2h16n8192_causal": {
+            **bwd_causal,
+            "pct_of_2250_tflops": 100.0 * bwd_causal["bwd_main_tflops"] / PAGES_PEAK_TFLOPS,
+            "roofline": roofline("fa_bwd_kernel<128>", bwd_causal["bwd_main_tflops"])},
+        "b2h16n4096": {**small, "roofline_bwd": roofline("fa_bwd_kernel<128>",
+                                                         small["bwd_main_tflops"])},
         "deterministic": deterministic_extra,
         "fp8_forward": fp8_extra,
         "two_cta_forward": two_cta_extra,
-        "roofline": {
-            "kernel": "fa_bwd_kernel<128>",
-            "bound": "tensor",
-            "achieved": bwd_main_tf,
-            "peak": peak,
-            "unit": "TFLOP/s",
-            "frac": bwd_main_tf / peak,
-            "peak_source": peak_note,
-            "traffic": (NCU_TRAFFIC["bytes"]
-                        if kernel_sources_sha256() == NCU_TRAFFIC["sources_sha256"] else None),
-            "traffic_unit": "bytes per launch (ncu, cold cache)",
-        },
-        "roofline_fwd": {"kernel": "fa_fwd_kernel<128>", "bound": "tensor", "achieved": fwd_tf,
-                         "peak": peak, "unit": "TFLOP/s", "frac": fwd_tf / peak},
+        "roofline": roofline(
+            "fa_bwd_kernel<128>", bwd_main_tf,
+            traffic=NCU_TRAFFIC["bytes"] if traffic_ok else None,
+            traffic_unit="bytes per launch (ncu, cold cache)"),
+        "roofline_fwd": roofline("fa_fwd_kernel<128>", fwd_tf),
+        "roofline_fwd_causal": roofline("fa_fwd_kernel<128>", causal_extra["fwd_tflops"]),
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": 4 * tensor_bytes, "d2h_bytes_per_step": 3 * tensor_bytes,
@@ -626,13 +707,14 @@ def sweep_arm(args):
             lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
             dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
             ws = fa.workspace_for(q)
+            wsf = {c: fa.fwd_workspace_for(q, c) for c in (False, True)}
             for causal in (False, True):
                 f_fwd, f_bwd = flops(B, H, N, d, causal)
                 fwd_ms, bwd_ms = [], []
                 for i in range(warmup + steps):
                     flush.zero_()
                     fa.fa_timing_enable(i >= warmup)
-                    fa.fa_fwd(q, k, v, o, lse, scale, causal)
+                    fa.fa_fwd(q, k, v, o, lse, scale, causal, wsf[causal])
                     fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, ws)
                     if i >= warmup:
                         fwd_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
@@ -647,7 +729,7 @@ def sweep_arm(args):
                                   "bwd_main_ms": bm, "bwd_main_tflops": f_bwd / bm / 1e9,
                                   "bwd_pct_of_2250": 100 * f_bwd / bm / 1e9 / PAGES_PEAK_TFLOPS}),
                       flush=True)
-            del q, k, v, do, o, lse, dq, dk, dv, ws
+            del q, k, v, do, o, lse, dq, dk, dv, ws, wsf
 
 
 def main():

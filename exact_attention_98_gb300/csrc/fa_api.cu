@@ -124,14 +124,15 @@ bool encode_u8_map(CUtensorMap* map, const void* base, long long cols, long long
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Share of the forward's exponentials on the FMA pipe, per 8 (env override).
-int poly_per_octet() {
-  static std::once_flag once;
-  static int value = kDefaultPolyPerOctet;
-  std::call_once(once, [] {
+// Share of the forward's exponentials on the FMA pipe, per 8: the initial
+// value from FA_FWD_POLY_PER_OCTET (default kDefaultPolyPerOctet), then
+// whatever fa_set_exp2_poly_share() sets.
+std::atomic<int>& poly_share() {
+  static std::atomic<int> value{[] {
     const char* e = getenv("FA_FWD_POLY_PER_OCTET");
-    if (e && e[0] >= '0' && e[0] <= '3' && e[1] == '\0') value = e[0] - '0';
-  });
+    if (e && e[0] >= '0' && e[0] <= '3' && e[1] == '\0') return e[0] - '0';
+    return kDefaultPolyPerOctet;
+  }()};
   return value;
 }
 
@@ -188,30 +189,6 @@ int sm_count() {
   return counts[dev];
 }
 
-// A private stream-ordered memory pool per device for the forward's split
-// scratch: it keeps what it has reserved (release threshold at the maximum),
-// so that after the first call an allocation costs no driver mapping, and it
-// leaves the process's default pool untouched.
-cudaMemPool_t scratch_pool() {
-  static std::mutex mu;
-  static cudaMemPool_t pools[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!pools[dev]) {
-    cudaMemPoolProps props = {};
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    cudaMemPool_t pool = nullptr;
-    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
-    uint64_t keep = ~0ull;
-    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    pools[dev] = pool;
-  }
-  return pools[dev];
-}
-
 constexpr size_t kWsAlign = 256;
 size_t round_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 
@@ -237,28 +214,6 @@ __global__ void bounded_wait_kernel(unsigned int* status, unsigned long long lim
   const WaitCtl ctl{&abort_flag, status};
   mbar_wait_warp(smem_u32(&mbar), 0, ctl, 0x0F0, limit_ns);
   __syncthreads();
-}
-
-// Scratch of fa_bwd_noalloc: the backward's D and dQ accumulator for callers
-// that cannot allocate.  Fixed size, one per device, shared by every call.
-static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
-
-// Device address of g_noalloc_scratch for the current device.  Host code may
-// not pass the array's name to a kernel (on the host it names a host-side
-// stand-in), so the address is looked up once per device, with that device
-// current, and cached.
-void* noalloc_scratch_ptr() {
-  static std::mutex mu;
-  static void* ptrs[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    ptrs[dev] = p;
-  }
-  return ptrs[dev];
 }
 
 }  // namespace
@@ -287,23 +242,65 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
              int d, float scale, int causal, int num_splits, void* workspace,
              size_t workspace_bytes, void* stream, int fp8 = 0, int rotate = 0, int pair = 0);
 
-}  // namespace
-
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-           int d, float scale, int causal, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, 0, stream);
-}
-
-int fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                int N, int d, float scale, int causal, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, 0, stream, 0, 0, 1);
-}
-
 // Partial buffers of `slots` split items of 256 rows: O (fp32, d columns),
 // then LSE.
 size_t split_scratch_bytes(size_t slots, int d) {
   return round_up(slots * 2 * kBlockM * d * sizeof(float)) +
          round_up(slots * 2 * kBlockM * sizeof(float));
+}
+
+// The forward's last-round split.  Non-causal items all cost the same, so
+// when they do not fill whole rounds of the persistent grid (one CTA per SM)
+// the last partial round's `tail` blocks are cut into `ns` key ranges, as
+// many as fill that round, each of at least 8 key tiles.  False when no
+// split applies.
+bool tail_split(long long blocks, int n_ktiles, int causal, int sms, int* tail, int* ns) {
+  if (causal || sms <= 0 || blocks <= sms) return false;
+  const int t = static_cast<int>(blocks % sms);
+  if (t == 0) return false;
+  const int n = sms / t;
+  if (n < 2 || n_ktiles < 8 * n) return false;
+  *tail = t;
+  *ns = n;
+  return true;
+}
+
+// Scratch of the last-round split of a (B, H, N, d) forward on the current
+// device; 0 when none applies.
+size_t tail_split_bytes(int B, int H, int N, int d, int causal) {
+  const long long blocks = static_cast<long long>(B) * H * ((N + 2 * kBlockM - 1) / (2 * kBlockM));
+  int tail = 0, ns = 0;
+  if (!tail_split(blocks, (N + kBlockN - 1) / kBlockN, causal, sm_count(), &tail, &ns)) return 0;
+  return split_scratch_bytes(static_cast<size_t>(tail) * ns, d);
+}
+
+// Bytes of the FP8 operands and scales at the head of the FP8 workspace.
+size_t fp8_buffer_bytes(int B, int H, int N) {
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t rows = BH * N;
+  const size_t Np = (static_cast<size_t>(N) + 15) / 16 * 16;
+  return 2 * round_up(rows * 128) + round_up(BH * 128 * Np) + round_up(rows * sizeof(float)) +
+         round_up(2 * BH * sizeof(unsigned int)) +
+         round_up(fp8_amax_part_count(static_cast<int>(BH), N) * sizeof(float));
+}
+
+}  // namespace
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, 1, workspace, workspace_bytes,
+                  stream);
+}
+
+size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal) {
+  bool empty = false;
+  if (check_shape(B, H, N, d, 1.0f, &empty) != FA_OK || empty) return 0;
+  return tail_split_bytes(B, H, N, d, causal);
+}
+
+int fa_fwd_2cta(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int N, int d, float scale, int causal, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, 1, nullptr, 0, stream, 0, 0, 1);
 }
 
 size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
@@ -317,12 +314,7 @@ size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits
 size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d) {
   bool empty = false;
   if (check_shape(B, H, N, d, 1.0f, &empty) != FA_OK || empty || d != 128) return 0;
-  const size_t BH = static_cast<size_t>(B) * H;
-  const size_t rows = BH * N;
-  const size_t Np = (static_cast<size_t>(N) + 15) / 16 * 16;
-  return 2 * round_up(rows * 128) + round_up(BH * 128 * Np) + round_up(rows * sizeof(float)) +
-         round_up(2 * BH * sizeof(unsigned int)) +
-         round_up(fp8_amax_part_count(static_cast<int>(BH), N) * sizeof(float));
+  return fp8_buffer_bytes(B, H, N) + tail_split_bytes(B, H, N, d, 0);
 }
 
 int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -340,8 +332,20 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                   workspace_bytes, stream);
 }
 
+int fa_set_exp2_poly_share(int per_octet) {
+  if (per_octet < 0 || per_octet > 3) return FA_ERR_INVALID_ARG;
+  poly_share().store(per_octet, std::memory_order_relaxed);
+  return FA_OK;
+}
+
+int fa_get_exp2_poly_share(void) { return poly_share().load(std::memory_order_relaxed); }
+
 namespace {
 
+// num_splits > 1: every block cut into that many key ranges (fa_fwd_splitkv,
+// workspace required).  fp8: the workspace holds the e4m3 operands first.
+// Otherwise the workspace is optional and, when given, takes the last-round
+// split's partials (after the FP8 buffers in FP8 mode).
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
              int d, float scale, int causal, int num_splits, void* workspace,
              size_t workspace_bytes, void* stream, int fp8, int rotate, int pair) {
@@ -359,9 +363,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   // head) in int
   if (fp8 && static_cast<long long>(B) * H * (3LL * ((N + 127) / 128) + 1) > 0x7fffffffLL)
     return FA_ERR_UNSUPPORTED;
-  if (num_splits > 1 || fp8) {
+  if (num_splits > 1 || fp8 || workspace != nullptr) {
     const size_t need = fp8 ? fa_fwd_fp8_workspace_bytes(B, H, N, d)
-                            : fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits);
+                        : num_splits > 1 ? fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits)
+                                         : fa_fwd_workspace_bytes(B, H, N, d, causal);
     if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & (kWsAlign - 1)) != 0) return FA_ERR_WORKSPACE;
   }
@@ -373,6 +378,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.fp8 = fp8;
   p.q_descale = nullptr;
   p.fp8_amax = nullptr;
+  // the part of the workspace the last-round split may use
+  char* split_ws = static_cast<char*>(workspace);
   if (fp8) {
     Fp8Buffers fb;
     char* w = static_cast<char*>(workspace);
@@ -388,6 +395,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     fb.amax = reinterpret_cast<unsigned int*>(w);
     w += round_up(2 * static_cast<size_t>(BH) * sizeof(unsigned int));
     fb.amax_part = reinterpret_cast<float*>(w);
+    split_ws = static_cast<char*>(workspace) + fp8_buffer_bytes(B, H, N);
     if (!encode_u8_map(&p.tm_q, fb.q8, 128, N, BH, 128) ||
         !encode_u8_map(&p.tm_k, fb.k8, 128, N, BH, 128) ||
         !encode_u8_map(&p.tm_v, fb.v8t, fb.Np, 128, BH, fb.Np))
@@ -418,54 +426,34 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.causal = causal;
   p.c = scale * 1.4426950408889634f;
   p.ln2 = 0.6931471805599453f;
-  p.poly_per_octet = poly_per_octet();
+  p.poly_per_octet = poly_share().load(std::memory_order_relaxed);
   if (static_cast<long long>(p.n_qblk) * BH * num_splits > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   const int blocks = p.n_qblk * BH;
-  // Which blocks are split: all of them (num_splits > 1, the caller's
-  // workspace), else the last partial round of the persistent grid
-  // (non-causal: its blocks all cost the same), into as many key ranges as
-  // fill the round, with scratch from the stream-ordered allocator.
-  void* scratch = nullptr;
+  // Which blocks are split: all of them (num_splits > 1), else, when the
+  // caller gave a workspace, the last partial round of the persistent grid
+  // (see tail_split); the partials go to the workspace.
   p.split_from = blocks;
   p.num_splits = 1;
   p.o_part = p.lse_part = nullptr;
+  int tail = 0, ns = 0;
   if (num_splits > 1) {
     p.split_from = 0;
     p.num_splits = num_splits;
-    scratch = workspace;
-  } else if (!causal && !pair) {
-    const int sms = sm_count();
-    const int tail = sms > 0 ? blocks % sms : 0;
-    const int ns = tail > 0 ? sms / tail : 0;
-    if (blocks > sms && ns >= 2 && n_ktiles >= 8 * ns) {  // ranges of at least 8 key tiles
-      void* mem = nullptr;
-      cudaMemPool_t pool = scratch_pool();
-      if (pool != nullptr &&
-          cudaMallocFromPoolAsync(&mem, split_scratch_bytes(static_cast<size_t>(tail) * ns, d), pool,
-                                  s) == cudaSuccess) {
-        p.split_from = blocks - tail;
-        p.num_splits = ns;
-        scratch = mem;
-      } else {
-        (void)cudaGetLastError();  // run unsplit
-      }
-    }
+  } else if (workspace != nullptr && !pair &&
+             tail_split(blocks, n_ktiles, causal, sm_count(), &tail, &ns)) {
+    p.split_from = blocks - tail;
+    p.num_splits = ns;
   }
   if (p.split_from < blocks) {
     const size_t slots = static_cast<size_t>(blocks - p.split_from) * p.num_splits;
-    p.o_part = static_cast<float*>(scratch);
-    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(scratch) +
-                                          round_up(slots * 2 * kBlockM * d * sizeof(float)));
+    p.o_part = reinterpret_cast<float*>(split_ws);
+    p.lse_part = reinterpret_cast<float*>(split_ws + round_up(slots * 2 * kBlockM * d * sizeof(float)));
   }
   p.n_items = p.split_from + (blocks - p.split_from) * p.num_splits;
   cudaError_t err = timing_record(0, true, s);
   if (err == cudaSuccess) err = launch_fwd(p, d, s);
   if (err == cudaSuccess && p.split_from < blocks) err = launch_fwd_merge(p, o, lse, d, s);
   if (err == cudaSuccess) err = timing_record(0, false, s);
-  if (scratch != nullptr && scratch != workspace) {
-    const cudaError_t ferr = cudaFreeAsync(scratch, s);
-    if (err == cudaSuccess) err = ferr;
-  }
   return err == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -567,22 +555,6 @@ int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void
                          size_t workspace_bytes, void* stream) {
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
                   workspace_bytes, stream, true);
-}
-
-int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                   const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-                   float scale, int causal, void* stream) {
-  bool empty = false;
-  int rc = check_shape(B, H, N, d, scale, &empty);
-  if (rc != FA_OK || empty) return rc;
-  if (fa_bwd_workspace_bytes(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_TOO_LARGE;
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  void* scratch = noalloc_scratch_ptr();
-  if (!scratch) return FA_ERR_CUDA;
-  // fa_bwd's first kernel zeroes the dQ accumulator and overwrites D, so the
-  // previous call's contents of the scratch do not matter.
-  return fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, scratch,
-                FA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 int fa_last_device_status(void* stream) {

@@ -509,23 +509,22 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
-// Pair form: arrives once on the barrier at `bar` (this CTA's address) in
-// every CTA of `cta_mask` (bit r = rank r) when the pair MMAs this thread
-// issued so far have completed.
+// Pair form: arrives once on the barrier at shared::cluster address
+// `cluster_bar` (this CTA's own address, or one from cluster_smem() for the
+// other CTA of the pair) when the pair MMAs this thread issued so far have
+// completed.  A barrier in each CTA takes one commit each.
 template <bool kWarp = false>
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+__device__ __forceinline__ void mma_commit_pair(uint32_t cluster_bar) {
   if constexpr (kWarp)
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;\n\t}" ::"r"(bar),
-        "h"(cta_mask)
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            cluster_bar)
         : "memory");
   else
     asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            cluster_bar)
         : "memory");
 }
 

@@ -395,10 +395,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       // FP8: V^T is K-major ([d][key]); bf16: V is MN-major ([key][d]).
       constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3_f32(kM, D, false, false)
                                         : idesc_bf16_f32(kM, D, false, true);
-      // A commit reaches both CTAs of a pair.
+      // Pair mode: one commit to the barrier in each CTA of the pair.
       auto commit = [&](int b) {
-        if constexpr (PAIR) mma_commit_pair<kWarpIssue>(bar(b), 3);
-        else mma_commit<kWarpIssue>(bar(b));
+        if constexpr (PAIR) {
+          mma_commit_pair<kWarpIssue>(bar(b));
+          mma_commit_pair<kWarpIssue>(cluster_smem(bar(b), 1));
+        } else {
+          mma_commit<kWarpIssue>(bar(b));
+        }
       };
       const uint32_t q_smem = sbase + C::kQOff;
       const uint32_t ring = sbase + C::kRingOff;
@@ -529,7 +533,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         base += 2 * item.nmax;
       }
       // Every MMA this thread issued must finish before tensor memory is freed.
-      if constexpr (PAIR) mma_commit_pair<kWarpIssue>(bar(C::kBarMmaDone), 1);
+      if constexpr (PAIR) mma_commit_pair<kWarpIssue>(bar(C::kBarMmaDone));
       else mma_commit<kWarpIssue>(bar(C::kBarMmaDone));
       mbar_wait_drain(bar(C::kBarMmaDone), 0);
     }

@@ -44,8 +44,14 @@ def _load() -> ctypes.CDLL:
             "(there is no CPU fallback)")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_workspace_bytes.restype = sz
+    lib.fa_set_exp2_poly_share.argtypes = [i]
+    lib.fa_set_exp2_poly_share.restype = i
+    lib.fa_get_exp2_poly_share.argtypes = []
+    lib.fa_get_exp2_poly_share.restype = i
     lib.fa_fwd_2cta.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd_2cta.restype = i
     lib.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -162,10 +168,25 @@ def _workspace(ws, device):
 # --- the C entry points --------------------------------------------------------
 
 
-def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, workspace=None, stream=None) -> None:
+    """workspace: None, or a CUDA tensor of at least fa_fwd_workspace_bytes()
+    bytes that lets the call split its last partial round of work."""
     B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o)), lse)
+    ws_ptr, ws_bytes = _workspace(workspace, q.device)
     _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
-                      int(bool(causal)), _stream(stream)), "fa_fwd")
+                      int(bool(causal)), ws_ptr, ws_bytes, _stream(stream)), "fa_fwd")
+
+
+def fa_fwd_workspace_bytes(B: int, H: int, N: int, d: int, causal: bool) -> int:
+    return int(lib.fa_fwd_workspace_bytes(B, H, N, d, int(bool(causal))))
+
+
+def fa_set_exp2_poly_share(per_octet: int) -> None:
+    _check(lib.fa_set_exp2_poly_share(int(per_octet)), "fa_set_exp2_poly_share")
+
+
+def fa_get_exp2_poly_share() -> int:
+    return int(lib.fa_get_exp2_poly_share())
 
 
 def fa_fwd_2cta(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
@@ -317,12 +338,20 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
             raise ValueError("the CTA-pair forward has no key-range split")
         fa_fwd_2cta(q, k, v, o, lse, scale, causal, stream)
     elif num_splits == 1:
-        fa_fwd(q, k, v, o, lse, scale, causal, stream)
+        fa_fwd(q, k, v, o, lse, scale, causal, fwd_workspace_for(q, causal), stream)
     else:
         n = fa_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits)
         ws = torch.empty(max(n, 1), dtype=torch.uint8, device=q.device)
         fa_fwd_splitkv(q, k, v, o, lse, scale, causal, num_splits, ws, stream)
     return o, lse
+
+
+def fwd_workspace_for(q, causal: bool):
+    """fa_fwd's optional workspace for q's shape on the current device (None
+    when the call would not use one)."""
+    B, H, N, d = _shape(q)
+    n = fa_fwd_workspace_bytes(B, H, N, d, causal)
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n > 0 else None
 
 
 def workspace_for(q, deterministic: bool = False):

@@ -19,10 +19,11 @@
  *   - d must be 64 or 128.  Any N >= 0 is accepted; a ragged last tile is
  *     masked.  B, H, N of 0 are a no-op that returns FA_OK.
  *   - Queries and keys have the same length N, so "causal" is unambiguous.
- *   - The caller owns every input, output and workspace buffer.  The only
- *     device memory the library takes on its own is fa_fwd's scratch for its
- *     split last round (from a private stream-ordered pool, see fa_fwd) and
- *     fa_bwd_noalloc's fixed scratch array.
+ *   - The caller owns every input, output and workspace buffer; no entry
+ *     point allocates or frees device memory.  The one piece of device
+ *     memory the library holds is fa_bwd_noalloc's fixed scratch array,
+ *     which lives in a module of its own and is loaded only by a process
+ *     that calls fa_bwd_noalloc (see there).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream).  The return value reports argument validation and
  *     launch errors only.  A kernel that gives up on a bounded wait records
@@ -63,20 +64,50 @@ typedef enum {
  *   lse     : out, fp32 [B, H, N]
  *   scale   : the factor on Q K^T (usually 1/sqrt(d)); must be finite and > 0
  *   causal  : 0 = every key, 1 = key j <= query i
+ *   workspace, workspace_bytes : optional device scratch owned by the caller
+ *             (NULL / 0 = none).  With at least fa_fwd_workspace_bytes()
+ *             bytes (256-byte aligned) the call may balance its last round
+ *             of work (below); without it the result is the same, computed
+ *             without that split.  Contents on entry do not matter.
  * Kernels: TMA-staged Q/K/V tiles, tcgen05 MMAs accumulating S and O in
  * tensor memory, warp-specialised load / MMA / softmax roles, polynomial exp2
- * mixed with the MUFU unit, O rescaled only when a row max grows past a
- * threshold (FlashAttention-4 abstract, items 1-3).  One persistent CTA per
- * SM walks the (batch, head, 256-query block) work items.  Non-causal, when
- * the last round of items would leave SMs idle, those items are cut into key
- * ranges merged by log-sum-exp (see fa_fwd_splitkv); their fp32 partials
- * come from a library-private stream-ordered memory pool on `stream`
- * (created on the device's first such call, kept for the process), so the
- * call stays asynchronous and may be captured in a CUDA graph once that
- * pool exists.
+ * on the FMA pipe selectable beside the MUFU unit (fa_set_exp2_poly_share),
+ * O rescaled only when a row max grows past a threshold (FlashAttention-4
+ * abstract, items 1-3).  One persistent CTA per SM walks the (batch, head,
+ * 256-query block) work items.  Non-causal, when the last round of items
+ * would leave SMs idle and a workspace is given, those items are cut into
+ * key ranges merged by log-sum-exp (as fa_fwd_splitkv does), their fp32
+ * partials kept in the workspace.
+ * Returns FA_ERR_WORKSPACE for a non-NULL workspace that is short or not
+ * 256-byte aligned.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-           int N, int d, float scale, int causal, void* stream);
+           int N, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+           void* stream);
+
+/*
+ * Bytes of optional workspace fa_fwd uses to split its last partial round of
+ * work items on the current device (the split depends on the device's SM
+ * count): fp32 partial O and LSE of the split items.  0 when no split applies
+ * (causal problems, problems whose items fill whole rounds, short key
+ * ranges) or for empty or unsupported shapes.
+ */
+size_t fa_fwd_workspace_bytes(int B, int H, int N, int d, int causal);
+
+/*
+ * Share of the bf16 forward's exponentials evaluated in software on the FMA
+ * pipe: per_octet of every 8 exponentials of a row tile (0..3) go to a
+ * degree-3 polynomial exp2 (2^x = 2^round(x) * p(x - round(x)), max relative
+ * error 1.01e-4), the rest to the MUFU ex2 unit ("Программная эмуляция
+ * экспоненты" of "FlashAttention-3 и FlashAttention-4"; FlashAttention-4
+ * abstract, item 2).  Process-wide, for calls made after it; the initial
+ * value is 0, or FA_FWD_POLY_PER_OCTET from the environment.  On GB300 the
+ * MUFU unit is not the forward's limit and every share above 0 measured
+ * slower.  Returns FA_ERR_INVALID_ARG outside 0..3.
+ * fa_get_exp2_poly_share() returns the current value.
+ */
+int fa_set_exp2_poly_share(int per_octet);
+int fa_get_exp2_poly_share(void);
 
 /*
  * 2-CTA forward: the same operation, arguments and errors as fa_fwd, computed
@@ -133,7 +164,9 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
  * The result approximates fa_fwd's to FP8 precision (about 5% relative
  * Frobenius error on O for N(0,1) inputs).
  *   rotate    : 1 = rotate Q and K (incoherent processing), 0 = plain FP8
- *   workspace : fa_fwd_fp8_workspace_bytes() bytes, 256-byte aligned
+ *   workspace : fa_fwd_fp8_workspace_bytes() bytes, 256-byte aligned: the
+ *               e4m3 operands and their scales, then the partials of the
+ *               last-round split fa_fwd makes on the current device
  * Returns FA_ERR_UNSUPPORTED for d != 128, FA_ERR_WORKSPACE for a missing,
  * short or misaligned workspace, FA_ERR_INVALID_ARG for rotate not 0 or 1.
  */
@@ -204,8 +237,12 @@ int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void
  *
  * Same arguments and results as fa_bwd, minus the workspace: the scratch
  * (D and the fp32 dQ accumulator) lives in one fixed array of
- * FA_NOALLOC_SCRATCH_BYTES (96 MiB) of device memory inside the library,
- * which every GPU that loads the library keeps until the process exits.
+ * FA_NOALLOC_SCRATCH_BYTES (96 MiB) of device memory inside the library.
+ * The array sits in a module of its own, which the CUDA runtime loads on a
+ * device at the process's first fa_bwd_noalloc call there (with the
+ * runtime's default lazy module loading; CUDA_MODULE_LOADING=EAGER loads it
+ * with the library); from then on that device keeps it until the process
+ * exits.  Processes that never call fa_bwd_noalloc do not hold it.
  * Problems whose fa_bwd_workspace_bytes() exceeds it (at d = 128 roughly
  * B*H*N > 195,000 rows, at d = 64 > 380,000) return FA_ERR_TOO_LARGE.
  * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
@@ -271,7 +308,8 @@ int fa_timing_last_ms(int kernel, float* ms);
  * entry points, streams and threads (launches that CUDA refused are not
  * counted).  The difference of two readings counts the launches in between,
  * e.g. in a timed region: fa_fwd launches one kernel, or two when it splits
- * its last partial round of work (the forward, then the merge); fa_bwd three;
+ * its last partial round of work in the caller's workspace (the forward,
+ * then the merge); fa_bwd three;
  * fa_bwd_deterministic three; fa_fwd_fp8 three (two preparation kernels and
  * the forward; four with the merge, as fa_fwd); fa_fwd_splitkv two;
  * fa_fwd_2cta one.

@@ -130,11 +130,17 @@ def compare_bwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_
                 kv_heads=(), deterministic=False):
     """Backward parity.  Heads with index < full_heads (None = all) compare
     every row of dQ, dK, dV; other heads compare sampled dQ rows, and the
-    heads listed in kv_heads also sampled dK/dV rows."""
+    heads listed in kv_heads also sampled dK/dV rows.
+
+    Besides the bounded errors, the returned dict reports (without a bound)
+    "dq_exact_o": dQ's error against the plain definition, D formed from the
+    oracle's exact fp64 O instead of its bf16-rounded O, over the same rows.
+    The gap between the two is the cost of carrying O in bf16 between the
+    passes; on the softmax-stress inputs it exceeds the 2e-2 bound."""
     inputs, grads, scale = run_bwd(B, H, N, d, causal, seed, stress, deterministic=deterministic)
     q64, k64, v64, do64 = (t.double().numpy() for t in inputs)
     dq, dk, dv = grads
-    worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0}
+    worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0, "dq_exact_o": 0.0}
     for b in range(B):
         for h in range(H):
             idx = b * H + h
@@ -148,10 +154,16 @@ def compare_bwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_
                                 qrows=qrows, krows=krows, o_bf16=True)
             qs = slice(None) if qrows is None else qrows
             worst["dq"] = max(worst["dq"], check_grad(dq[b, h][qs], r[0], what + " dQ"))
+            exact = oracle.bwd_head(q64[b, h], k64[b, h], v64[b, h], do64[b, h], scale, causal,
+                                    qrows=qrows, krows=[], o_bf16=False)[0]
+            worst["dq_exact_o"] = max(worst["dq_exact_o"], rel_fro(dq[b, h][qs], exact))
             if krows is None or len(krows):
                 ks = slice(None) if krows is None else krows
                 worst["dk"] = max(worst["dk"], check_grad(dk[b, h][ks], r[1], what + " dK"))
                 worst["dv"] = max(worst["dv"], check_grad(dv[b, h][ks], r[2], what + " dV"))
+    print(f"B{B} H{H} N{N} d{d} causal={causal} stress={stress}: dQ {worst['dq']:.2e} "
+          f"(D from bf16 O; {worst['dq_exact_o']:.2e} from exact O), dK {worst['dk']:.2e}, "
+          f"dV {worst['dv']:.2e}")
     return worst, grads, inputs
 
 

@@ -65,8 +65,9 @@ P = ctypes.c_void_p
 
 
 def fwd(lib, q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, B=1, H=1, N=128, d=64,
-        scale=0.125, causal=0):
-    return lib.lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, causal, None)
+        scale=0.125, causal=0, ws=0, ws_bytes=0):
+    return lib.lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, causal, P(ws),
+                          ws_bytes, None)
 
 
 def test_fwd_validation(lib):
@@ -82,9 +83,35 @@ def test_fwd_validation(lib):
     assert fwd(lib, k=0x1008) == lib.FA_ERR_INVALID_ARG  # not 16-byte aligned
     assert fwd(lib, lse=0x1002) == lib.FA_ERR_INVALID_ARG
     assert fwd(lib, causal=2) == lib.FA_ERR_INVALID_ARG
+    # the optional workspace, when given, must be 256-byte aligned
+    assert fwd(lib, ws=0x10010, ws_bytes=1 << 20) == lib.FA_ERR_WORKSPACE
     # empty problems are a no-op even with null pointers
     assert fwd(lib, q=0, k=0, v=0, o=0, lse=0, N=0) == lib.FA_OK
     assert fwd(lib, q=0, k=0, v=0, o=0, lse=0, B=0) == lib.FA_OK
+
+
+def test_fwd_workspace_bytes(lib):
+    """The last-round split needs scratch only where it applies: never for
+    causal problems, empty or unsupported shapes, or work that fills whole
+    rounds; here (no GPU, so no SM count) never at all."""
+    ws = lib.fa_fwd_workspace_bytes
+    assert ws(2, 16, 4096, 128, True) == 0
+    assert ws(0, 16, 4096, 128, False) == 0
+    assert ws(2, 16, 4096, 96, False) == 0
+    assert ws(1, 1, 128, 64, False) == 0  # one work item: nothing to balance
+
+
+def test_exp2_poly_share_setting(lib):
+    before = lib.fa_get_exp2_poly_share()
+    try:
+        for n in (0, 1, 2, 3):
+            lib.fa_set_exp2_poly_share(n)
+            assert lib.fa_get_exp2_poly_share() == n
+        for bad in (-1, 4, 8):
+            assert lib.lib.fa_set_exp2_poly_share(bad) == lib.FA_ERR_INVALID_ARG
+        assert lib.fa_get_exp2_poly_share() == 3
+    finally:
+        lib.fa_set_exp2_poly_share(before)
 
 
 def test_fwd_2cta_validation(lib):
@@ -157,8 +184,10 @@ def test_fp8_workspace_bytes(lib):
     B, H, N = 2, 3, 300
     rows, bh, np_ = B * H * N, B * H, 304
     blocks = (N + 127) // 128  # per-block amax slots of K and V
+    # the FP8 operands and scales, then the forward's last-round split partials
     assert ws(B, H, N, 128) == (2 * up(rows * 128) + up(bh * 128 * np_) + up(rows * 4) +
-                                up(2 * bh * 4) + up(2 * bh * blocks * 4))
+                                up(2 * bh * 4) + up(2 * bh * blocks * 4) +
+                                lib.fa_fwd_workspace_bytes(B, H, N, 128, False))
     assert ws(B, H, N, 64) == 0  # d = 128 only
     assert ws(0, H, N, 128) == 0
 

@@ -23,8 +23,10 @@ def test_ragged_and_multi_tile(N, d, causal):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_softmax_stress(d, causal):
-    compare_bwd(1, 3, 768, d, causal, stress=True)
+def test_softmax_stress(d, causal, record_property):
+    worst, _, _ = compare_bwd(1, 3, 768, d, causal, stress=True)
+    # reported, not bounded: dQ against D formed from the exact O
+    record_property("dq_exact_o", worst["dq_exact_o"])
 
 
 def test_b2_h16_n8192_causal():

@@ -14,8 +14,8 @@ pytestmark = pytest.mark.gpu
 def test_cuda_graph_capture_of_a_step():
     """fwd + bwd captured once and replayed: the replay equals an eager step
     (O, LSE, dK, dV bit for bit; dQ up to the order of its fp32 additions).
-    B2 H16 N4096 non-causal also takes the forward's tail split, whose
-    scratch comes from a stream-ordered pool, inside the graph."""
+    B2 H16 N4096 non-causal also takes the forward's last-round split, in
+    the caller's workspace, inside the graph."""
     from exact_attention_98_gb300 import fa
     from exact_attention_98_gb300.inputs import attention_inputs
 
@@ -25,9 +25,11 @@ def test_cuda_graph_capture_of_a_step():
     o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device="cuda")
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
     ws = fa.workspace_for(q)
+    wsf = fa.fwd_workspace_for(q, False)
+    assert wsf is not None  # 512 items on 152 SMs: the last round is split
     s = torch.cuda.Stream()
-    with torch.cuda.stream(s):  # eager reference (also creates the library's pool)
-        fa.fa_fwd(q, k, v, o, lse, scale, False)
+    with torch.cuda.stream(s):  # eager reference
+        fa.fa_fwd(q, k, v, o, lse, scale, False, wsf)
         fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, False, ws)
     s.synchronize()
     ref = [t.clone() for t in (o, lse, dq, dk, dv)]
@@ -35,7 +37,7 @@ def test_cuda_graph_capture_of_a_step():
         t.zero_()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=s):
-        fa.fa_fwd(q, k, v, o, lse, scale, False)
+        fa.fa_fwd(q, k, v, o, lse, scale, False, wsf)
         fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, False, ws)
     for _ in range(2):
         graph.replay()

@@ -46,6 +46,42 @@ def test_hadamard_rows_are_orthogonal_and_plus_minus_one():
     assert np.array_equal(h @ h.T, 128 * np.eye(128))
 
 
+def test_quantise_row_scales_by_hand():
+    """One scale per row (axis=1) against one for the whole array: row 0 has
+    amax 1 (scale 448), row 1 amax 8 (scale 56)."""
+    x = np.array([[1.0, 0.5, 0.25, 0.0], [8.0, 4.0, 2.0, 1.0]])
+    q8, desc = F.quantise(x, axis=1)
+    assert np.array_equal(q8, [[448, 224, 112, 0], [448, 224, 112, 56]])
+    assert np.array_equal(desc, [[1 / 448], [1 / 56]])
+    q8, desc = F.quantise(x)
+    assert np.array_equal(q8, [[56, 28, 14, 0], [448, 224, 112, 56]]) and desc == 1 / 56
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_forward_by_hand(causal):
+    """A 2 x 4 case worked by hand, without rotation, scale = ln 2 (so that
+    exp(scale s) = 2^s).  Q rows have amax 1 and 3: row scales 448 and 448/3
+    put both rows exactly on the e4m3 grid, while one scale for all of Q
+    (448/3) would round row 0 (1 -> 144/(448/3), 0.5 -> 72/(448/3)) and change
+    its scores.  K (amax 2) and V (amax 4) are exact with their scales.
+      scores / ln 2 = Q K^T = [[2, 1], [3, -3]]
+      row 0: p = [1, 1/2], l = 3/2, 64 p = [64, 32] (exact in e4m3)
+             O = (v0 + v1 / 2) / (3/2) = [2, 2, 3, 17/6], LSE = 2 ln 2 + ln 3/2
+             (causal: key 0 only, O = v0, LSE = 2 ln 2)
+      row 1: p = [1, 1/64], l = 65/64, 64 p = [64, 1] (exact)
+             O = (64 v0 + v1) / 65 = [68, 130, 257, 256.5] / 65,
+             LSE = 3 ln 2 + ln 65/64"""
+    q = np.array([[1.0, 0.5, 0.0, 0.0], [0.0, 0.0, 3.0, -1.5]])
+    k = np.array([[2.0, 0.0, 1.0, 0.0], [0.0, 2.0, 0.0, 2.0]])
+    v = np.array([[1.0, 2.0, 4.0, 4.0], [4.0, 2.0, 1.0, 0.5]])
+    ln2 = math.log(2.0)
+    o, lse = F.forward_head(q, k, v, ln2, causal, rotate=False)
+    o0 = [1.0, 2.0, 4.0, 4.0] if causal else [2.0, 2.0, 3.0, 17.0 / 6.0]
+    l0 = 2 * ln2 + (0.0 if causal else math.log(1.5))
+    assert np.allclose(o, [o0, np.array([68.0, 130.0, 257.0, 256.5]) / 65.0], rtol=0, atol=1e-12)
+    assert np.allclose(lse, [l0, 3 * ln2 + math.log(65.0 / 64.0)], rtol=0, atol=1e-12)
+
+
 def test_quantise_is_lossless_on_the_e4m3_grid():
     grid = F.round_e4m3(np.linspace(-448, 448, 301))
     q8, desc = F.quantise(grid)
