@@ -41,16 +41,23 @@ def call_noalloc(fa, q, k, v, o, lse, do, grads, scale, causal):
 
 def check_dq(got, ref):
     """dQ is accumulated with fp32 atomics in an order that varies from call
-    to call, then rounded to bf16: an element may land one bf16 ulp away
-    (where the fp32 sums straddle a rounding boundary), and only rarely."""
+    to call, then rounded to bf16.  The order changes the fp32 sum by a few
+    fp32 ulps of its summands, which are of the size of the tensor's largest
+    elements; rounded to bf16 that moves an element by one bf16 ulp where the
+    sums straddle a rounding boundary, or, where cancellation leaves an
+    element much smaller than its summands, by about the fp32 noise itself.
+    So: every element within one bf16 ulp of fa_bwd's or within 1e-5 of the
+    largest |dQ|, few elements different, and a relative Frobenius error of
+    at most 1e-3 (one flipped bf16 element is 2^-8 relative)."""
     g = got.cpu().double().numpy()
     r = ref.cpu().double().numpy()
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(r), 1e-30))) - 7)
     diff = np.abs(g - r)
-    assert (diff <= ulp * 1.0001 + 1e-30).all(), float((diff / ulp).max())
-    assert (diff > 0).mean() <= 1e-3, float((diff > 0).mean())
+    floor = 1e-5 * np.abs(r).max()
+    assert (diff <= np.maximum(ulp * 1.0001, floor)).all(), float(diff.max())
+    assert (diff > 0).mean() <= 1e-2, float((diff > 0).mean())
     rel = np.linalg.norm(g - r) / np.linalg.norm(r)
-    assert rel <= 1e-4, rel
+    assert rel <= 1e-3, rel
 
 
 @pytest.mark.parametrize("causal", [False, True])
