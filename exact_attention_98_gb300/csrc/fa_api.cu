@@ -479,7 +479,7 @@ namespace {
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
              float scale, int causal, void* workspace, size_t workspace_bytes, void* stream,
-             bool deterministic) {
+             bool deterministic, bool pair = false) {
   bool empty = false;
   int rc = check_shape(B, H, N, d, scale, &empty);
   if (rc != FA_OK || empty) return rc;
@@ -488,6 +488,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
       !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (pair && d != 128) return FA_ERR_UNSUPPORTED;
   const size_t need = deterministic ? fa_bwd_deterministic_workspace_bytes(B, H, N, d)
                                     : fa_bwd_workspace_bytes(B, H, N, d);
   if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
@@ -502,6 +503,37 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   float* dq_acc = deterministic ? nullptr : dq_buf;
   const int n_kblk = (N + kBlockN - 1) / kBlockN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (pair) {
+    BwdPairParams pp;
+    if (!encode_tile_map(&pp.tm_q, q, N, BH, d) || !encode_tile_map(&pp.tm_do, dout, N, BH, d) ||
+        !encode_tile_map(&pp.tm_q64, q, N, BH, d, 64) ||
+        !encode_tile_map(&pp.tm_do64, dout, N, BH, d, 64) ||
+        !encode_tile_map(&pp.tm_k, k, N, BH, d) || !encode_tile_map(&pp.tm_v, v, N, BH, d))
+      return FA_ERR_CUDA;
+    pp.lse = lse;
+    pp.dsum = dsum;
+    pp.dq_acc = dq_acc;
+    pp.dk = dk;
+    pp.dv = dv;
+    pp.status = status_ptr();
+    if (!pp.status) return FA_ERR_CUDA;
+    pp.N = N;
+    pp.BH = BH;
+    pp.n_kblk = n_kblk;
+    pp.n_kpair = (n_kblk + 1) / 2;
+    pp.causal = causal;
+    pp.c = scale * 1.4426950408889634f;
+    pp.scale = scale;
+    pp.inv_scale = 1.0f / scale;
+    if (2LL * pp.n_kpair * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    if (launch_bwd_pre(o, dout, dsum, dq_acc, rows, d, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (timing_record(1, true, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_bwd_pair(pp, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_bwd_post(dq_acc, dq, rows * d, s) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+  }
 
   BwdParams p;
   if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
@@ -547,6 +579,13 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
                   workspace_bytes, stream, false);
+}
+
+int fa_bwd_2cta(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                  workspace_bytes, stream, false, true);
 }
 
 int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,

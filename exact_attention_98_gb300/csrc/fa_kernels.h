@@ -98,6 +98,35 @@ struct BwdParams {
   float log2e;
 };
 
+// Backward by CTA pairs (d = 128): a cluster of two CTAs owns two
+// consecutive key tiles of one head (256 keys) and shares every product as
+// one tcgen05 cta_group::2 MMA.
+struct BwdPairParams {
+  CUtensorMap tm_q;     // bf16 [BH, N, d], box {64, 128, 1}: Q rows x one 64-column half of d
+  CUtensorMap tm_do;
+  CUtensorMap tm_q64;   // box {64, 64, 1}: this CTA's 64 query rows, one 64-column block
+  CUtensorMap tm_do64;
+  CUtensorMap tm_k;     // box {64, 128, 1}
+  CUtensorMap tm_v;
+  const float* lse;     // fp32 [BH, N]
+  const float* dsum;    // fp32 [BH, N]: D = rowsum(dO * O)
+  float* dq_acc;        // fp32 [BH, N, d], zeroed before the main kernel
+  void* dk;             // bf16 [BH, N, d]
+  void* dv;             // bf16 [BH, N, d]
+  unsigned int* status;
+  int N;
+  int BH;
+  int n_kblk;   // ceil(N / 128)
+  int n_kpair;  // ceil(n_kblk / 2): key-tile pairs per head
+  int causal;
+  float c;          // scale * log2(e)
+  float scale;
+  float inv_scale;
+};
+
+// Backward main kernel run by CTA pairs (d = 128 only).
+cudaError_t launch_bwd_pair(const BwdPairParams& p, cudaStream_t stream);
+
 // FP8 forward inputs (d = 128), in the caller's workspace.
 struct Fp8Buffers {
   uint8_t* q8;          // e4m3 [BH, N, 128], Q rotated, one scale per row

@@ -76,6 +76,8 @@ def _load() -> ctypes.CDLL:
     lib.fa_exp2_poly_eval.restype = i
     lib.fa_debug_bounded_wait.argtypes = [ctypes.c_ulonglong, vp]
     lib.fa_debug_bounded_wait.restype = i
+    lib.fa_bwd_2cta.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, sz, vp]
+    lib.fa_bwd_2cta.restype = i
     lib.fa_bwd_deterministic_workspace_bytes.argtypes = [i, i, i, i]
     lib.fa_bwd_deterministic_workspace_bytes.restype = sz
     lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp,
@@ -249,6 +251,18 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool, worksp
                       ws_ptr, ws_bytes, _stream(stream)), "fa_bwd")
 
 
+def fa_bwd_2cta(q, k, v, o, lse, dout, dq, dk, dv, scale: float, causal: bool, workspace,
+                stream=None) -> None:
+    """fa_bwd computed by CTA pairs sharing each product (d = 128); same
+    workspace as fa_bwd."""
+    B, H, N, d = _check_attention(q, (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout),
+                                      ("dq", dq), ("dk", dk), ("dv", dv)), lse)
+    ws_ptr, ws_bytes = _workspace(workspace, q.device)
+    _check(lib.fa_bwd_2cta(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                           _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                           ws_ptr, ws_bytes, _stream(stream)), "fa_bwd_2cta")
+
+
 def fa_bwd_deterministic_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return int(lib.fa_bwd_deterministic_workspace_bytes(B, H, N, d))
 
@@ -363,14 +377,17 @@ def workspace_for(q, deterministic: bool = False):
 
 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
-             workspace=None, stream=None, deterministic: bool = False):
+             workspace=None, stream=None, deterministic: bool = False, two_cta: bool = False):
     """Returns (dq, dk, dv) freshly allocated on q's device.  deterministic:
-    fa_bwd_deterministic (bit-identical from run to run) instead of fa_bwd."""
+    fa_bwd_deterministic (bit-identical from run to run) instead of fa_bwd;
+    two_cta: the CTA-pair backward (fa_bwd_2cta)."""
     B, H, N, d = _shape(q)
     scale = default_scale(d) if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    if deterministic and two_cta:
+        raise ValueError("the CTA-pair backward adds dQ with atomics")
     if workspace is None:
         workspace = workspace_for(q, deterministic)
-    run = fa_bwd_deterministic if deterministic else fa_bwd
+    run = fa_bwd_deterministic if deterministic else fa_bwd_2cta if two_cta else fa_bwd
     run(q, k, v, o, lse, dout, dq, dk, dv, scale, causal, workspace, stream)
     return dq, dk, dv

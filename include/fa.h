@@ -203,6 +203,26 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * 2-CTA backward: the same operation, arguments, workspace and errors as
+ * fa_bwd, computed by pairs of CTAs (a cluster of two on one TPC) that own two
+ * consecutive 128-key tiles of one head and share every product as one
+ * tcgen05 cta_group::2 MMA ("FlashAttention-3 и FlashAttention-4", section
+ * "Режим 2-CTA MMA": two CTAs on one matrix operation halve the
+ * shared-memory operand traffic and the backward's atomic updates;
+ * FlashAttention-4 abstract, item 3).  S^T, dP^T, dV and dK are M = 256
+ * products in which each CTA loads half of every Q / dO operand;
+ * dQ^T = K^T dS^T is one product over the pair's 256 keys, each CTA adding
+ * its 64 rows of d, so dQ takes one fp32 addition per element per 256 keys
+ * instead of per 128.  Each compute warpgroup writes its half of dS into the
+ * shared memory of the CTA that needs it (distributed shared memory).
+ * Only d = 128 (others return FA_ERR_UNSUPPORTED).  dK and dV equal fa_bwd's
+ * within rounding; dQ within the order of its fp32 additions.
+ */
+int fa_bwd_2cta(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device workspace fa_bwd_deterministic needs: fp32 D [B, H, N] and
  * one fp32 dQ contribution per key tile, ceil(N / 128) x [B, H, N, d], each
  * part 256-byte aligned (at B2 H16 N4096 d128 about 2.1 GB).  Returns 0 for
@@ -312,7 +332,7 @@ int fa_timing_last_ms(int kernel, float* ms);
  * then the merge); fa_bwd three;
  * fa_bwd_deterministic three; fa_fwd_fp8 three (two preparation kernels and
  * the forward; four with the merge, as fa_fwd); fa_fwd_splitkv two;
- * fa_fwd_2cta one.
+ * fa_fwd_2cta one; fa_bwd_2cta three.
  */
 unsigned long long fa_launch_count(void);
 

@@ -109,9 +109,11 @@ def compare_fwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_
     return worst_o, worst_l
 
 
-def run_bwd(B, H, N, d, causal, seed=0, stress=False, scale=None, deterministic=False):
+def run_bwd(B, H, N, d, causal, seed=0, stress=False, scale=None, deterministic=False,
+            two_cta=False):
     """GPU forward then backward; O and LSE come from this library's forward.
-    deterministic: the backward runs through fa_bwd_deterministic."""
+    deterministic: the backward runs through fa_bwd_deterministic; two_cta:
+    through fa_bwd_2cta."""
     from exact_attention_98_gb300 import fa
 
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -120,14 +122,14 @@ def run_bwd(B, H, N, d, causal, seed=0, stress=False, scale=None, deterministic=
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     o, lse = fa.forward(qd, kd, vd, causal=causal, scale=scale)
     dq, dk, dv = fa.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale,
-                             deterministic=deterministic)
+                             deterministic=deterministic, two_cta=two_cta)
     status = fa.fa_last_device_status()
     assert status == fa.FA_OK, fa.status_string(status)
     return (q, k, v, do), (to64(dq), to64(dk), to64(dv)), scale
 
 
 def compare_bwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_per_head=None,
-                kv_heads=(), deterministic=False):
+                kv_heads=(), deterministic=False, two_cta=False):
     """Backward parity.  Heads with index < full_heads (None = all) compare
     every row of dQ, dK, dV; other heads compare sampled dQ rows, and the
     heads listed in kv_heads also sampled dK/dV rows.
@@ -137,7 +139,8 @@ def compare_bwd(B, H, N, d, causal, seed=0, stress=False, full_heads=None, rows_
     oracle's exact fp64 O instead of its bf16-rounded O, over the same rows.
     The gap between the two is the cost of carrying O in bf16 between the
     passes; on the softmax-stress inputs it exceeds the 2e-2 bound."""
-    inputs, grads, scale = run_bwd(B, H, N, d, causal, seed, stress, deterministic=deterministic)
+    inputs, grads, scale = run_bwd(B, H, N, d, causal, seed, stress, deterministic=deterministic,
+                                   two_cta=two_cta)
     q64, k64, v64, do64 = (t.double().numpy() for t in inputs)
     dq, dk, dv = grads
     worst = {"dq": 0.0, "dk": 0.0, "dv": 0.0, "dq_exact_o": 0.0}
