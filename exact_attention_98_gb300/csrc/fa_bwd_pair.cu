@@ -26,8 +26,12 @@
 // product needs, in each CTA, the 256 keys' rows of K restricted to its 64
 // columns of d (loaded once), and dS for its 64 queries over all 256 keys:
 // the compute warpgroup that owns query half h (thread = key row) writes its
-// dS row into CTA h's shared memory, over distributed shared memory when h
-// is the other CTA.
+// dS row into CTA h's operand buffer.  For the CTA's own half that is a
+// local store; the other half is staged locally and sent to the other CTA as
+// one 16 KB bulk copy over distributed shared memory (async proxy, completing
+// on a barrier of the receiving CTA).  Remote stores by the compute threads
+// themselves would need a cluster-scope proxy fence, measured at about 2000
+// cycles per tile.
 //
 // tcgen05 layouts measured on the device: an M = 256 pair product gives each
 // CTA its 128 rows in lanes 0..127, N columns; an M = 128 pair product gives
@@ -53,7 +57,9 @@
 //   warp  12    loads (each CTA its own halves; every copy is counted on
 //               rank 0's barriers) and the bias rows of its query half
 //   warp  13    tensor-memory allocator; rank 0's lane 0 issues every MMA
-//   warps 14-15 idle
+//   warp  14    dS exchange: sends the staged half to the other CTA, and
+//               reports the half it receives to rank 0's MMA issuer
+//   warp  15    idle
 // Launched with 128 registers per thread; the warpgroups then re-split them
 // (compute 144, drain 128, load/MMA 96).
 #include "fa_device.cuh"
@@ -75,6 +81,7 @@ struct PairBwdCfg {
   static constexpr int kDrainWarp0 = 8;
   static constexpr int kProducerWarp = 12;
   static constexpr int kMmaWarp = 13;
+  static constexpr int kExchangeWarp = 14;
   static constexpr int kTileBytes = 128 * 128 * 2;  // 128 rows x 128 columns
   static constexpr int kHalfBytes = 128 * 64 * 2;   // 128 rows x 64 columns (one swizzle block)
   static constexpr int kQuarterBytes = 64 * 64 * 2;  // 64 rows x 64 columns
@@ -95,7 +102,11 @@ struct PairBwdCfg {
   static constexpr int kBiasLbo = 128;
   static constexpr int kBiasSbo = 256;
   static constexpr int kBiasOff = kOnesOff + kOnesBytes;  // [stage][lse, d]
-  static constexpr int kBarOff = kBiasOff + kStages * 2 * kBiasTileBytes;
+  // dS of this CTA's keys for the other CTA's query half (128 key rows x 64
+  // queries, laid out as in the receiving buffer), sent by bulk copy
+  static constexpr int kStageOff = kBiasOff + kStages * 2 * kBiasTileBytes;
+  static constexpr int kStageBytes = 128 * 128;
+  static constexpr int kBarOff = kStageOff + kStageBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarYFull = 1;  // kStages
   static constexpr int kBarYEmpty = kBarYFull + kStages;
@@ -109,7 +120,9 @@ struct PairBwdCfg {
   static constexpr int kBarDQFull = kBarDSFull + 1;
   static constexpr int kBarDQEmpty = kBarDQFull + 1;
   static constexpr int kBarMmaDone = kBarDQEmpty + 1;
-  static constexpr int kNumBars = kBarMmaDone + 1;
+  static constexpr int kBarDSStaged = kBarMmaDone + 1;  // the staged half is written
+  static constexpr int kBarDSIn = kBarDSStaged + 1;     // the other CTA's half has landed
+  static constexpr int kNumBars = kBarDSIn + 1;
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAbortOff = kTmemSlotOff + 4;
   static constexpr int kSmemBytes = kAbortOff + 4 + 1024;
@@ -141,6 +154,8 @@ enum : unsigned int {
   kSiteDQFull = 0x30B,
   kSiteDQEmpty = 0x30C,
   kSiteMmaDone = 0x30D,
+  kSiteDSStaged = 0x30E,
+  kSiteDSIn = 0x30F,
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -149,17 +164,16 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                "r"(d)
                : "memory");
 }
-// The same store into the other CTA of the pair (shared::cluster address).
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
-               "r"(c), "r"(d)
-               : "memory");
-}
-// Orders this thread's generic-proxy writes to shared memory of either CTA
-// of the cluster before later tensor-core reads of the same bytes.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// the other CTA's (shared::cluster address `dst`), completing on the barrier
+// at shared::cluster address `cluster_bar` in the receiving CTA.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "r"(src), "r"(bytes), "r"(cluster_bar)
+      : "memory");
 }
 
 __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
@@ -207,10 +221,14 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
     mbar_init(bar(C::kBarDPFull), 1);
     mbar_init(bar(C::kBarPFull), 16);   // one arrival per compute warp of both CTAs
     mbar_init(bar(C::kBarDSTmem), 16);
-    mbar_init(bar(C::kBarDSFull), 16);
+    // rank 0: the four warps of each CTA that store their own query half in
+    // place, and each CTA's exchange warp once the other half has landed
+    mbar_init(bar(C::kBarDSFull), 10);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQEmpty), 8);  // one arrival per drain warp of both CTAs
     mbar_init(bar(C::kBarMmaDone), 1);
+    mbar_init(bar(C::kBarDSStaged), 4);  // the staging warpgroup's warps
+    mbar_init(bar(C::kBarDSIn), 1);      // the exchange warp's arrival with the byte count
     fence_mbar_init();
   }
   // bias operands: A = all ones; the B tiles start at zero and the loader
@@ -321,6 +339,34 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
           const unsigned long long t0 = globaltimer();
           while (globaltimer() - t0 < 100000ull) __nanosleep(1000);
         }
+      }
+    } else if (warp == C::kExchangeWarp && lane == 0) {
+      // ----------------------------------------------------------- dS exchange
+      // Per tile: once the staging warpgroup has written this CTA's keys' dS
+      // for the other CTA's query half, send it (16 KB) into the other CTA's
+      // buffer of stage s at key rows [128 rank, +128); then wait for the
+      // other CTA's copy into this CTA's buffer and report it to rank 0.
+      const uint32_t peer = rank ^ 1u;
+      int sent = 0, received = 0;
+      for (int it = 0; it < n_iter; ++it) {
+        const int s = it % C::kStages;
+        if (!mbar_wait(bar(C::kBarDSStaged), it & 1, ctl, kSiteDSStaged)) break;
+        mbar_arrive_expect_tx(bar(C::kBarDSIn), C::kStageBytes);
+        const uint32_t dst = sbase + C::kYOff + s * C::kYBytes + rank * C::kStageBytes;
+        bulk_copy_to_peer(cluster_smem(dst, peer), sbase + C::kStageOff, C::kStageBytes,
+                          cluster_smem(bar(C::kBarDSIn), peer));
+        sent = it + 1;
+        if (!mbar_wait<true>(bar(C::kBarDSIn), it & 1, ctl, kSiteDSIn)) break;
+        received = it + 1;
+        mbar_arrive_cluster(bar0(C::kBarDSFull));
+      }
+      if (sent > received) {
+        // Give-up path: the other CTA's copy into this CTA may still land
+        // (bounded wait), and this CTA's own copy may still read the staging
+        // buffer (a bounded pause).
+        mbar_wait_drain(bar(C::kBarDSIn), (sent - 1) & 1);
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) __nanosleep(1000);
       }
     } else if (warp == C::kMmaWarp && rank == 0 && lane == 0) {
       // ----------------------------------------------------------- MMA issue
@@ -459,7 +505,7 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
     const f32x2 scale2 = f2_pack(p.scale, p.scale);
     // this thread's dS row in CTA wg's buffer: key row 128 rank + kr of 256
     const int ds_row = static_cast<int>(rank) * kBlock + kr;
-    const bool ds_local = wg == static_cast<int>(rank);
+    const bool ds_local = wg == static_cast<int>(rank);  // else staged and sent
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % C::kStages;
@@ -561,21 +607,23 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
       if (lane == 0) mbar_arrive_cluster(bar0(C::kBarDSTmem));
       // dS row of this key, this warpgroup's 64 queries, as an MN-major
       // operand with 128B swizzle: 128 bytes per key row, 16-byte chunk index
-      // XOR (key row mod 8); stage s of CTA wg (S^T_i and dP^T_i, the pair
-      // products that read that stage in both CTAs, are complete).
-      const uint32_t ds_addr = sbase + C::kYOff + s * C::kYBytes + ds_row * 128;
-      const uint32_t ds_dst = ds_local ? ds_addr : cluster_smem(ds_addr, static_cast<uint32_t>(wg));
+      // XOR (key row mod 8).  The CTA's own query half goes straight into
+      // its buffer (stage s: S^T_i and dP^T_i, the pair products that read
+      // that stage in both CTAs, are complete); the other half into the
+      // staging buffer in the same layout (key row 128 rank + kr has the same
+      // row mod 8 as kr), which the exchange warp sends on.
+      const uint32_t ds_dst = ds_local ? sbase + C::kYOff + s * C::kYBytes + ds_row * 128
+                                       : sbase + C::kStageOff + kr * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const uint32_t a = ds_dst + ((c8 ^ (ds_row & 7)) << 4);
-        if (ds_local)
-          st_shared_v4(a, dsw[4 * c8], dsw[4 * c8 + 1], dsw[4 * c8 + 2], dsw[4 * c8 + 3]);
-        else
-          st_cluster_v4(a, dsw[4 * c8], dsw[4 * c8 + 1], dsw[4 * c8 + 2], dsw[4 * c8 + 3]);
-      }
-      fence_proxy_async_cluster();
+      for (int c8 = 0; c8 < 8; ++c8)
+        st_shared_v4(ds_dst + ((c8 ^ (kr & 7)) << 4), dsw[4 * c8], dsw[4 * c8 + 1],
+                     dsw[4 * c8 + 2], dsw[4 * c8 + 3]);
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(bar0(C::kBarDSFull));
+      if (lane == 0) {
+        if (ds_local) mbar_arrive_cluster(bar0(C::kBarDSFull));
+        else mbar_arrive(bar(C::kBarDSStaged));
+      }
     }
 
     // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (already scaled)
