@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(bar0(C::kBarYFull + s));
+        if (lane == 0) mbar_arrive_peer(bar0(C::kBarYFull + s));
         // Q_i and dO_i, all 128 rows of this CTA's half of d, once dK of the
         // previous tile has read the single buffer
         if (it > 0) {
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
         sent = it + 1;
         if (!mbar_wait<true>(bar(C::kBarDSIn), it & 1, ctl, kSiteDSIn)) break;
         received = it + 1;
-        mbar_arrive_cluster(bar0(C::kBarDSFull));
+        mbar_arrive_peer(bar0(C::kBarDSFull));
       }
       if (sent > received) {
         // Give-up path: the other CTA's copy into this CTA may still land
@@ -431,15 +431,24 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
                       kk > 0 ? 1u : 0u);
       };
 
-      bool ok = wait(C::kBarKV, 0, kSiteKV);
+      // Per query tile i (stage s): dP^T_i; [P_i] dV_i; S^T_{i+1} (its
+      // softmax then overlaps dK_i and dQ_i; it overwrites P^T_i, which dV_i,
+      // issued before it, has read); [dS_i in tensor memory] dK_i; [dS_i in
+      // shared memory] dQ_i.  S^T_0 before the loop.
+      auto issue_s = [&](int it) {
+        const int s = it % C::kStages;
+        const bool r = wait(C::kBarYFull + s, (it / C::kStages) & 1, kSiteYFull);
+        if (!r) return false;
+        tc_fence_after();
+        issue_nt(sbase + C::kKOff, sbase + C::kYOff + s * C::kYBytes, C::kColS);
+        issue_bias(s, 0, C::kColS);
+        commit2(C::kBarSFull);
+        return true;
+      };
+      bool ok = wait(C::kBarKV, 0, kSiteKV) && issue_s(0);
       for (int it = 0; ok && it < n_iter; ++it) {
         const int s = it % C::kStages;
         const uint32_t y = sbase + C::kYOff + s * C::kYBytes;
-        if (!(ok = wait(C::kBarYFull + s, (it / C::kStages) & 1, kSiteYFull))) break;
-        tc_fence_after();
-        issue_nt(sbase + C::kKOff, y, C::kColS);
-        issue_bias(s, 0, C::kColS);
-        commit2(C::kBarSFull);
         if (it > 0) {  // dQ_{i-1}^T has left the dP^T columns
           if (!(ok = wait(C::kBarDQEmpty, (it - 1) & 1, kSiteDQEmpty))) break;
           tc_fence_after();
@@ -451,6 +460,7 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
         if (!(ok = wait(C::kBarPFull, it & 1, kSitePFull))) break;
         tc_fence_after();
         issue_tn(C::kColS, sbase + C::kXOff + C::kHalfBytes, C::kColDV, it > 0);
+        if (it + 1 < n_iter && !(ok = issue_s(it + 1))) break;
         if (!(ok = wait(C::kBarDSTmem, it & 1, kSiteDSTmem))) break;
         tc_fence_after();
         issue_tn(C::kColDP, sbase + C::kXOff, C::kColDK, it > 0);
@@ -486,7 +496,7 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
       // dQ_i^T has left tensor memory: the dP^T columns may be written again
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(bar0(C::kBarDQEmpty));
+      if (lane == 0) mbar_arrive_peer(bar0(C::kBarDQEmpty));
       float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.N + qb) * C::D + dcol;
 #pragma unroll
       for (int qc = 0; qc < 64; ++qc)
@@ -570,7 +580,7 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(bar0(C::kBarPFull));
+      if (lane == 0) mbar_arrive_peer(bar0(C::kBarPFull));
 
       // dS = scale * P dP'^T, dP'^T = dP^T - D by the bias MMA: to tensor
       // memory (for dK) and to CTA wg's shared memory (for dQ).
@@ -604,7 +614,7 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(bar0(C::kBarDSTmem));
+      if (lane == 0) mbar_arrive_peer(bar0(C::kBarDSTmem));
       // dS row of this key, this warpgroup's 64 queries, as an MN-major
       // operand with 128B swizzle: 128 bytes per key row, 16-byte chunk index
       // XOR (key row mod 8).  The CTA's own query half goes straight into
@@ -621,7 +631,7 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        if (ds_local) mbar_arrive_cluster(bar0(C::kBarDSFull));
+        if (ds_local) mbar_arrive_peer(bar0(C::kBarDSFull));
         else mbar_arrive(bar(C::kBarDSStaged));
       }
     }
