@@ -60,7 +60,70 @@ def parse():
                          "fixed-token sweep (B*N = 32768, H = 16, N = 1k..32k, d = 64/128, both masks)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (for profiler runs)")
+    ap.add_argument("--loop", choices=sorted(LOOP_ENTRIES),
+                    help="instead of the bench line: call one entry point warmup + steps times "
+                         "on --shape (L2 flushed before each call) and print its median time; "
+                         "the case a profiler captures")
+    ap.add_argument("--shape", default="2,16,4096,128", help="B,H,N,d for --loop")
+    ap.add_argument("--causal", action="store_true", help="causal mask for --loop")
+    ap.add_argument("--poly", type=int, default=None,
+                    help="exponentials per 8 on the FMA pipe in the forward (--loop)")
     return ap.parse_args()
+
+
+# --loop entry points: name -> (forward or backward, call)
+LOOP_ENTRIES = ("fwd", "fwd_2cta", "bwd", "bwd_2cta", "bwd_deterministic")
+
+
+def loop_arm(args):
+    """One entry point called repeatedly on one shape, each call timed with
+    CUDA events on the launching stream (L2 flushed before each call)."""
+    import torch
+
+    from exact_attention_98_gb300 import fa
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    B, H, N, d = (int(x) for x in args.shape.split(","))
+    causal = bool(args.causal)
+    scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", 0)
+    if args.poly is not None:
+        fa.fa_set_exp2_poly_share(args.poly)
+    q, k, v, do = (t.to(dev) for t in attention_inputs(B, H, N, d, seed=1))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    wsf = fa.fwd_workspace_for(q, causal)
+    ws = fa.workspace_for(q, deterministic=args.loop == "bwd_deterministic")
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    calls = {
+        "fwd": lambda: fa.fa_fwd(q, k, v, o, lse, scale, causal, wsf),
+        "fwd_2cta": lambda: fa.fa_fwd_2cta(q, k, v, o, lse, scale, causal),
+        "bwd": lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, ws),
+        "bwd_2cta": lambda: fa.fa_bwd_2cta(q, k, v, o, lse, do, dq, dk, dv, scale, causal, ws),
+        "bwd_deterministic": lambda: fa.fa_bwd_deterministic(q, k, v, o, lse, do, dq, dk, dv,
+                                                             scale, causal, ws),
+    }
+    call = calls[args.loop]
+    ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            ms.append(e0.elapsed_time(e1))
+    status = fa.fa_last_device_status()
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.status_string(status)}")
+    f_fwd, f_bwd = flops(B, H, N, d, causal)
+    f = f_fwd if args.loop.startswith("fwd") else f_bwd
+    med = statistics.median(ms)
+    print(json.dumps({"loop": args.loop, "shape": [B, H, N, d], "causal": causal,
+                      "poly": fa.fa_get_exp2_poly_share(), "ms": med,
+                      "tflops": f / med / 1e9, "calls": len(ms)}), flush=True)
 
 
 # DRAM traffic of one launch of the dominant kernel (the backward main kernel)
@@ -734,6 +797,9 @@ def sweep_arm(args):
 
 def main():
     args = parse()
+    if args.loop:
+        loop_arm(args)
+        return
     if args.sweep:
         sweep_arm(args)
         return

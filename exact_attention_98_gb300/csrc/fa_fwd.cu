@@ -719,7 +719,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         if constexpr (PAIR) {
           // one arrival per warp, on rank 0's barrier
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(cluster_smem(bar(C::kBarPFull + t), 0));
+          if (lane == 0) mbar_arrive_peer(cluster_smem(bar(C::kBarPFull + t), 0));
         } else {
           mbar_arrive(bar(C::kBarPFull + t));
         }
