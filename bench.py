@@ -593,6 +593,20 @@ def native_arm(args):
     del slots, hq, hk, hv, hdo, hdq, hdk, hdv, qd, kd, vd, dod, o, lse, dq, dk, dv, ws, wsf
     torch.cuda.empty_cache()
 
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    peak = peaks.get("bf16_tflops")
+    peak_note = "measured burst cuBLAS bf16 (MEASURED_PEAKS.json bf16_tflops)"
+    if peak is None:
+        peak, peak_note = 1900.0, "fallback 1.9 PFLOP/s bf16"
+
+    def roofline(kernel, achieved, **extra):
+        return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_note, **extra}
+
     # The B2 H16 N8192 causal backward, kernel events.
     bwd_causal = kernel_rates(fa, BWD_CAUSAL, True, flush, stream, fwd=False)
     # The B2 H16 N4096 step (non-causal) and the other entry points on it.
@@ -665,23 +679,28 @@ def native_arm(args):
     two_cta_extra = {"kernel_tflops": s_fwd / (statistics.median(pair_ms) * 1e-3) / 1e12,
                      "workload": "B2 H16 N4096 d128 non-causal",
                      "note": "fa_fwd_2cta: CTA pairs sharing M = 256 products"}
+
+    # The CTA-pair backward (fa_bwd_2cta), main kernel events.
+    ws2 = fa.workspace_for(sq)
+    pair_bwd_ms = []
+    fa.fa_timing_enable(True)
+    for i in range(3 + 5):
+        flush.zero_()
+        fa.fa_bwd_2cta(sq, sk, sv, so, slse, sdo, sdq, sdk, sdv, 1.0 / math.sqrt(sd), False, ws2)
+        if i >= 3:
+            pair_bwd_ms.append(fa.fa_timing_last_ms(fa.KERNEL_BWD_MAIN))
+    fa.fa_timing_enable(False)
+    if fa.fa_last_device_status() != fa.FA_OK:
+        raise RuntimeError("device status after the CTA-pair backward")
+    del ws2
+    pb = s_bwd / (statistics.median(pair_bwd_ms) * 1e-3) / 1e12
+    two_cta_bwd_extra = {"kernel_tflops": pb, "workload": "B2 H16 N4096 d128 non-causal",
+                         "roofline": roofline("fa_bwd_pair_kernel", pb),
+                         "note": "fa_bwd_2cta: CTA pairs sharing cta_group::2 products, dQ "
+                                 "added once per 256 keys"}
     del sq, sk, sv, sdo, so, slse, sdq, sdk, sdv, o8, lse8
     clocks.stop()
     clk = clocks.summary()
-
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except Exception:
-        pass
-    peak = peaks.get("bf16_tflops")
-    peak_note = "measured burst cuBLAS bf16 (MEASURED_PEAKS.json bf16_tflops)"
-    if peak is None:
-        peak, peak_note = 1900.0, "fallback 1.9 PFLOP/s bf16"
-
-    def roofline(kernel, achieved, **extra):
-        return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_note, **extra}
 
     traffic_ok = (NCU_TRAFFIC["bytes"] is not None and
                   kernel_sources_sha256() == NCU_TRAFFIC["sources_sha256"])
@@ -723,6 +742,7 @@ def native_arm(args):
         "deterministic": deterministic_extra,
         "fp8_forward": fp8_extra,
         "two_cta_forward": two_cta_extra,
+        "two_cta_backward": two_cta_bwd_extra,
         "roofline": roofline(
             "fa_bwd_kernel<128>", bwd_main_tf,
             traffic=NCU_TRAFFIC["bytes"] if traffic_ok else None,

@@ -181,20 +181,14 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
-// Arrival (release, cluster scope) on a barrier given by its shared::cluster
-// address (possibly in the other CTA).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
-}
-
 // Arrival on a barrier of the other CTA of a pair (shared::cluster address)
 // with the default semantics of mbarrier.arrive (release at CTA scope), the
 // form tcgen05 pipelines use to hand data a thread has finished writing
 // (tensor memory after tcgen05.wait::st and tcgen05.fence::before_thread_sync,
 // or shared memory after fence.proxy.async) to the CTA that issues the pair's
-// MMAs.  Measured on GB300 at a few hundred cycles less per arrival than the
-// cluster-scope release of mbar_arrive_cluster.
+// MMAs.  In the pair backward, arrivals with a cluster-scope release
+// (mbarrier.arrive.release.cluster) measured 600-1300 cycles each on the
+// arriving warp, and the kernel 1.5x slower with them.
 __device__ __forceinline__ void mbar_arrive_peer(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }

@@ -56,6 +56,40 @@ def test_tail_split_with_ragged_keys(causal):
     compare_fwd(2, 16, 4000, 128, causal, full_heads=1, rows_per_head=128)
 
 
+def test_forward_splits_only_in_a_given_workspace():
+    """B2 H16 N4096 non-causal: 512 work items on the SMs leave a partial
+    last round.  Without a workspace fa_fwd launches one kernel and
+    allocates nothing; with one it splits that round (forward + merge).  Both
+    meet the forward's bounds on head 0 and stay within rounding of each
+    other."""
+    from exact_attention_98_gb300 import fa
+    from exact_attention_98_gb300.inputs import attention_inputs
+    import oracle
+    from parity import check_lse, check_o, to64
+
+    B, H, N, d = 2, 16, 4096, 128
+    q, k, v, _ = attention_inputs(B, H, N, d, seed=4, with_dout=False)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    scale = 1 / math.sqrt(d)
+    outs = []
+    for ws in (None, fa.fwd_workspace_for(qd, False)):
+        o, lse = torch.empty_like(qd), torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        free0, n0 = torch.cuda.mem_get_info()[0], fa.fa_launch_count()
+        fa.fa_fwd(qd, kd, vd, o, lse, scale, False, ws)
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert fa.fa_launch_count() - n0 == (1 if ws is None else 2)
+        outs.append((to64(o), to64(lse)))
+    assert fa.fa_last_device_status() == fa.FA_OK
+    o_ref, l_ref = oracle.fwd_head(*(t[0, 0].double().numpy() for t in (q, k, v)), scale, False)
+    for o, lse in outs:
+        check_o(o[0, 0], o_ref, "head 0")
+        check_lse(lse[0, 0], l_ref, "head 0")
+    assert np.abs(outs[0][0] - outs[1][0]).max() <= 1e-2
+    assert np.abs(outs[0][1] - outs[1][1]).max() <= 1e-4
+
+
 @pytest.mark.parametrize("N", [1, 5, 129])
 def test_fp8_degenerate_lengths(N):
     """FP8 forward on one key, a few keys and one key past a tile: V^T's
@@ -101,6 +135,7 @@ def test_launch_counter_per_call():
 
     # 2 query blocks of 256 rows x 2 heads: fewer than the SMs, never split
     assert count(lambda: fa.fa_fwd(q, k, v, o, lse, scale, False)) == 1
+    assert fa.fa_fwd_workspace_bytes(B, H, N, d, False) == 0
     ws = fa.workspace_for(q)
     assert count(lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, False, ws)) == 3
     wsd = fa.workspace_for(q, deterministic=True)
@@ -112,4 +147,5 @@ def test_launch_counter_per_call():
     ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
     assert count(lambda: fa.fa_fwd_fp8(q, k, v, o, lse, scale, False, True, ws8)) == 3
     assert count(lambda: fa.fa_fwd_2cta(q, k, v, o, lse, scale, False)) == 1
+    assert count(lambda: fa.fa_bwd_2cta(q, k, v, o, lse, do, dq, dk, dv, scale, False, ws)) == 3
     assert fa.fa_last_device_status() == fa.FA_OK
