@@ -128,14 +128,17 @@ def loop_arm(args):
 
 # DRAM traffic of one launch of the dominant kernel (the backward main kernel)
 # on this workload: dram__bytes_read.sum + dram__bytes_write.sum from one
-# `ncu --set full` capture (cold cache).  It describes the kernel built from
-# the sources whose digest is recorded with it, and is reported as null as
-# soon as any of them changes.
+# `ncu --set full` capture (cold cache) of B1 H4 N32768 d128 (207763200 +
+# 90309632 bytes), times 4 for the 16 independent heads of the headline (the
+# full-size launch is too large to capture).  It describes the kernel built
+# from the sources whose digest is recorded with it, and is reported as null
+# as soon as any of them changes.
 NCU_TRAFFIC = {
     "kernel": "fa_bwd_kernel<128>",
     "workload": WORKLOAD_NAME,
-    "bytes": None,
-    "sources_sha256": "",
+    "bytes": 4 * (207763200 + 90309632),
+    "captured": "B1 H4 N32768 d128, scaled by 4",
+    "sources_sha256": "7ed55919b2edab01bf9f8c4a9eac56a415eff874b2d179b627624df57a52d806",
 }
 KERNEL_SOURCES = ("fa_bwd.cu", "fa_device.cuh", "fa_kernels.h", "exp2_poly_coeffs.h")
 
@@ -746,7 +749,11 @@ def native_arm(args):
         "roofline": roofline(
             "fa_bwd_kernel<128>", bwd_main_tf,
             traffic=NCU_TRAFFIC["bytes"] if traffic_ok else None,
-            traffic_unit="bytes per launch (ncu, cold cache)"),
+            traffic_unit="bytes per launch (ncu, cold cache; " + NCU_TRAFFIC["captured"] + ")",
+            algorithmic_bytes=(4 * 2 * B * H * N * d  # Q, K, V, dO read
+                               + 2 * 2 * B * H * N * d  # dK, dV written
+                               + 2 * 4 * B * H * N * d  # fp32 dQ accumulator read and written
+                               + 2 * 4 * B * H * N)),  # LSE, D read
         "roofline_fwd": roofline("fa_fwd_kernel<128>", fwd_tf),
         "roofline_fwd_causal": roofline("fa_fwd_kernel<128>", causal_extra["fwd_tflops"]),
         "clocks": clk,
