@@ -702,8 +702,15 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
             float x0, x1, p0, p1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(r[ch][e]), __uint_as_float(r[ch][e + 1])), c2, negm2),
                       x0, x1);
-            if (!edge && ((ch * 32 + e) & 7) < POLY) {
+            // element e's position in its group of 8 (even): elements at
+            // positions below POLY take the polynomial, a pair at a time
+            // where both do
+            const int pos = (ch * 32 + e) & 7;
+            if (!edge && pos + 1 < POLY) {
               exp2_poly2(x0, x1, p0, p1);
+            } else if (!edge && pos < POLY) {
+              p0 = exp2_poly(x0);
+              p1 = ex2_mufu(x1);
             } else {
               p0 = ex2_mufu(x0);
               p1 = ex2_mufu(x1);
