@@ -16,9 +16,9 @@
 // and does its own arithmetic while sharing a warp scheduler with two
 // softmax warps, and in steady state the tensor pipe runs at about 70% of
 // its rate.  Exponentials moved to the FMA pipe add softmax instructions to
-// that competition: measured on B2 H16 N4096 d128, the
-// forward ran at 1073 TFLOP/s with every exponential on MUFU and at 861 /
-// 859 / 699 TFLOP/s with 1 / 2 / 3 of every 8 on the FMA pipe, so the
+// that competition: measured on B2 H16 N8192 d128, the
+// forward ran at 1515 TFLOP/s with every exponential on MUFU and at 1089 /
+// 1086 / 885 TFLOP/s with 1 / 2 / 3 of every 8 on the FMA pipe, so the
 // default share is 0; the other shares stay instantiated and selectable.
 //
 // Persistent CTAs (one per SM) walk the work items; an item is two 128-row
@@ -199,8 +199,9 @@ __device__ __forceinline__ int fwd_item_index(int r) {
   return r * G + ((r & 1) ? G - 1 - c : c);
 }
 
-// POLY: of every 8 exponentials of the softmax, this many are evaluated by
-// exp2_poly on the FMA pipe, the rest by MUFU ex2.
+// POLY: of every 8 exponentials of the softmax (a non-edge row tile), those
+// at positions 0 .. POLY-1 are evaluated by the polynomial on the FMA pipe
+// (exp2_poly2 for a pair, exp2_poly for a lone one), the rest by MUFU ex2.
 template <int D, int POLY, bool FP8, bool PAIR = false>
 __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p) {
