@@ -79,7 +79,15 @@ struct BwdCfg {
   static constexpr int kMmaWarp = 13;
   static constexpr int kTileBytes = kBlockM * D * 2;
   static constexpr int kHalfBytes = kBlockM * 64 * 2;
-  static constexpr int kStages = 2;
+  // Q_i/dO_i stages: two at d = 128 (all shared memory allows), three at
+  // d = 64, where the next tile's S^T is issued right after dV_i (see the
+  // MMA loop) and its Q tile needs the longer lead.
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  // The next tile's S^T right after dV_i instead of after dQ_i: at d = 64,
+  // where dQ_i has tensor-memory columns of its own (so dP^T_{i+1} does not
+  // wait for its drain) and a third stage gives the next Q tile its lead.
+  // At d = 128 tensor memory is full and measured slower (8%).
+  static constexpr bool kEarlyS = (D == 64);
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTileBytes;
   static constexpr int kQOff = 2 * kTileBytes;                     // kStages tiles
@@ -95,10 +103,13 @@ struct BwdCfg {
   static constexpr int kDsumOff = kBiasOff + kStages * 2 * kBiasTileBytes - kStages * kBlockM * 4;
   static constexpr int kDsTileBytes = kBlockN * kBlockM * 2;  // dS is 128 x 128 for any d
   // At d = 128 the dS tile reuses the dO_i buffer; at d = 64 that buffer is
-  // too small and dS gets one buffer per stage.
+  // too small and dS alternates between two buffers of its own (dS_{i+2}
+  // is written after dP^T_{i+2} completes, and dQ_i, issued before it, has
+  // read dS_i by then).
   static constexpr int kDsOff = kDsumOff + kStages * kBlockM * 4;
   static constexpr bool kDsInDO = (D == 128);
-  static constexpr int kDsBytes = kDsInDO ? 0 : kStages * kDsTileBytes;
+  static constexpr int kDsBufs = 2;
+  static constexpr int kDsBytes = kDsInDO ? 0 : kDsBufs * kDsTileBytes;
   // dQ staging: d/16 chunks of 128 rows x 16 fp32 (64-byte swizzled rows),
   // the first half in the stage's Q buffer, the second in its dO buffer.
   static constexpr int kDqCols = 16;
@@ -127,16 +138,21 @@ struct BwdCfg {
   static constexpr int kTmemSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAbortOff = kTmemSlotOff + 4;
   static constexpr int kSmemBytes = kAbortOff + 4 + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColDP = 128;  // dP^T, dS^T, then dQ
+  static constexpr uint32_t kColDP = 128;  // dP^T, dS^T, then (d = 128) dQ^T
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
+  // dQ_i: at d = 128 over the dP^T columns (tensor memory is full); at
+  // d = 64 in the free columns after dK
+  static constexpr uint32_t kColDQ = (D == 128) ? kColDP : 256 + 2 * D;
+  static_assert(kColDQ + (D == 128 ? kBlockM : D) <= 512, "tensor-memory columns");
   static constexpr int kDrainBarrier = 1;  // named barrier of the d = 64 drain (0 is __syncthreads)
   static_assert(kDrainBarrier > 0, "named barrier 0 is the CTA barrier");
-  // Shared-memory offset of stage s's dS tile.
-  static __device__ __forceinline__ int ds_off(int s) {
-    return (D == 128) ? kDOOff + s * kTileBytes : kDsOff + s * kDsTileBytes;
+  // Shared-memory offset of query tile it's dS tile (stage s = it % kStages).
+  static __device__ __forceinline__ int ds_off(int it) {
+    return (D == 128) ? kDOOff + (it % kStages) * kTileBytes : kDsOff + (it % kDsBufs) * kDsTileBytes;
   }
   // Tensor-memory column (relative to the S^T or dP^T region) of the packed
   // bf16 pair for query columns 16*kk.. of the tile: warpgroup kk/4 owns
@@ -341,23 +357,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           const uint64_t ds_desc = step(dsd, kk * 2048);
           const uint64_t k_desc = step(kd, kk * 2048);
           if (C::kDqTransposed)
-            mma_ss(tmem_base + C::kColDP, k_desc, ds_desc, kIdescQ, kk > 0 ? 1u : 0u);
+            mma_ss(tmem_base + C::kColDQ, k_desc, ds_desc, kIdescQ, kk > 0 ? 1u : 0u);
           else
-            mma_ss(tmem_base + C::kColDP, ds_desc, k_desc, kIdescQ, kk > 0 ? 1u : 0u);
+            mma_ss(tmem_base + C::kColDQ, ds_desc, k_desc, kIdescQ, kk > 0 ? 1u : 0u);
         }
       };
 
+      // S^T_i = K Q_i^T and its bias, once stage s of Q_i has landed.
+      auto issue_s = [&](int it) -> bool {
+        const int s = it % C::kStages;
+        if (!mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull)) return false;
+        tc_fence_after();
+        issue_nt(k_smem, sbase + C::kQOff + s * C::kTileBytes, C::kColS);
+        issue_bias(2 * s, C::kColS);
+        mma_commit(bar(C::kBarSFull));
+        return true;
+      };
       bool ok = mbar_wait(bar(C::kBarKV), 0, ctl, kSiteKV);
+      if (C::kEarlyS && ok) ok = issue_s(0);
       for (int it = 0; ok && it < n_iter; ++it) {
         const int s = it % C::kStages;
         const uint32_t q_s = sbase + C::kQOff + s * C::kTileBytes;
         const uint32_t do_s = sbase + C::kDOOff + s * C::kTileBytes;
-        if (!(ok = mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull))) break;
-        tc_fence_after();
-        issue_nt(k_smem, q_s, C::kColS);
-        issue_bias(2 * s, C::kColS);
-        mma_commit(bar(C::kBarSFull));
-        if (it > 0) {
+        if (!C::kEarlyS && !(ok = issue_s(it))) break;
+        if (!C::kEarlyS && it > 0) {  // dQ_{i-1}^T has left the dP^T columns
           if (!(ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl, kSiteDQEmpty))) break;
           tc_fence_after();
         }
@@ -368,13 +391,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_after();
         issue_tn(C::kColS, do_s, C::kColDV, it > 0);
         mma_commit(bar(C::kBarDVDone));
+        // S^T_{i+1} over P^T_i, which dV_i (issued before it) has read.
+        if (C::kEarlyS && it + 1 < n_iter && !(ok = issue_s(it + 1))) break;
         // dK_i needs dS^T_i in tensor memory only; dQ_i also needs its copy in
         // shared memory, which the compute warps write while dK_i runs.
         if (!(ok = mbar_wait(bar(C::kBarDSTmem), it & 1, ctl, kSiteDSTmem))) break;
         tc_fence_after();
         issue_tn(C::kColDP, q_s, C::kColDK, it > 0);
         if (!(ok = mbar_wait(bar(C::kBarDSFull), it & 1, ctl, kSiteDSFull))) break;
-        issue_dq(sbase + C::ds_off(s));
+        if (C::kEarlyS && it > 0) {  // the drain has read dQ_{i-1} from its columns
+          if (!(ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl, kSiteDQEmpty))) break;
+          tc_fence_after();
+        }
+        issue_dq(sbase + C::ds_off(it));
         mma_commit(bar(C::kBarDQFull));
         // With the transposed dQ the drain needs no shared memory: dQ_i was
         // the last reader of the stage.  Otherwise the drain returns it.
@@ -389,7 +418,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int quarter = warp & 3;
     const int qr = quarter * 32 + lane;  // query row within the tile
     const bool leader = (warp == C::kDrainWarp0 && lane == 0);
-    const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDP;
+    const uint32_t t_dq = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + C::kColDQ;
     if constexpr (C::kDqTransposed) {
       // thread = d index (lane of dQ_i^T); each warp adds 32 consecutive
       // floats of one query row per reduction
@@ -597,7 +626,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // dS tile laid out as an MN-major operand with 128B swizzle:
       // [query half][key row][64 queries], 16-byte chunk index XOR (key row
       // mod 8).
-      uint8_t* ds_tile = smem + C::ds_off(s);
+      uint8_t* ds_tile = smem + C::ds_off(it);
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         const int q = wg * 64 + c8 * 8;  // first query of this 16-byte chunk
