@@ -15,11 +15,11 @@
 //   tensor memory (512 columns x 128 lanes)
 //     [  0,128)  S^T = K Q_i^T (fp32, lane = key) -> P^T (bf16)
 //     [128,256)  dP^T = V dO_i^T (fp32, lane = key) -> dS^T (bf16)
-//                -> then dQ_i: d = 64, dQ_i = dS K (fp32, lane = query, d
-//                columns); d = 128, dQ_i^T = K^T dS^T (lane = d, 128 query
+//                -> then, at d = 128, dQ_i^T = K^T dS^T (lane = d, 128 query
 //                columns)
 //     [256,256+d)      dV accumulator (lane = key)
 //     [256+d,256+2d)   dK accumulator (lane = key)
+//     [384,448)        d = 64 only: dQ_i = dS K (fp32, lane = query)
 //   Each compute warpgroup owns 64 query columns of S^T and dP^T and packs
 //   its bf16 P^T / dS^T into the first 32 of them, so neither warpgroup
 //   overwrites fp32 values the other has not read yet.  The dQ product reads
@@ -27,9 +27,12 @@
 //   consumed it; at d = 64 in its own buffer).  dQ_i lands in the dP^T
 //   columns, so draining it overlaps the next tile's S^T product and softmax.
 //
-// Per query tile i (MMA issue order):
+// Per query tile i (MMA issue order), d = 128:
 //   S^T = K Q_i^T ; [dQ_{i-1} drained] dP^T = V dO_i^T ;
 //   [P^T ready] dV += P^T dO_i ; [dS ready] dK += dS^T Q_i ; dQ_i = dS K
+// d = 64 (dQ in columns of its own, three Q/dO stages): the next tile's S^T
+// follows dV_i, so its exponentials overlap dK_i and dQ_i:
+//   dP^T ; [P^T] dV ; S^T_{i+1} ; [dS] dK ; [dQ_{i-1} drained] dQ_i
 // with P^T = exp2(S^T c - LSE_i log2 e) and dS = scale * P (dP - D_i): the
 // softmax scale is folded into dS, so dK and dQ come out scaled.
 //
