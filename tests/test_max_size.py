@@ -7,6 +7,7 @@ first and the last head (the largest offsets) are compared with the fp64
 oracle on sampled rows: O and LSE element by element, dQ rows by relative
 Frobenius error; dK and dV of those heads through the properties that hold
 at any size (dK rows sum to zero, dV rows sum to the dO rows).  The 2-CTA
+backward must stay within rounding of the backward on those heads, the 2-CTA
 forward must equal the forward bit for bit, and the FP8 forward must stay
 within its bounds."""
 import math
@@ -63,7 +64,17 @@ def test_forward_backward(big):
         assert np.abs(dkh.sum(axis=0)).max() <= 2e-2 * np.abs(dkh).sum(axis=0).max(), what
         dv_err = np.abs(dvh.sum(axis=0) - doh.sum(axis=0)).max()
         assert dv_err <= 2e-2 * np.abs(doh).sum(axis=0).max(), what
-    del dq, dk, dv
+    # the 2-CTA backward on the same inputs: within rounding of fa_bwd on the
+    # first and last heads (dK, dV in full; dQ on the sampled rows, which the
+    # oracle bounds as above)
+    dq2, dk2, dv2 = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale, two_cta=True)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    for h in (0, H - 1):
+        rows = sampled_rows(N, 64, 0, h, H)
+        for a, b in ((dk, dk2), (dv, dv2)):
+            assert rel_fro(head64(b, h), head64(a, h)) <= 2e-3, h
+        assert rel_fro(to64(dq2[0, h])[rows], to64(dq[0, h])[rows]) <= 2e-3, h
+    del dq, dk, dv, dq2, dk2, dv2
     # the 2-CTA forward: the same products and per-row arithmetic
     o2, lse2 = fa.forward(q, k, v, causal=True, scale=scale, two_cta=True)
     assert fa.fa_last_device_status() == fa.FA_OK
