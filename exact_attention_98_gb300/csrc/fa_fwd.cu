@@ -657,22 +657,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
     uint32_t phase = 0;
     int pvc = 0;
     int sct = 0;  // rotating S buffers: this tile's S products so far
-    // Rotating S buffers: o_full of this tile completes once per P V, and
-    // its phases are observed one by one, in order (o_seen of them so far).
-    // Before releasing its P number k this warpgroup observes P V number
-    // k - 1, so when it waits for phase k the barrier cannot have completed
-    // phase k + 1 (P V number k + 1 needs P number k + 1, not yet released):
-    // a parity wait never confuses a phase with the one two steps later.
-    int o_seen = 0;
-    auto wait_o = [&](int upto) -> bool {
-      while (o_seen <= upto) {
-        const bool r = __all_sync(0xffffffffu, mbar_wait(bar(C::kBarOFull + t), o_seen & 1, ctl, kSiteOFull));
-        if (!r) return false;
-        ++o_seen;
-      }
-      tc_fence_after();
-      return true;
-    };
     // rotating S buffers: S products of the CTA before this item
     int s_before = 0;
     bool ok = true;
@@ -774,7 +758,10 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
           if (C::kRot && j > 0) {
             // rotating S buffers: P V of this tile's previous P may still be
             // accumulating into O (S runs ahead of it); wait for it
-            if (!(ok = wait_o(pvc - 1))) break;
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar(C::kBarOFull + t), (pvc - 1) & 1, ctl, kSiteOFull));
+            if (!ok) break;
+            tc_fence_after();
           }
           if (j > 0) {
             const f32x2 a2 = f2_pack(alpha, alpha);
@@ -857,9 +844,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         }
         }
         tmem_st_wait();
-        // rotating S buffers: P V of the previous P done before this P is
-        // released (keeps o_full at most one phase ahead of o_seen)
-        if (C::kRot && pvc > 0 && !(ok = wait_o(pvc - 1))) break;
         tc_fence_before();
         if constexpr (PAIR) {
           // one arrival per warp, on rank 0's barrier
@@ -882,7 +866,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       // next item's first P V overwrite O_t.
       if (ok) {
         if constexpr (C::kRot) {
-          ok = wait_o(pvc - 1);
+          ok = mbar_wait(bar(C::kBarOFull + t), (pvc - 1) & 1, ctl, kSiteOFull);
         } else {
           ok = mbar_wait(bar(C::kBarOFull + t), (phase >> 1) & 1u, ctl, kSiteOFull);
           phase ^= 2u;
