@@ -66,11 +66,8 @@ struct FwdCfg {
   static_assert(!PAIR || (D == 128 && !FP8), "pair forward: bf16, d = 128");
   static constexpr int kThreads = 384;
   static constexpr int kLaunchRegs = 168;   // what ptxas must allocate (checked at launch)
-  // rotating S buffers (d = 64, below): the issuing warp keeps two cursors
-  // over the work and gets more of the registers
-  static constexpr bool kRotRegs = (D == 64 && !FP8 && !PAIR);
-  static constexpr int kSoftmaxRegs = kRotRegs ? 200 : 208;  // 2 x 128 threads
-  static constexpr int kOtherRegs = kRotRegs ? 104 : 88;     // 128 threads (load, MMA): no spills
+  static constexpr int kSoftmaxRegs = 208;  // 2 x 128 threads
+  static constexpr int kOtherRegs = 88;     // 128 threads (load, MMA): no spills
   static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
   static constexpr int kProducerWarp = 8;
@@ -94,13 +91,7 @@ struct FwdCfg {
   static constexpr int kBarFull = 2;
   static constexpr int kBarEmpty = 2 + kSlots;
   static constexpr int kBarSFull = 2 + 2 * kSlots;
-  // s_full barriers per query tile: one; with rotating S buffers three, used
-  // in turn (the tile's running S count mod 3), because up to three of a
-  // tile's S products can complete before its softmax warpgroup waits for the
-  // first of them (while it writes an item's epilogue), and a barrier may
-  // complete at most one phase between two waits on it
-  static constexpr int kSFullPerTile = kRotRegs ? 3 : 1;
-  static constexpr int kBarPFull = kBarSFull + 2 * kSFullPerTile;
+  static constexpr int kBarPFull = kBarSFull + 2;
   static constexpr int kBarOFull = kBarPFull + 2;
   static constexpr int kBarMmaDone = kBarOFull + 2;
   static constexpr int kNumBars = kBarMmaDone + 1;
@@ -110,15 +101,8 @@ struct FwdCfg {
   static constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static constexpr uint32_t kTmemCols = 512;
-  // Rotating S buffers (bf16, d = 64, one CTA): three 128-column S buffers
-  // shared by the two query tiles, so that the issuing warp can run up to
-  // three S products ahead of the P V products (S number n goes to buffer
-  // n mod 3, which the P V product of S number n - 3 has finished reading).
-  static constexpr bool kRot = kRotRegs;
-  static constexpr int kSBufs = kRot ? 3 : 2;
-  static constexpr uint32_t kSCol0 = 0;                 // S buffer b at b * 128
-  static constexpr uint32_t kOCol0 = 128 * kSBufs;      // O_t at kOCol0 + t * D
-  static_assert(kOCol0 + 2 * D <= kTmemCols, "tensor-memory columns");
+  static constexpr uint32_t kSCol0 = 0;    // S_t / P_t at t * 128
+  static constexpr uint32_t kOCol0 = 256;  // O_t at 256 + t * D
 };
 
 // Wait-site codes recorded on a timeout (bits 8..23 of the status word).
@@ -249,8 +233,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       mbar_init(bar(C::kBarFull + s), 1);
       mbar_init(bar(C::kBarEmpty + s), 1);
     }
-    for (int i = 0; i < 2 * C::kSFullPerTile; ++i) mbar_init(bar(C::kBarSFull + i), 1);
     for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarSFull + t), 1);
       // pair mode: one arrival per softmax warp of both CTAs (on rank 0's)
       mbar_init(bar(C::kBarPFull + t), PAIR ? 8 : kBlockM);
       mbar_init(bar(C::kBarOFull + t), 1);
@@ -439,10 +423,10 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         return desc;
       };
       auto step = [](uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); };
-      auto issue_s = [&](int t, int kslot, int buf) {
+      auto issue_s = [&](int t, int kslot) {
         const uint64_t a0 = opaque(sdesc_sw128(q_smem + t * C::kTileBytes, 16, 1024));
         const uint64_t b0 = opaque(sdesc_sw128(ring + kslot * C::kSlotBytes, 16, 1024));
-        const uint32_t dcol = tmem_base + C::kSCol0 + buf * 128;
+        const uint32_t dcol = tmem_base + C::kSCol0 + t * 128;
         if constexpr (FP8) {
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk)  // 32 e4m3 = 32 bytes of the 128-byte row
@@ -464,8 +448,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       // 32-bit column) sits in tensor memory over S_t; V is MN-major in shared
       // memory (d contiguous), 8-key groups 1024 B apart, 64-wide d blocks
       // kHalfBytes apart (pair mode: one 64-wide block per CTA).
-      auto issue_pv = [&](int t, int vslot, bool accumulate, int buf) {
-        const uint32_t acol = tmem_base + C::kSCol0 + buf * 128;
+      auto issue_pv = [&](int t, int vslot, bool accumulate) {
+        const uint32_t acol = tmem_base + C::kSCol0 + t * 128;
         const uint32_t dcol = tmem_base + C::kOCol0 + t * D;
         if constexpr (FP8) {
           // P_t as e4m3, four per 32-bit column: 32 keys = 8 columns per MMA;
@@ -489,86 +473,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         }
       };
 
-      if constexpr (C::kRot) {
-        // Rotating S buffers: the CTA's products in one sequence over its
-        // items, (j, t) in the order S_0(j), S_1(j) (a tile whose key range
-        // ends earlier is skipped).  Two cursors walk it: cs the next S to
-        // issue, cp the next P V.  S number n is issued once P V number
-        // n - 3 has been (its buffer is then free), so up to three S
-        // products run ahead of the P V products and a softmax warpgroup
-        // finds its next S done when it releases its P.  Every P V commits
-        // o_full of its tile (the softmax waits on it before it rescales O
-        // or reads O for the epilogue).
-        // A cursor keeps of its item only the key-tile counts of the two
-        // query tiles (nkv0, nkv1; nmax is their max).
-        struct Cursor {
-          int round, j, t, base, items, nkv0, nkv1;
-          bool done;
-          __device__ __forceinline__ int nmax() const { return max(nkv0, nkv1); }
-          __device__ __forceinline__ int nkv(int tt) const { return tt ? nkv1 : nkv0; }
-        };
-        auto settle = [&](Cursor& c) {  // the first (j, t) of the item at c.round or later
-          for (;;) {
-            const int wi = fwd_item_index(c.round);
-            if (wi >= p.n_items) { c.done = true; return; }
-            const FwdItem it = fwd_item(p, wi, n_ktiles);
-            c.nkv0 = it.nkv0;
-            c.nkv1 = it.nkv1;
-            if (it.nmax > 0) { c.j = 0; c.t = it.nkv0 > 0 ? 0 : 1; return; }
-            ++c.round;
-          }
-        };
-        auto advance = [&](Cursor& c) {
-          for (;;) {
-            if (c.t == 0) { c.t = 1; } else { c.t = 0; ++c.j; }
-            if (c.j >= c.nmax()) {
-              c.base += 2 * c.nmax();
-              ++c.items;
-              ++c.round;
-              settle(c);
-              return;
-            }
-            if (c.j < c.nkv(c.t)) return;
-          }
-        };
-        Cursor cs{0, 0, 0, 0, 0, 0, 0, false}, cp{0, 0, 0, 0, 0, 0, 0, false};
-        settle(cs);
-        settle(cp);
-        int n_s = 0, n_pv = 0, np0 = 0, np1 = 0, sc0 = 0, sc1 = 0;
-        bool ok = true;
-        while (ok && !cp.done) {
-          while (!cs.done && n_s < n_pv + 3) {
-            const int kidx = cs.base + 2 * cs.j;
-            const bool first = cs.j == 0 && (cs.t == 0 || cs.nkv0 == 0);
-            if (first && !(ok = wait(bar(C::kBarQFull), cs.items & 1, kSiteQFull))) break;
-            if (!(ok = wait(bar(C::kBarFull + slot_of(kidx)), parity_of(kidx), kSiteKFull))) break;
-            tc_fence_after();
-            issue_s(cs.t, slot_of(kidx), n_s % 3);
-            commit(C::kBarSFull + 3 * cs.t + (cs.t ? sc1++ : sc0++) % 3);
-            // the last S reading K_j, and the item's last S (Q is free then)
-            const bool k_done = cs.t == 1 || cs.j >= cs.nkv1;
-            const int items_before = cs.items;
-            advance(cs);
-            if (k_done) commit(C::kBarEmpty + slot_of(kidx));
-            if (cs.done || cs.items != items_before) commit(C::kBarQEmpty);
-            ++n_s;
-          }
-          if (!ok) break;
-          const int vidx = cp.base + 2 * cp.j + 1;
-          if (!(ok = wait(bar(C::kBarFull + slot_of(vidx)), parity_of(vidx), kSiteVFull))) break;
-          if (!(ok = wait(bar(C::kBarPFull + cp.t), (cp.t ? np1 : np0) & 1, kSitePFull))) break;
-          if (cp.t) ++np1; else ++np0;
-          tc_fence_after();
-          issue_pv(cp.t, slot_of(vidx), cp.j > 0, n_pv % 3);
-          commit(C::kBarOFull + cp.t);
-          if (cp.t == 1 || cp.j >= cp.nkv1) commit(C::kBarEmpty + slot_of(vidx));
-          advance(cp);
-          ++n_pv;
-        }
-        // Every MMA this warp issued must finish before tensor memory is freed.
-        mma_commit<kWarpIssue>(bar(C::kBarMmaDone));
-        mbar_wait_drain(bar(C::kBarMmaDone), 0);
-      } else {
       // Per item, with a running load index `base` and running P counts
       // np0, np1 (the parity of the p_full barriers) across items:
       //   S_0(0), S_1(0) | j: [P_0(j)] O_0 += P_0(j) V_j, S_0(j+1); [P_1(j)] ...
@@ -589,7 +493,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
           if (item.nkv(t) > 0) {
-            issue_s(t, slot_of(base), t);
+            issue_s(t, slot_of(base));
             commit(C::kBarSFull + t);
           }
         if (item.nmax == 1) commit(C::kBarQEmpty);  // every S of the item issued
@@ -608,7 +512,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
             if (!ok) break;
             if (t) ++np1; else ++np0;
             tc_fence_after();
-            issue_pv(t, slot_of(vidx), j > 0, t);
+            issue_pv(t, slot_of(vidx), j > 0);
             if (j == item.nkv(t) - 1) {
               commit(C::kBarOFull + t);
             } else {
@@ -618,7 +522,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
                 tc_fence_after();
                 k_next_ready = true;
               }
-              issue_s(t, slot_of(kidx), t);
+              issue_s(t, slot_of(kidx));
               commit(C::kBarSFull + t);
             }
           }
@@ -633,7 +537,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       if constexpr (PAIR) mma_commit_pair<kWarpIssue>(bar(C::kBarMmaDone));
       else mma_commit<kWarpIssue>(bar(C::kBarMmaDone));
       mbar_wait_drain(bar(C::kBarMmaDone), 0);
-      }
     }
    }
   } else {
@@ -646,19 +549,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
     // query tile 2t + rank of the pair's 512 rows)
     const int tile_row0 = PAIR ? (2 * t + static_cast<int>(rank)) * kBlockM : t * kBlockM;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t t_s0 = lane_base + C::kSCol0;
+    const uint32_t t_s = lane_base + C::kSCol0 + t * 128;
     const uint32_t t_o = lane_base + C::kOCol0 + t * D;
     float c = p.c;  // FP8: times the row's Q and the head's K descale, per item
     f32x2 c2 = f2_pack(c, c);
     const bool ragged = (p.N % kBlockN) != 0;
     // Barrier phases across items: bit 0 = s_full (flips per S tile),
-    // bit 1 = o_full (flips per item; rotating S buffers: per P V, counted
-    // by pvc, the P tiles this warpgroup has released).
+    // bit 1 = o_full (flips per item).
     uint32_t phase = 0;
-    int pvc = 0;
-    int sct = 0;  // rotating S buffers: this tile's S products so far
-    // rotating S buffers: S products of the CTA before this item
-    int s_before = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
       const int wi = fwd_item_index<PAIR>(round);
@@ -669,8 +567,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       // memory, like a spill slot): more live registers in the tile loop
       // below make ptxas spill about 25 others.
       const FwdItem itm = item_of(wi);
-      volatile int iv[5] = {itm.nkv0, itm.nkv1, itm.kb, (itm.q0 + tile_row0) / kBlockN, s_before};
-      s_before += itm.nkv0 + itm.nkv1;
+      volatile int iv[4] = {itm.nkv0, itm.nkv1, itm.kb, (itm.q0 + tile_row0) / kBlockN};
       if (iv[t] == 0) {
         // Split mode: an empty key range still leaves its partial result
         // for the merge (weight exp(-inf) = 0).
@@ -696,21 +593,11 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       f32x2 l2[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
                      f2_pack(0.0f, 0.0f)};
       for (int j = 0; j < iv[t]; ++j) {
-        if constexpr (C::kRot) {
-          ok = mbar_wait(bar(C::kBarSFull + 3 * t + sct % 3), (sct / 3) & 1, ctl, kSiteSFull);
-          ++sct;
-        } else {
-          ok = mbar_wait(bar(C::kBarSFull + t), phase & 1u, ctl, kSiteSFull);
-          phase ^= 1u;
-        }
+        ok = mbar_wait(bar(C::kBarSFull + t), phase & 1u, ctl, kSiteSFull);
+        phase ^= 1u;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        // This tile's S buffer: buffer t, or with rotating buffers the CTA's
-        // running S count mod 3 (S_0(j') before S_1(j') within an item).
-        const uint32_t t_s =
-            t_s0 + 128u * static_cast<uint32_t>(
-                       C::kRot ? (iv[4] + min(j + t, iv[0]) + min(j, iv[1])) % 3 : t);
         // The whole row of S (128 fp32) in registers: four loads, one wait.
         uint32_t r[4][32];
 #pragma unroll
@@ -755,14 +642,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         const bool need = (m_new - m_used) > kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
           const float alpha = need ? ex2_mufu(m_used - m_new) : 1.0f;
-          if (C::kRot && j > 0) {
-            // rotating S buffers: P V of this tile's previous P may still be
-            // accumulating into O (S runs ahead of it); wait for it
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(bar(C::kBarOFull + t), (pvc - 1) & 1, ctl, kSiteOFull));
-            if (!ok) break;
-            tc_fence_after();
-          }
           if (j > 0) {
             const f32x2 a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
@@ -852,7 +731,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         } else {
           mbar_arrive(bar(C::kBarPFull + t));
         }
-        ++pvc;
       }
       float l;
       {
@@ -865,12 +743,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       // here, before P_t(0) of the next item is released, is what lets the
       // next item's first P V overwrite O_t.
       if (ok) {
-        if constexpr (C::kRot) {
-          ok = mbar_wait(bar(C::kBarOFull + t), (pvc - 1) & 1, ctl, kSiteOFull);
-        } else {
-          ok = mbar_wait(bar(C::kBarOFull + t), (phase >> 1) & 1u, ctl, kSiteOFull);
-          phase ^= 2u;
-        }
+        ok = mbar_wait(bar(C::kBarOFull + t), (phase >> 1) & 1u, ctl, kSiteOFull);
+        phase ^= 2u;
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
           tc_fence_after();
