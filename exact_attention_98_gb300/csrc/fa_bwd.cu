@@ -460,7 +460,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % C::kStages;
       bool ok = mbar_wait(bar(C::kBarDQFull), it & 1, ctl, kSiteDQFull);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      if (!__all_sync(0xffffffffu, ok)) {
+        // Release drain warps already waiting at this tile's barrier below;
+        // they give up at their next wait (the CTA's abort flag is raised).
+        named_bar_arrive(C::kDrainBarrier, kBlockM);
+        break;
+      }
       tc_fence_after();
       // dK_i and dQ_i, the last readers of Q_i and dO_i, are complete: their
       // buffers take the fp32 dQ tile.

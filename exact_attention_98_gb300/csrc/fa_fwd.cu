@@ -762,21 +762,37 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
           if (item.part < 0) {
             __nv_bfloat16* orow =
                 static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
-#pragma unroll 1
+            // The whole O row in one batch of loads (pair mode: 32 columns at
+            // a time, registers are short there), then 32-byte stores where O
+            // allows them (a row is 2d bytes, so every row keeps O's alignment).
+            const bool o32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
+            constexpr int kBatch = PAIR ? 1 : D / 32;
+            uint32_t r[kBatch][32];
+#pragma unroll(PAIR ? 1 : D / 32)
             for (int ch = 0; ch < D / 32; ++ch) {
-              uint32_t r[32];
-              tmem_ld32(t_o + ch * 32, r);
-              tmem_ld_wait(r);
+              if (ch % kBatch == 0) {
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b) tmem_ld32(t_o + (ch + b) * 32, r[b]);
+                tmem_ld_wait(r[0]);
+#pragma unroll
+                for (int b = 1; b < kBatch; ++b) reg_fence(r[b]);
+              }
               uint32_t w[16];
 #pragma unroll
               for (int e = 0; e < 16; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
-                                   __uint_as_float(r[2 * e + 1]) * inv_l);
+                w[e] = pack_bf16x2(__uint_as_float(r[ch % kBatch][2 * e]) * inv_l,
+                                   __uint_as_float(r[ch % kBatch][2 * e + 1]) * inv_l);
               if (in_range) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+                if (o32) {
+                  st_global_v8(orow + ch * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                  st_global_v8(orow + ch * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14],
+                               w[15]);
+                } else {
+                  uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                  dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                  for (int v4 = 0; v4 < 4; ++v4)
+                    dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+                }
               }
             }
             if (in_range) p.lse[static_cast<size_t>(bh) * p.N + qpos] = lse_row;

@@ -115,6 +115,33 @@ def test_splitkv_single_key_tile():
     compare_fwd(1, 2, 100, 64, False, num_splits=1)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_only_16_byte_aligned(d):
+    """The API asks 16-byte alignment of O; the forward writes O rows with
+    32-byte stores when O allows them and with 16-byte stores otherwise.
+    An O that starts 16 bytes past a 32-byte boundary gets bit-identical
+    results to an aligned one."""
+    from exact_attention_98_gb300 import fa
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    B, H, N = 1, 2, 777
+    q, k, v, _ = (None if t is None else t.cuda()
+                  for t in attention_inputs(B, H, N, d, seed=5, with_dout=False))
+    scale = 1 / math.sqrt(d)
+    for causal in (False, True):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        assert o.data_ptr() % 32 == 0
+        fa.fa_fwd(q, k, v, o, lse, scale, causal)
+        buf = torch.empty(q.numel() + 8, dtype=q.dtype, device="cuda")
+        o16 = buf[8:].view_as(q)
+        assert o16.data_ptr() % 32 == 16
+        lse16 = torch.empty_like(lse)
+        fa.fa_fwd(q, k, v, o16, lse16, scale, causal)
+        assert fa.fa_last_device_status() == fa.FA_OK
+        assert torch.equal(o16, o) and torch.equal(lse16, lse)
+
+
 def test_launch_counter_per_call():
     """fa_launch_count advances by the number of kernels each call launches
     (the figure the benchmark reports as its launch count)."""
