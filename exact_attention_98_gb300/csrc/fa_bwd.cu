@@ -654,21 +654,36 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(wg == 0 ? p.dv : p.dk) +
-                             (static_cast<size_t>(bh) * p.N + kpos) * D;
+        void* base = wg == 0 ? p.dv : p.dk;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(base) + (static_cast<size_t>(bh) * p.N + kpos) * D;
+        // two 32-column chunks per load batch; 32-byte stores where the
+        // output allows them (a row is 2d bytes: rows keep its alignment)
+        const bool a32 = (reinterpret_cast<uintptr_t>(base) & 31u) == 0;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + col + ch * 32, r);
-          tmem_ld_wait(r);
+        for (int ch = 0; ch < D / 32; ch += 2) {
+          uint32_t r[2][32];
+          tmem_ld32(lane_base + col + ch * 32, r[0]);
+          tmem_ld32(lane_base + col + ch * 32 + 32, r[1]);
+          tmem_ld_wait(r[0]);
+          reg_fence(r[1]);
           if (row_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * v4]), __uint_as_float(r[8 * v4 + 1])),
-                                   pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3])),
-                                   pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5])),
-                                   pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7])));
+            for (int h = 0; h < 2; ++h) {
+              uint32_t w[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(r[h][2 * e]), __uint_as_float(r[h][2 * e + 1]));
+              __nv_bfloat16* dst = out + (ch + h) * 32;
+              if (a32) {
+                st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+                st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+              } else {
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                  reinterpret_cast<uint4*>(dst)[v4] =
+                      make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
+              }
+            }
           }
         }
       }

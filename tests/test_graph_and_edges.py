@@ -142,6 +142,32 @@ def test_output_only_16_byte_aligned(d):
         assert torch.equal(o16, o) and torch.equal(lse16, lse)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_gradients_only_16_byte_aligned(d):
+    """The same for the backward's dK and dV rows: outputs 16 bytes past a
+    32-byte boundary get the bits of aligned ones (dQ, summed with fp32
+    atomics in a varying order, is compared within the gradient bound)."""
+    from exact_attention_98_gb300 import fa
+    from exact_attention_98_gb300.inputs import attention_inputs
+
+    B, H, N = 1, 2, 777
+    q, k, v, do = (t.cuda() for t in attention_inputs(B, H, N, d, seed=6))
+    scale = 1 / math.sqrt(d)
+    ws = fa.workspace_for(q)
+    for causal in (False, True):
+        o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+        ref = [torch.empty_like(q) for _ in range(3)]
+        fa.fa_bwd(q, k, v, o, lse, do, *ref, scale, causal, ws)
+        bufs = [torch.empty(q.numel() + 8, dtype=q.dtype, device="cuda") for _ in range(3)]
+        got = [b[8:].view_as(q) for b in bufs]
+        assert all(g.data_ptr() % 32 == 16 for g in got)
+        fa.fa_bwd(q, k, v, o, lse, do, *got, scale, causal, ws)
+        assert fa.fa_last_device_status() == fa.FA_OK
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+        rel = (got[0].float() - ref[0].float()).norm() / ref[0].float().norm()
+        assert rel < 1e-3, float(rel)
+
+
 def test_launch_counter_per_call():
     """fa_launch_count advances by the number of kernels each call launches
     (the figure the benchmark reports as its launch count)."""
