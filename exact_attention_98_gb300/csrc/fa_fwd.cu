@@ -613,15 +613,16 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         const bool edge = (p.causal && (PAIR ? jabs >= iv[3] : jabs == iv[3])) ||
                           (ragged && jabs == n_ktiles - 1);
         if (edge) {
+          // the row keeps its first `lim` columns: keys below N and, causal,
+          // not after the query
           const int kbase = jabs * kBlockN;
-          const int qpos = iv[3] * kBlockN + row;
+          int lim = p.N - kbase;
+          if (p.causal) lim = min(lim, iv[3] * kBlockN + row - kbase + 1);
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int kpos = kbase + ch * 32 + e;
-              if (kpos >= p.N || (p.causal && kpos > qpos)) r[ch][e] = __float_as_uint(-INFINITY);
-            }
+            for (int e = 0; e < 32; ++e)
+              if (ch * 32 + e >= lim) r[ch][e] = __float_as_uint(-INFINITY);
         }
         // row max of the tile (raw scores; c > 0), eight independent chains
         float mxa[8];
