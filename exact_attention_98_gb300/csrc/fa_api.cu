@@ -450,6 +450,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     p.lse_part = reinterpret_cast<float*>(split_ws + round_up(slots * 2 * kBlockM * d * sizeof(float)));
   }
   p.n_items = p.split_from + (blocks - p.split_from) * p.num_splits;
+  p.div_bh = FastDiv(static_cast<uint32_t>(BH));
+  p.div_qblk = FastDiv(static_cast<uint32_t>(p.n_qblk));
+  p.div_splits = FastDiv(static_cast<uint32_t>(p.num_splits));
   cudaError_t err = timing_record(0, true, s);
   if (err == cudaSuccess) err = launch_fwd(p, d, s);
   if (err == cudaSuccess && p.split_from < blocks) err = launch_fwd_merge(p, o, lse, d, s);

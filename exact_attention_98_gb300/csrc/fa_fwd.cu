@@ -122,10 +122,13 @@ enum : unsigned int {
 // head are processed together and share its K and V in L2; causal, the
 // heaviest blocks (the last query blocks, which see the most keys) of every
 // head first.
-__device__ __forceinline__ void fwd_block(int blk, int causal, int BH, int n_qblk, int& bh,
-                                          int& q0, int rows = 2 * kBlockM) {
-  bh = causal ? blk % BH : blk / n_qblk;
-  const int qblk = n_qblk - 1 - (causal ? blk / BH : blk % n_qblk);
+__device__ __forceinline__ void fwd_block(int blk, int causal, const FastDiv& div_bh,
+                                          const FastDiv& div_qblk, int& bh, int& q0,
+                                          int rows = 2 * kBlockM) {
+  const FastDiv& dv = causal ? div_bh : div_qblk;
+  const int quo = dv.div(blk), rem = blk - quo * static_cast<int>(dv.d);
+  bh = causal ? rem : quo;
+  const int qblk = static_cast<int>(div_qblk.d) - 1 - (causal ? quo : rem);
   q0 = qblk * rows;
 }
 
@@ -149,19 +152,20 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int w, int n_kti
   it.part = -1;
   if (w >= p.split_from) {
     const int u = w - p.split_from;
-    blk = p.split_from + u / p.num_splits;
-    split = u % p.num_splits;
+    const int b = p.div_splits.div(u);
+    blk = p.split_from + b;
+    split = u - b * p.num_splits;
     ns = p.num_splits;
     it.part = u;
   }
-  fwd_block(blk, p.causal, p.BH, p.n_qblk, it.bh, it.q0);
+  fwd_block(blk, p.causal, p.div_bh, p.div_qblk, it.bh, it.q0);
   // key tiles [0, end) a query tile starting at qs attends to
   auto end_of = [&](int qs) {
     return qs >= p.N ? 0 : (p.causal ? min(n_ktiles, qs / kBlockN + 1) : n_ktiles);
   };
   const int end0 = end_of(it.q0);
   const int end1 = end_of(it.q0 + kBlockM);
-  const int per = (max(end0, end1) + ns - 1) / ns;
+  const int per = ns == 1 ? max(end0, end1) : p.div_splits.div(max(end0, end1) + ns - 1);
   it.kb = split * per;
   it.nkv0 = max(0, min(end0 - it.kb, per));
   it.nkv1 = max(0, min(end1 - it.kb, per));
@@ -178,7 +182,7 @@ __device__ __forceinline__ FwdItem pair_item(const FwdParams& p, int w, int n_kt
   FwdItem it;
   it.part = -1;
   it.kb = 0;
-  fwd_block(w, p.causal, p.BH, p.n_qblk, it.bh, it.q0, 4 * kBlockM);
+  fwd_block(w, p.causal, p.div_bh, p.div_qblk, it.bh, it.q0, 4 * kBlockM);
   auto end_of = [&](int qs) {
     return qs >= p.N ? 0 : (p.causal ? min(n_ktiles, qs / kBlockN + 1) : n_ktiles);
   };
@@ -562,8 +566,9 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       const int wi = fwd_item_index<PAIR>(round);
       if (wi >= p.n_items) break;
       // Key tiles of this warpgroup's query tile in the item's range, the
-      // range's first key tile and the index of this warpgroup's query tile
-      // (its diagonal key tile), kept in a small volatile array (so in local
+      // range's first key tile, the index of this warpgroup's query tile
+      // (its diagonal key tile) and the item's head, first row and partial
+      // slot (for the epilogue), kept in a small volatile array (so in local
       // memory, like a spill slot): more live registers in the tile loop
       // below make ptxas spill about 25 others.
       const FwdItem itm = item_of(wi);
@@ -752,6 +757,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
           const FwdItem item = item_of(wi);
           const int bh = item.bh;
           const int qpos = item.q0 + tile_row0 + row;
+          const int part = item.part;
           const bool in_range = qpos < p.N;
           float inv_l = 1.0f / l;
           float lse_row = m_used * p.ln2 + logf(l);
@@ -760,7 +766,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
             inv_l *= va > 0.0f ? va * (1.0f / 448.0f) : 1.0f;
             lse_row -= 6.0f * p.ln2;
           }
-          if (item.part < 0) {
+          if (part < 0) {
             __nv_bfloat16* orow =
                 static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
             // The whole O row in one batch of loads (pair mode: 32 columns at
@@ -800,7 +806,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
           } else {
             // Split mode: this key range's O (normalised over the range) and
             // LSE in fp32, for the merge.
-            const size_t prow = static_cast<size_t>(item.part) * 2 * kBlockM + t * kBlockM + row;
+            const size_t prow = static_cast<size_t>(part) * 2 * kBlockM + t * kBlockM + row;
             float* orow = p.o_part + prow * D;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
@@ -930,7 +936,8 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const float* __restrict_
                                                         __nv_bfloat16* __restrict__ o,
                                                         float* __restrict__ lse, int num_splits,
                                                         int n_blocks, int split_from, int causal,
-                                                        int BH, int n_qblk, int N, int d) {
+                                                        FastDiv div_bh, FastDiv div_qblk, int N,
+                                                        int d) {
   grid_dependency_wait();  // the partial results of the forward before it
   const int per_row = d / 8;
   const long long n8 = static_cast<long long>(n_blocks) * 2 * kBlockM * per_row;
@@ -941,7 +948,7 @@ __global__ void __launch_bounds__(256) fwd_merge_kernel(const float* __restrict_
     const int r = static_cast<int>(prow0 % (2 * kBlockM));
     const int col = static_cast<int>(i % per_row) * 8;
     int bh, q0;
-    fwd_block(split_from + t, causal, BH, n_qblk, bh, q0);
+    fwd_block(split_from + t, causal, div_bh, div_qblk, bh, q0);
     const int q = q0 + r;
     if (q >= N) continue;
     auto prow = [&](int s) {
@@ -985,8 +992,8 @@ cudaError_t launch_fwd_merge(const FwdParams& p, void* o, float* lse, int d,
   const cudaError_t err = launch_dependent(
       fwd_merge_kernel, dim3(static_cast<unsigned int>(blocks < 1 ? 1 : blocks)), dim3(256), 0,
       stream, static_cast<const float*>(p.o_part), static_cast<const float*>(p.lse_part),
-      static_cast<__nv_bfloat16*>(o), lse, p.num_splits, n_blocks, p.split_from, p.causal, p.BH,
-      p.n_qblk, p.N, d);
+      static_cast<__nv_bfloat16*>(o), lse, p.num_splits, n_blocks, p.split_from, p.causal,
+      p.div_bh, p.div_qblk, p.N, d);
   if (err != cudaSuccess) return err;
   return launched(1);
 }

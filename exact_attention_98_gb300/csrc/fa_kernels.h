@@ -10,6 +10,8 @@
 
 #include <utility>
 
+#include "fa_fastdiv.h"
+
 namespace fa {
 
 // Tile shape shared by the forward and backward kernels: 128 query rows x 128
@@ -63,6 +65,9 @@ struct FwdParams {
   float c;          // scale * log2(e): scores enter exp2 in these units
   float ln2;        // ln(2), to turn the log2-unit row max into LSE
   int poly_per_octet;  // exponentials per 8 on the FMA pipe (0..3)
+  // BH, n_qblk and num_splits as multiply-shift divisors for the work-item
+  // walk that every role of every CTA repeats per item
+  FastDiv div_bh, div_qblk, div_splits;
 };
 
 // Default share of the forward's exponentials evaluated by the polynomial on
