@@ -414,6 +414,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
              !encode_tile_map(&p.tm_v, v, N, BH, d)) {
     return FA_ERR_CUDA;
   }
+  if (!encode_tile_map(&p.tm_o, o, N, BH, d)) return FA_ERR_CUDA;
   p.o = o;
   p.lse = lse;
   p.status = status_ptr();

@@ -256,6 +256,20 @@ __device__ __forceinline__ void bulk_wait() {
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Named barrier that also returns the AND of `v` over its `count` threads, so
+// that they go on (or leave a loop) together.
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 // Arrival on a named barrier without waiting: how a warp that leaves a loop
 // early releases the warps already waiting in that loop's bar.sync.
 __device__ __forceinline__ void named_bar_arrive(int id, int count) {

@@ -77,13 +77,19 @@ struct FwdCfg {
   static_assert(FP8 || kTileBytes == (D / 64) * kHalfBytes, "bf16 tile = its swizzle blocks");
   // one ring slot: a K or V tile, or in pair mode this CTA's half of one
   static constexpr int kSlotBytes = PAIR ? kTileBytes / 2 : kTileBytes;
-  static constexpr int kSlots = FP8 ? 10 : PAIR ? 9 : ((D == 128) ? 5 : 6);
+  static constexpr int kSlots = FP8 ? 10 : PAIR ? 9 : ((D == 128) ? 4 : 6);
   // pair mode: a pad of one slot after the ring, so that no operand
   // read that starts in the last slot can leave the allocation
   static constexpr int kRingPad = PAIR ? kSlotBytes : 0;
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kSlots * kSlotBytes + kRingPad;
+  // O staging (not in pair mode, where shared memory is full): per softmax
+  // warpgroup 128 rows x 64 columns of bf16 O (one 128B-swizzle box, 16 KB),
+  // written out by bulk tensor stores
+  static constexpr bool kStageO = !PAIR;
+  static constexpr int kStageBytes = kBlockM * 64 * 2;
+  static constexpr int kStageOff = kRingOff + kSlots * kSlotBytes + kRingPad;
+  static constexpr int kBarOff = kStageOff + (kStageO ? 2 * kStageBytes : 0);
   // barriers: q_full, q_empty, full[kSlots], empty[kSlots], s_full[2],
   // p_full[2], o_full[2], mma_done
   static constexpr int kBarQFull = 0;
@@ -752,6 +758,11 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         ok = mbar_wait(bar(C::kBarOFull + t), (phase >> 1) & 1u, ctl, kSiteOFull);
         phase ^= 2u;
         ok = __all_sync(0xffffffffu, ok);
+      }
+      // The staged epilogue synchronises the warpgroup's four warps: they
+      // enter it, or leave the item loop, together.
+      if constexpr (C::kStageO) ok = named_bar_and(1 + t, kBlockM, ok);
+      {
         if (ok) {
           tc_fence_after();
           const FwdItem item = item_of(wi);
@@ -766,7 +777,48 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
             inv_l *= va > 0.0f ? va * (1.0f / 448.0f) : 1.0f;
             lse_row -= 6.0f * p.ln2;
           }
-          if (part < 0) {
+          if (C::kStageO && part < 0) {
+            // The whole O row in one batch of loads, normalised and packed;
+            // then per 64 columns: staged in this warpgroup's buffer (a 128B-
+            // swizzle box: row r at r * 128 bytes, 16-byte chunk c at
+            // (c ^ (r mod 8)) * 16) and written by one bulk tensor store,
+            // which drops rows past N.
+            uint32_t r[D / 32][32];
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(t_o + ch * 32, r[ch]);
+            tmem_ld_wait(r[0]);
+#pragma unroll
+            for (int ch = 1; ch < D / 32; ++ch) reg_fence(r[ch]);
+            uint32_t w[D / 2];
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch)
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                w[ch * 16 + e] = pack_bf16x2(__uint_as_float(r[ch][2 * e]) * inv_l,
+                                             __uint_as_float(r[ch][2 * e + 1]) * inv_l);
+            uint8_t* stage = smem + C::kStageOff + t * C::kStageBytes + row * 128;
+            const uint32_t stage_s = sbase + C::kStageOff + t * C::kStageBytes;
+            const int qrow0 = item.q0 + tile_row0;
+#pragma unroll
+            for (int h = 0; h < D / 64; ++h) {
+              // the buffer's previous bulk store has read it
+              if (row == 0) bulk_wait_read<0>();
+              named_bar_sync(1 + t, kBlockM);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const int wi = h * 32 + c * 4;
+                *reinterpret_cast<uint4*>(stage + ((c ^ (row & 7)) << 4)) =
+                    make_uint4(w[wi], w[wi + 1], w[wi + 2], w[wi + 3]);
+              }
+              fence_proxy_async_smem();
+              named_bar_sync(1 + t, kBlockM);
+              if (row == 0) {
+                tma_store_3d(&p.tm_o, stage_s, h * 64, qrow0, bh);
+                bulk_commit();
+              }
+            }
+            if (in_range) p.lse[static_cast<size_t>(bh) * p.N + qpos] = lse_row;
+          } else if (part < 0) {
             __nv_bfloat16* orow =
                 static_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(bh) * p.N + qpos) * D;
             // The whole O row in one batch of loads (pair mode: 32 columns at
@@ -827,6 +879,10 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
           }
         }
       }
+    }
+    // the last bulk stores of O are complete before the CTA ends
+    if constexpr (C::kStageO) {
+      if (row == 0) bulk_wait<0>();
     }
   }
 

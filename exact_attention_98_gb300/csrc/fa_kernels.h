@@ -33,6 +33,7 @@ struct FwdParams {
   CUtensorMap tm_q;  // bf16 [BH, N, d], box {64, 128, 1}, 128B swizzle
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_o;      // bf16 O [BH, N, d], box {64, 128, 1}, 128B swizzle (bulk stores)
   void* o;               // bf16 [BH, N, d]
   float* lse;            // fp32 [BH, N]
   unsigned int* status;  // device status word
