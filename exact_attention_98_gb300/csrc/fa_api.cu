@@ -542,6 +542,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   BwdParams p;
   if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
       !encode_tile_map(&p.tm_v, v, N, BH, d) || !encode_tile_map(&p.tm_do, dout, N, BH, d) ||
+      !encode_tile_map(&p.tm_dk, dk, N, BH, d) || !encode_tile_map(&p.tm_dv, dv, N, BH, d) ||
       !encode_dq_map(&p.tm_dq, dq_buf, N,
                      deterministic ? static_cast<long long>(n_kblk) * BH : BH, d))
     return FA_ERR_CUDA;

@@ -153,6 +153,14 @@ struct BwdCfg {
   static_assert(kColDQ + (D == 128 ? kBlockM : D) <= 512, "tensor-memory columns");
   static constexpr int kDrainBarrier = 1;  // named barrier of the d = 64 drain (0 is __syncthreads)
   static_assert(kDrainBarrier > 0, "named barrier 0 is the CTA barrier");
+  // Epilogue staging of the bf16 dV (warpgroup 0) and dK (warpgroup 1)
+  // tiles, d/64 boxes of 128 rows x 64 columns each: at d = 128 in stage 0's
+  // Q and dO buffers, at d = 64 in the two dS buffers; named barriers 2, 3.
+  static constexpr int kEpiBoxBytes = kBlockN * 64 * 2;
+  static constexpr int kEpiStageOff = (D == 128) ? kQOff : kDsOff;
+  static constexpr int kEpiStageStride = (D == 128) ? kDOOff - kQOff : kDsTileBytes;
+  static_assert(kEpiStageStride >= (D / 64) * kEpiBoxBytes, "epilogue staging");
+  static constexpr int kEpiBarrier0 = 2;
   // Shared-memory offset of query tile it's dS tile (stage s = it % kStages).
   static __device__ __forceinline__ int ds_off(int it) {
     return (D == 128) ? kDOOff + (it % kStages) * kTileBytes : kDsOff + (it % kDsBufs) * kDsTileBytes;
@@ -648,44 +656,52 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_arrive(bar(C::kBarDSFull));
     }
 
-    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (already scaled)
+    // Epilogue: warpgroup 0 writes dV, warpgroup 1 dK (already scaled).
+    // Once every product is complete, shared memory that held query tiles
+    // (d = 128: stage 0's Q and dO buffers) or dS (d = 64) is free: each
+    // warpgroup stages its bf16 tile there, 64 columns per 128B-swizzle box
+    // (row r at r * 128 bytes, 16-byte chunk c at (c ^ (r mod 8)) * 16), and
+    // one of its threads writes it with bulk tensor stores, which drop rows
+    // past N.  The warpgroup's four warps enter this together (the barrier
+    // ANDs their status) because they synchronise inside it.
     if (ok) {
       ok = mbar_wait(bar(C::kBarMmaDone), 0, ctl, kSiteMmaDone);
-      if (__all_sync(0xffffffffu, ok)) {
-        tc_fence_after();
-        const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
-        void* base = wg == 0 ? p.dv : p.dk;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(base) + (static_cast<size_t>(bh) * p.N + kpos) * D;
-        // two 32-column chunks per load batch; 32-byte stores where the
-        // output allows them (a row is 2d bytes: rows keep its alignment)
-        const bool a32 = (reinterpret_cast<uintptr_t>(base) & 31u) == 0;
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    ok = named_bar_and(C::kEpiBarrier0 + wg, kBlockM, ok);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
+      const int stage_off = C::kEpiStageOff + wg * C::kEpiStageStride;
+      uint8_t* stage = smem + stage_off + kr * 128;
 #pragma unroll 1
-        for (int ch = 0; ch < D / 32; ch += 2) {
-          uint32_t r[2][32];
-          tmem_ld32(lane_base + col + ch * 32, r[0]);
-          tmem_ld32(lane_base + col + ch * 32 + 32, r[1]);
-          tmem_ld_wait(r[0]);
-          reg_fence(r[1]);
-          if (row_valid) {
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t r[2][32];
+        tmem_ld32(lane_base + col + h * 64, r[0]);
+        tmem_ld32(lane_base + col + h * 64 + 32, r[1]);
+        tmem_ld_wait(r[0]);
+        reg_fence(r[1]);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t w[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                w[e] = pack_bf16x2(__uint_as_float(r[h][2 * e]), __uint_as_float(r[h][2 * e + 1]));
-              __nv_bfloat16* dst = out + (ch + h) * 32;
-              if (a32) {
-                st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-                st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
-              } else {
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                  reinterpret_cast<uint4*>(dst)[v4] =
-                      make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
-              }
-            }
-          }
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t* x = &r[c >> 2][(c & 3) * 8];
+          *reinterpret_cast<uint4*>(stage + h * C::kEpiBoxBytes + ((c ^ (kr & 7)) << 4)) =
+              make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                         pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                         pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                         pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
         }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(C::kEpiBarrier0 + wg, kBlockM);
+      if (kr == 0) {
+        const CUtensorMap* map = wg == 0 ? &p.tm_dv : &p.tm_dk;
+#pragma unroll 1
+        for (int h = 0; h < D / 64; ++h)
+          tma_store_3d(map, sbase + stage_off + h * C::kEpiBoxBytes, h * 64, k0, bh);
+        bulk_commit();
+        // The CTA may end once the stores have read shared memory; the
+        // grid's completion covers their writes.
+        bulk_wait_read<0>();
       }
     }
   }

@@ -880,9 +880,10 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         }
       }
     }
-    // the last bulk stores of O are complete before the CTA ends
+    // The CTA may end once the last bulk stores of O have read shared
+    // memory; the grid's completion covers their writes.
     if constexpr (C::kStageO) {
-      if (row == 0) bulk_wait<0>();
+      if (row == 0) bulk_wait_read<0>();
     }
   }
 

@@ -84,6 +84,9 @@ struct BwdParams {
   // fp32 dQ target, box {16, 128, 1}, 64B swizzle: the accumulator
   // [BH, N, d], or in deterministic mode the partial sums [n_kblk * BH, N, d]
   CUtensorMap tm_dq;
+  // bf16 dK and dV [BH, N, d], box {64, 128, 1}, 128B swizzle (bulk stores)
+  CUtensorMap tm_dk;
+  CUtensorMap tm_dv;
   const float* lse;   // fp32 [BH, N]
   const float* dsum;  // fp32 [BH, N]: D = rowsum(dO * O)
   float* dq_acc;      // fp32 [BH, N, d], zeroed before the main kernel (atomic mode)
