@@ -603,7 +603,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
       // row sum of exp2(x - m_used): four f32x2 accumulators (eight partial sums)
       f32x2 l2[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
                      f2_pack(0.0f, 0.0f)};
-      for (int j = 0; j < iv[t]; ++j) {
+      for (int j = 0, nk = iv[t]; j < nk; ++j) {
+        // The key tile and whether it needs a mask, from the small local array
+        // before the wait for S, so that the loads' latency hides in it.
+        const int jabs = iv[2] + j;  // key tile index
+        // causal: the diagonal tile (pair mode: and the tile after it, which
+        // the earlier CTA of the pair masks whole)
+        const bool edge = (p.causal && (PAIR ? jabs >= iv[3] : jabs == iv[3])) ||
+                          (ragged && jabs == n_ktiles - 1);
         ok = mbar_wait(bar(C::kBarSFull + t), phase & 1u, ctl, kSiteSFull);
         phase ^= 1u;
         ok = __all_sync(0xffffffffu, ok);
@@ -618,11 +625,6 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         reg_fence(r[2]);
         reg_fence(r[3]);
 
-        const int jabs = iv[2] + j;  // key tile index
-        // causal: the diagonal tile (pair mode: and the tile after it, which
-        // the earlier CTA of the pair masks whole)
-        const bool edge = (p.causal && (PAIR ? jabs >= iv[3] : jabs == iv[3])) ||
-                          (ragged && jabs == n_ktiles - 1);
         if (edge) {
           // the row keeps its first `lim` columns: keys below N and, causal,
           // not after the query
