@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kBarSFull + t), 1);
-      // pair mode: one arrival per softmax warp of both CTAs (on rank 0's)
-      mbar_init(bar(C::kBarPFull + t), PAIR ? 8 : kBlockM);
+      // one arrival per softmax warp (pair mode: of both CTAs, on rank 0's)
+      mbar_init(bar(C::kBarPFull + t), PAIR ? 8 : 4);
       mbar_init(bar(C::kBarOFull + t), 1);
     }
     mbar_init(bar(C::kBarMmaDone), 1);
@@ -738,12 +738,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8, PAIR>::kThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
+        // one arrival per warp once all its lanes' stores are complete
+        // (pair mode: on rank 0's barrier)
+        __syncwarp();
         if constexpr (PAIR) {
-          // one arrival per warp, on rank 0's barrier
-          __syncwarp();
           if (lane == 0) mbar_arrive_peer(cluster_smem(bar(C::kBarPFull + t), 0));
         } else {
-          mbar_arrive(bar(C::kBarPFull + t));
+          if (lane == 0) mbar_arrive(bar(C::kBarPFull + t));
         }
       }
       float l;
