@@ -535,7 +535,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     if (timing_record(1, true, s) != cudaSuccess) return FA_ERR_CUDA;
     if (launch_bwd_pair(pp, s) != cudaSuccess) return FA_ERR_CUDA;
     if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
-    if (launch_bwd_post(dq_acc, dq, rows * d, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_bwd_post(dq_acc, dq, rows * d, scale, s) != cudaSuccess) return FA_ERR_CUDA;
     return FA_OK;
   }
 
@@ -569,9 +569,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   if (launch_bwd_main(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
   if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
   if (deterministic) {
-    if (launch_bwd_dq_reduce(dq_buf, dq, BH, N, d, n_kblk, causal, s) != cudaSuccess)
+    if (launch_bwd_dq_reduce(dq_buf, dq, BH, N, d, n_kblk, causal, scale, s) != cudaSuccess)
       return FA_ERR_CUDA;
-  } else if (launch_bwd_post(dq_acc, dq, rows * d, s) != cudaSuccess) {
+  } else if (launch_bwd_post(dq_acc, dq, rows * d, scale, s) != cudaSuccess) {
     return FA_ERR_CUDA;
   }
   return FA_OK;

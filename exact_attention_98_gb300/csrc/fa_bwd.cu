@@ -33,15 +33,16 @@
 // d = 64 (dQ in columns of its own, three Q/dO stages): the next tile's S^T
 // follows dV_i, so its exponentials overlap dK_i and dQ_i:
 //   dP^T ; [P^T] dV ; S^T_{i+1} ; [dS] dK ; [dQ_{i-1} drained] dQ_i
-// with P^T = exp2(S^T c - LSE_i log2 e) and dS = scale * P (dP - D_i): the
-// softmax scale is folded into dS, so dK and dQ come out scaled.
+// with P^T = exp2(S^T c - LSE_i log2 e) and dS = P (dP - D_i) without the
+// softmax scale, which is applied once at the end instead: to dK in the
+// write-out and to dQ in its conversion to bf16.
 //
 // The per-query terms -LSE_i / scale and -D_i enter through the tensor core
 // as a rank-1 bias: one more K = 16 MMA adds ones(128 x 16) * b^T onto S^T
 // (and onto dP^T), where column k of b holds the query's value split into
 // bf16 hi + lo parts (about 16 significant bits) in its first two entries and
 // zeros elsewhere.  The compute warps then need no per-query loads at all:
-// P = exp2(c S'^T) and dS = scale P dP'^T.
+// P = exp2(c S'^T) and dS = P dP'^T (the softmax scale comes later).
 //
 // Warp roles (512 threads = four warpgroups):
 //   warps 0-7   compute: two warpgroups, thread = key row, warpgroup w takes
@@ -536,7 +537,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const bool row_valid = kpos < p.N;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const f32x2 c2 = f2_pack(p.c, p.c);
-    const f32x2 scale2 = f2_pack(p.scale, p.scale);
     bool ok = true;
     for (int it = 0; it < n_iter; ++it) {
       const int s = it % C::kStages;
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull));
 
-      // dS = scale * P dP'^T, dP'^T = dP^T - D by the bias MMA: to tensor
+      // dS = P dP'^T (unscaled), dP'^T = dP^T - D by the bias MMA: to tensor
       // memory (for dK) and, once dV has finished reading dO_i, into shared
       // memory (for dQ).
       ok = mbar_wait(bar(C::kBarDPFull), it & 1, ctl, kSiteDPFull);
@@ -619,11 +619,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int e2 = 0; e2 < 16; ++e2) {
           float a0, a1;
-          f2_unpack(f2_mul(f2_mul(f2_pack(__uint_as_float(dr[ch][2 * e2]),
-                                          __uint_as_float(dr[ch][2 * e2 + 1])),
-                                  f2_pack(__uint_as_float(pw[ch * 16 + e2] << 16),
-                                          __uint_as_float(pw[ch * 16 + e2] & 0xFFFF0000u))),
-                           scale2),
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(dr[ch][2 * e2]),
+                                   __uint_as_float(dr[ch][2 * e2 + 1])),
+                           f2_pack(__uint_as_float(pw[ch * 16 + e2] << 16),
+                                   __uint_as_float(pw[ch * 16 + e2] & 0xFFFF0000u))),
                     a0, a1);
           dsw[ch * 16 + e2] = pack_bf16x2(a0, a1);
         }
@@ -656,7 +655,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_arrive(bar(C::kBarDSFull));
     }
 
-    // Epilogue: warpgroup 0 writes dV, warpgroup 1 dK (already scaled).
+    // Epilogue: warpgroup 0 writes dV, warpgroup 1 dK (times the softmax
+    // scale, which dS left out).
     // Once every product is complete, shared memory that held query tiles
     // (d = 128: stage 0's Q and dO buffers) or dS (d = 64) is free: each
     // warpgroup stages its bf16 tile there, 64 columns per 128B-swizzle box
@@ -672,6 +672,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (ok) {
       tc_fence_after();
       const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
+      const float mul = wg == 0 ? 1.0f : p.scale;
       const int stage_off = C::kEpiStageOff + wg * C::kEpiStageStride;
       uint8_t* stage = smem + stage_off + kr * 128;
 #pragma unroll 1
@@ -685,10 +686,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int c = 0; c < 8; ++c) {
           const uint32_t* x = &r[c >> 2][(c & 3) * 8];
           *reinterpret_cast<uint4*>(stage + h * C::kEpiBoxBytes + ((c ^ (kr & 7)) << 4)) =
-              make_uint4(pack_bf16x2(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                         pack_bf16x2(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                         pack_bf16x2(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                         pack_bf16x2(__uint_as_float(x[6]), __uint_as_float(x[7])));
+              make_uint4(pack_bf16x2(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul),
+                         pack_bf16x2(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul),
+                         pack_bf16x2(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul),
+                         pack_bf16x2(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul));
         }
       }
       fence_proxy_async_smem();

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 // flight against HBM latency).
 __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__ dq_acc,
                                                        __nv_bfloat16* __restrict__ dq,
-                                                       long long n8) {
+                                                       long long n8, float mul) {
   grid_dependency_wait();  // the accumulator of the main kernel before it
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i0 < n8;
@@ -79,10 +79,10 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
       const long long i = i0 + u * stride;
       if (i < n8) {
         uint4 w;
-        w.x = pack_bf16x2(a[u].x, a[u].y);
-        w.y = pack_bf16x2(a[u].z, a[u].w);
-        w.z = pack_bf16x2(b[u].x, b[u].y);
-        w.w = pack_bf16x2(b[u].z, b[u].w);
+        w.x = pack_bf16x2(a[u].x * mul, a[u].y * mul);
+        w.y = pack_bf16x2(a[u].z * mul, a[u].w * mul);
+        w.z = pack_bf16x2(b[u].x * mul, b[u].y * mul);
+        w.w = pack_bf16x2(b[u].z * mul, b[u].w * mul);
         reinterpret_cast<uint4*>(dq)[i] = w;
       }
     }
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
 __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float* __restrict__ part,
                                                             __nv_bfloat16* __restrict__ dq,
                                                             int BH, int N, int d, int n_kblk,
-                                                            int causal, long long n8) {
+                                                            int causal, long long n8, float mul) {
   grid_dependency_wait();  // the contributions of the main kernel before it
   const int per_row = d / 8;
   const size_t slice = static_cast<size_t>(BH) * N * d;  // one key tile's contributions
@@ -113,10 +113,10 @@ __global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float* __restr
       a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
     }
     uint4 w;
-    w.x = pack_bf16x2(a[0], a[1]);
-    w.y = pack_bf16x2(a[2], a[3]);
-    w.z = pack_bf16x2(a[4], a[5]);
-    w.w = pack_bf16x2(a[6], a[7]);
+    w.x = pack_bf16x2(a[0] * mul, a[1] * mul);
+    w.y = pack_bf16x2(a[2] * mul, a[3] * mul);
+    w.z = pack_bf16x2(a[4] * mul, a[5] * mul);
+    w.w = pack_bf16x2(a[6] * mul, a[7] * mul);
     reinterpret_cast<uint4*>(dq)[i] = w;
   }
 }
@@ -145,20 +145,21 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* 
   return launched(1);
 }
 
-cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, cudaStream_t stream) {
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, float mul,
+                            cudaStream_t stream) {
   const long long n8 = elems / 8;  // d is a multiple of 8, so elems is too
   const cudaError_t err = launch_dependent(bwd_post_kernel, dim3(grid_for(n8, 256)), dim3(256), 0,
-                                           stream, dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
+                                           stream, dq_acc, static_cast<__nv_bfloat16*>(dq), n8, mul);
   if (err != cudaSuccess) return err;
   return launched(1);
 }
 
 cudaError_t launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, int n_kblk,
-                                 int causal, cudaStream_t stream) {
+                                 int causal, float mul, cudaStream_t stream) {
   const long long n8 = static_cast<long long>(BH) * N * d / 8;
   const cudaError_t err = launch_dependent(bwd_dq_reduce_kernel, dim3(grid_for(n8, 256)), dim3(256),
                                            0, stream, dq_part, static_cast<__nv_bfloat16*>(dq), BH,
-                                           N, d, n_kblk, causal, n8);
+                                           N, d, n_kblk, causal, n8, mul);
   if (err != cudaSuccess) return err;
   return launched(1);
 }

@@ -512,7 +512,6 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
     const bool row_valid = kpos < p.N;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const f32x2 c2 = f2_pack(p.c, p.c);
-    const f32x2 scale2 = f2_pack(p.scale, p.scale);
     // this thread's dS row in CTA wg's buffer: key row 128 rank + kr of 256
     const int ds_row = static_cast<int>(rank) * kBlock + kr;
     const bool ds_local = wg == static_cast<int>(rank);  // else staged and sent
@@ -582,7 +581,9 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_peer(bar0(C::kBarPFull));
 
-      // dS = scale * P dP'^T, dP'^T = dP^T - D by the bias MMA: to tensor
+      // dS = P dP'^T (unscaled: the softmax scale goes to dK in the
+      // write-out and to dQ in its conversion), dP'^T = dP^T - D by the bias
+      // MMA: to tensor
       // memory (for dK) and to CTA wg's shared memory (for dQ).
       ok = mbar_wait(bar(C::kBarDPFull), it & 1, ctl, kSiteDPFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -598,11 +599,10 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
 #pragma unroll
         for (int e2 = 0; e2 < 16; ++e2) {
           float a0, a1;
-          f2_unpack(f2_mul(f2_mul(f2_pack(__uint_as_float(dr[ch][2 * e2]),
-                                          __uint_as_float(dr[ch][2 * e2 + 1])),
-                                  f2_pack(__uint_as_float(pw[ch * 16 + e2] << 16),
-                                          __uint_as_float(pw[ch * 16 + e2] & 0xFFFF0000u))),
-                           scale2),
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(dr[ch][2 * e2]),
+                                   __uint_as_float(dr[ch][2 * e2 + 1])),
+                           f2_pack(__uint_as_float(pw[ch * 16 + e2] << 16),
+                                   __uint_as_float(pw[ch * 16 + e2] & 0xFFFF0000u))),
                     a0, a1);
           dsw[ch * 16 + e2] = pack_bf16x2(a0, a1);
         }
@@ -636,12 +636,14 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
       }
     }
 
-    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (already scaled)
+    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (times the
+    // softmax scale, which dS left out)
     if (ok) {
       ok = mbar_wait(bar(C::kBarMmaDone), 0, ctl, kSiteMmaDone);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
         const uint32_t col = wg == 0 ? C::kColDV : C::kColDK;
+        const float mul = wg == 0 ? 1.0f : p.scale;
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(wg == 0 ? p.dv : p.dk) +
                              (static_cast<size_t>(bh) * p.N + kpos) * C::D;
 #pragma unroll 1
@@ -653,10 +655,11 @@ __global__ void __launch_bounds__(PairBwdCfg::kThreads, 1)
             uint4* dst = reinterpret_cast<uint4*>(out + ch * 32);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * v4]), __uint_as_float(r[8 * v4 + 1])),
-                                   pack_bf16x2(__uint_as_float(r[8 * v4 + 2]), __uint_as_float(r[8 * v4 + 3])),
-                                   pack_bf16x2(__uint_as_float(r[8 * v4 + 4]), __uint_as_float(r[8 * v4 + 5])),
-                                   pack_bf16x2(__uint_as_float(r[8 * v4 + 6]), __uint_as_float(r[8 * v4 + 7])));
+              dst[v4] = make_uint4(
+                  pack_bf16x2(__uint_as_float(r[8 * v4]) * mul, __uint_as_float(r[8 * v4 + 1]) * mul),
+                  pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * mul, __uint_as_float(r[8 * v4 + 3]) * mul),
+                  pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * mul, __uint_as_float(r[8 * v4 + 5]) * mul),
+                  pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * mul, __uint_as_float(r[8 * v4 + 7]) * mul));
           }
         }
       }

@@ -102,7 +102,7 @@ struct BwdParams {
   int n_kblk;  // ceil(N / 128)
   int causal;
   float c;      // scale * log2(e)
-  float scale;  // folded into dS so that dQ and dK come out scaled
+  float scale;  // applied to dK in the write-out and to dQ in its conversion (dS leaves it out)
   float inv_scale;  // 1 / scale: -LSE / scale is the bias in raw score units
   float log2e;
 };
@@ -129,7 +129,7 @@ struct BwdPairParams {
   int n_kpair;  // ceil(n_kblk / 2): key-tile pairs per head
   int causal;
   float c;          // scale * log2(e)
-  float scale;
+  float scale;      // applied to dK in the write-out and to dQ in its conversion
   float inv_scale;
 };
 
@@ -197,12 +197,14 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* 
                            long long rows, int d, cudaStream_t stream);
 // Backward main kernel (key/value stationary).
 cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
-// dQ = dQ accumulator -> bf16.
-cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, cudaStream_t stream);
-// Deterministic mode: dQ = sum over key tiles kt = 0, 1, ... (in that order)
-// of dq_part[kt] -> bf16.  Causal: query tile i has contributions from
-// kt <= i only.
+// dQ = mul * dQ accumulator -> bf16 (mul: the softmax scale, which the main
+// kernels leave out of dS).
+cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, float mul,
+                            cudaStream_t stream);
+// Deterministic mode: dQ = mul * sum over key tiles kt = 0, 1, ... (in that
+// order) of dq_part[kt] -> bf16.  Causal: query tile i has contributions
+// from kt <= i only.
 cudaError_t launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, int n_kblk,
-                                 int causal, cudaStream_t stream);
+                                 int causal, float mul, cudaStream_t stream);
 
 }  // namespace fa
