@@ -68,6 +68,9 @@ def parse():
     ap.add_argument("--causal", action="store_true", help="causal mask for --loop")
     ap.add_argument("--poly", type=int, default=None,
                     help="exponentials per 8 on the FMA pipe in the forward (--loop)")
+    ap.add_argument("--oracle-configs", action="store_true",
+                    help="instead of the bench line: the fp64 oracle timed on the host cores on "
+                         "each configuration's oracle coverage (one JSON line each; no GPU)")
     return ap.parse_args()
 
 
@@ -830,8 +833,77 @@ def sweep_arm(args):
             del q, k, v, do, o, lse, dq, dk, dv, ws, wsf
 
 
+def oracle_configs_arm(args):
+    """The oracle's own cost on the coverage the parity tests give it, per
+    configuration: B1 H2 N128 d64 in full (fwd + bwd, both masks); head 0 of
+    B2 H16 N4096 d128 in full (fwd); 512 sampled rows of head 0 of B1 H16
+    N32768 d128 causal (fwd); 256 sampled rows of head 0 of B2 H16 N8192 d128
+    causal (fwd + the dQ rows of the bwd).  Algorithmic FLOPs as on the GPU
+    (causal rows count the keys they attend to).  Host cores only."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_98_gb300.inputs import attention_inputs, sampled_rows
+
+    def head0(B, H, N, d, causal_seed=0):
+        q, k, v, do = attention_inputs(B, H, N, d, seed=causal_seed)
+        return tuple(t.double().numpy()[0, 0] for t in (q, k, v, do))
+
+    def line(name, flop, secs, extra):
+        print(json.dumps({"oracle_config": name, "gflop": flop / 1e9, "seconds": secs,
+                          "gflop_per_s": flop / secs / 1e9, "threads": oracle.num_threads(),
+                          "cpu_model": cpu_model(), "nproc": os.cpu_count(), **extra}), flush=True)
+
+    # config 1 in full, both masks
+    q, k, v, do = attention_inputs(1, 2, 128, 64, seed=0)
+    q, k, v, do = (t.double().numpy() for t in (q, k, v, do))
+    t0 = time.perf_counter()
+    f = 0.0
+    for causal in (False, True):
+        oracle.fwd(q, k, v, 0.125, causal)
+        oracle.bwd(q, k, v, do, 0.125, causal)
+        ff, fb = flops(1, 2, 128, 64, causal)
+        f += ff + fb
+    line("1: B1 H2 N128 d64, fwd+bwd, both masks, full", f, time.perf_counter() - t0, {})
+
+    # config 2, head 0 in full (forward)
+    N, d = 4096, 128
+    q, k, v, _ = head0(2, 16, N, d)
+    t0 = time.perf_counter()
+    oracle.fwd_head(q, k, v, 1.0 / math.sqrt(d), False)
+    secs = time.perf_counter() - t0
+    line("2: B2 H16 N4096 d128, head 0 in full, fwd", 4.0 * N * N * d, secs,
+         {"projected_full_fwd_s": secs * 2 * 16})
+
+    # config 3, sampled rows (causal forward)
+    N = 32768
+    q, k, v, _ = head0(1, 16, N, d)
+    rows = sorted(set(int(x) for x in np.linspace(0, N - 1, 512)))
+    t0 = time.perf_counter()
+    oracle.fwd_head(q, k, v, 1.0 / math.sqrt(d), True, rows=rows)
+    secs = time.perf_counter() - t0
+    f = sum(4.0 * (r + 1) * d for r in rows)
+    line("3: B1 H16 N32768 d128 causal, 512 rows of head 0, fwd", f, secs,
+         {"projected_full_fwd_s": secs * (4.0 * 16 * N * N * d / 2) / f})
+
+    # config 4, sampled rows (causal: forward and the dQ rows of the backward)
+    N = 8192
+    q, k, v, do = head0(2, 16, N, d)
+    rows = sorted(set(int(x) for x in np.linspace(0, N - 1, 256)))
+    t0 = time.perf_counter()
+    oracle.fwd_head(q, k, v, 1.0 / math.sqrt(d), True, rows=rows)
+    oracle.bwd_head(q, k, v, do, 1.0 / math.sqrt(d), True, qrows=rows, krows=[])
+    secs = time.perf_counter() - t0
+    f = sum(10.0 * (r + 1) * d for r in rows)
+    line("4: B2 H16 N8192 d128 causal, 256 rows of head 0, fwd + dQ rows of bwd", f, secs,
+         {"projected_full_fwd_bwd_s": secs * (14.0 * 2 * 16 * N * N * d / 2) / f})
+
+
 def main():
     args = parse()
+    if args.oracle_configs:
+        oracle_configs_arm(args)
+        return
     if args.loop:
         loop_arm(args)
         return
