@@ -75,7 +75,7 @@ def parse():
 
 
 # --loop entry points: name -> (forward or backward, call)
-LOOP_ENTRIES = ("fwd", "fwd_2cta", "bwd", "bwd_2cta", "bwd_deterministic")
+LOOP_ENTRIES = ("fwd", "fwd_2cta", "fwd_fp8", "bwd", "bwd_2cta", "bwd_deterministic")
 
 
 def loop_arm(args):
@@ -97,18 +97,23 @@ def loop_arm(args):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
     wsf = fa.fwd_workspace_for(q, causal)
     ws = fa.workspace_for(q, deterministic=args.loop == "bwd_deterministic")
+    ws8 = None
+    if args.loop == "fwd_fp8":
+        ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     calls = {
         "fwd": lambda: fa.fa_fwd(q, k, v, o, lse, scale, causal, wsf),
         "fwd_2cta": lambda: fa.fa_fwd_2cta(q, k, v, o, lse, scale, causal),
+        "fwd_fp8": lambda: fa.fa_fwd_fp8(q, k, v, o, lse, scale, causal, True, ws8),
         "bwd": lambda: fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, scale, causal, ws),
         "bwd_2cta": lambda: fa.fa_bwd_2cta(q, k, v, o, lse, do, dq, dk, dv, scale, causal, ws),
         "bwd_deterministic": lambda: fa.fa_bwd_deterministic(q, k, v, o, lse, do, dq, dk, dv,
                                                              scale, causal, ws),
     }
     call = calls[args.loop]
-    ms = []
+    ms, kern_ms = [], []
+    fa.fa_timing_enable(True)
     for i in range(args.warmup + args.steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -118,6 +123,9 @@ def loop_arm(args):
         e1.synchronize()
         if i >= args.warmup:
             ms.append(e0.elapsed_time(e1))
+            if args.loop in ("fwd", "fwd_fp8"):
+                kern_ms.append(fa.fa_timing_last_ms(fa.KERNEL_FWD))
+    fa.fa_timing_enable(False)
     status = fa.fa_last_device_status()
     if status != fa.FA_OK:
         raise RuntimeError(f"device status {fa.status_string(status)}")
@@ -126,7 +134,8 @@ def loop_arm(args):
     med = statistics.median(ms)
     print(json.dumps({"loop": args.loop, "shape": [B, H, N, d], "causal": causal,
                       "poly": fa.fa_get_exp2_poly_share(), "ms": med,
-                      "tflops": f / med / 1e9, "calls": len(ms)}), flush=True)
+                      "tflops": f / med / 1e9, "calls": len(ms),
+                      "kernel_ms": statistics.median(kern_ms) if kern_ms else None}), flush=True)
 
 
 # DRAM traffic of one launch of the dominant kernel (the backward main kernel)
