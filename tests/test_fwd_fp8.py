@@ -74,9 +74,13 @@ def near_equal_e4m3(a, b, what, frac=2e-3):
         assert np.all(np.abs(a[diff] - b[diff]) <= step * 1.0001), what
 
 
+# B1 H2 N300: every unit of the preparation in a CTA of its own; B2 H8 N2048:
+# more units than resident CTAs, so CTAs take several, across heads and from
+# K to V
+@pytest.mark.parametrize("shape", [(1, 2, 300), (2, 8, 2048)])
 @pytest.mark.parametrize("rotate", [True, False])
-def test_workspace_operands_match_reference_steps(rotate):
-    B, H, N = 1, 2, 300
+def test_workspace_operands_match_reference_steps(rotate, shape):
+    B, H, N = shape
     q, k, v, _ = attention_inputs(B, H, N, 128, seed=11, with_dout=False)
     _, _, ws, _ = run(q, k, v, False, rotate)
     q8, k8, v8t, qdesc, kamax, vamax = decode_workspace(ws, B, H, N)
@@ -118,6 +122,27 @@ def test_against_exact_oracle_and_recipe(N, causal, rotate):
             rec = np.linalg.norm(o[b, h] - o_rec) / np.linalg.norm(o_rec)
             assert rec <= 0.05, f"against the FP8 recipe on the same operands: {rec:.3e}"
             assert np.abs(lse[b, h] - l_rec).max() <= 2e-3
+
+
+def test_workspace_contents_do_not_matter():
+    """The preparation writes every amax slot it reads and the forward every
+    output it reads, so a workspace full of NaN bytes (0xFF) and a zeroed one
+    give bit-identical results."""
+    from exact_attention_98_gb300 import fa
+
+    B, H, N, d = 2, 8, 2048, 128
+    q, k, v, _ = (None if t is None else t.cuda()
+                  for t in attention_inputs(B, H, N, d, seed=5, with_dout=False))
+    outs = []
+    for fill in (0xFF, 0x00):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        ws = torch.full((fa.fa_fwd_fp8_workspace_bytes(B, H, N, d),), fill, dtype=torch.uint8,
+                        device="cuda")
+        fa.fa_fwd_fp8(q, k, v, o, lse, 1 / math.sqrt(d), True, True, ws)
+        assert fa.fa_last_device_status() == fa.FA_OK
+        outs.append((o, lse))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
 def test_rotation_lowers_the_error_with_outlier_channels():
