@@ -9,6 +9,7 @@
 
 #include "fa.h"
 #include "fa_device.cuh"
+#include "fa_bwd_dq.h"
 #include "fa_kernels.h"
 
 namespace fa {
@@ -474,6 +475,9 @@ size_t fa_bwd_deterministic_workspace_bytes(int B, int H, int N, int d) {
   bool empty = false;
   if (check_shape(B, H, N, d, 1.0f, &empty) != FA_OK || empty) return 0;
   const size_t rows = static_cast<size_t>(B) * H * N;
+  // d = 128: D only (dQ from the query-stationary kernel); d = 64: D and the
+  // per-key-tile dQ contributions
+  if (d == 128) return round_up(rows * sizeof(float));
   const size_t n_kblk = (static_cast<size_t>(N) + kBlockN - 1) / kBlockN;
   return round_up(rows * sizeof(float)) + round_up(n_kblk * rows * d * sizeof(float));
 }
@@ -536,6 +540,47 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     if (launch_bwd_pair(pp, s) != cudaSuccess) return FA_ERR_CUDA;
     if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
     if (launch_bwd_post(dq_acc, dq, rows * d, scale, s) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+  }
+
+  if (deterministic && d == 128) {
+    // dK, dV by the key-stationary kernel without its dQ product, then dQ by
+    // query-stationary CTAs that add the key tiles in order in tensor memory
+    BwdParams p;
+    BwdDqParams dp;
+    if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
+        !encode_tile_map(&p.tm_v, v, N, BH, d) || !encode_tile_map(&p.tm_do, dout, N, BH, d) ||
+        !encode_tile_map(&p.tm_dk, dk, N, BH, d) || !encode_tile_map(&p.tm_dv, dv, N, BH, d) ||
+        !encode_tile_map(&dp.tm_dq, dq, N, BH, d))
+      return FA_ERR_CUDA;
+    dp.tm_q = p.tm_q;
+    dp.tm_k = p.tm_k;
+    dp.tm_v = p.tm_v;
+    dp.tm_do = p.tm_do;
+    p.tm_dq = p.tm_q;  // unused without the dQ product
+    p.lse = dp.lse = lse;
+    p.dsum = dp.dsum = dsum;
+    p.dq_acc = nullptr;
+    p.dq_part = nullptr;
+    p.dk = dk;
+    p.dv = dv;
+    p.status = dp.status = status_ptr();
+    if (!p.status) return FA_ERR_CUDA;
+    p.N = dp.N = N;
+    p.BH = dp.BH = BH;
+    p.n_kblk = n_kblk;
+    dp.n_qtiles = (N + kBlockM - 1) / kBlockM;
+    p.causal = dp.causal = causal;
+    p.c = dp.c = scale * 1.4426950408889634f;
+    p.scale = dp.scale = scale;
+    p.inv_scale = dp.inv_scale = 1.0f / scale;
+    p.log2e = 1.4426950408889634f;
+    if (static_cast<long long>(n_kblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    if (launch_bwd_pre(o, dout, dsum, nullptr, rows, d, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (timing_record(1, true, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_bwd_dkdv(p, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_bwd_dq(dp, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
     return FA_OK;
   }
 

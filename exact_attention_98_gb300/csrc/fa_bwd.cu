@@ -1,6 +1,8 @@
 // Backward exact attention for sm_103a: key/value-stationary CTAs, all five
 // GEMMs of a tile on tcgen05 with their accumulators in tensor memory, dQ
-// added into an fp32 accumulator.
+// added into an fp32 accumulator (fa_bwd_kernel).  fa_bwd_dkdv_kernel is the
+// same body at d = 128 without the dQ product, for the deterministic mode
+// (whose dQ comes from the query-stationary kernel of fa_bwd_dq.cu).
 //
 // The pages single out the backward pass as limited by shared-memory traffic
 // and by its reductions and atomic updates ("Pourquoi l'approche standard ne
@@ -67,14 +69,21 @@
 namespace fa {
 namespace {
 
-template <int D>
+template <int D, bool kNoDQ = false>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
+  static_assert(!kNoDQ || D == 128, "dK/dV-only mode: d = 128");
+  // kNoDQ: dK and dV only (the deterministic mode's first pass; dQ comes
+  // from the query-stationary kernel): no dQ product, no dS copy in shared
+  // memory, no drain, and the next tile's S^T right after dV_i.
+  static constexpr bool kDQ = !kNoDQ;
   static constexpr int kThreads = 512;
   static constexpr int kLaunchRegs = 128;
   static constexpr int kComputeRegs = 144;  // 2 x 128 threads
-  static constexpr int kDrainRegs = 144;    // 128 threads: a whole dQ^T row in registers
-  static constexpr int kOtherRegs = 80;     // 128 threads (load, MMA): no spills
+  // 128 threads: a whole dQ^T row in registers (kNoDQ: idle, their share
+  // goes to the loader and the MMA warp)
+  static constexpr int kDrainRegs = kNoDQ ? 24 : 144;
+  static constexpr int kOtherRegs = kNoDQ ? 152 : 80;  // 128 threads (load, MMA): no spills
   static_assert(2 * 128 * kComputeRegs + 128 * kDrainRegs + 128 * kOtherRegs <=
                     kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
@@ -91,7 +100,7 @@ struct BwdCfg {
   // where dQ_i has tensor-memory columns of its own (so dP^T_{i+1} does not
   // wait for its drain) and a third stage gives the next Q tile its lead.
   // At d = 128 tensor memory is full and measured slower (8%).
-  static constexpr bool kEarlyS = (D == 64);
+  static constexpr bool kEarlyS = (D == 64) || kNoDQ;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTileBytes;
   static constexpr int kQOff = 2 * kTileBytes;                     // kStages tiles
@@ -189,10 +198,11 @@ enum : unsigned int {
   kSiteDSTmem = 0x20C,
 };
 
-template <int D>
-__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
-    fa_bwd_kernel(const __grid_constant__ BwdParams p) {
-  using C = BwdCfg<D>;
+// The kernel body; fa_bwd_kernel<D> (all five products) and
+// fa_bwd_dkdv_kernel (d = 128, dK and dV only) below are its two entry points.
+template <int D, bool kNoDQ>
+__device__ __forceinline__ void bwd_body(const BwdParams& p) {
+  using C = BwdCfg<D, kNoDQ>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
@@ -410,15 +420,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (!(ok = mbar_wait(bar(C::kBarDSTmem), it & 1, ctl, kSiteDSTmem))) break;
         tc_fence_after();
         issue_tn(C::kColDP, q_s, C::kColDK, it > 0);
-        if (!(ok = mbar_wait(bar(C::kBarDSFull), it & 1, ctl, kSiteDSFull))) break;
-        if (C::kEarlyS && it > 0) {  // the drain has read dQ_{i-1} from its columns
-          if (!(ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl, kSiteDQEmpty))) break;
-          tc_fence_after();
+        if constexpr (C::kDQ) {
+          if (!(ok = mbar_wait(bar(C::kBarDSFull), it & 1, ctl, kSiteDSFull))) break;
+          if (C::kEarlyS && it > 0) {  // the drain has read dQ_{i-1} from its columns
+            if (!(ok = mbar_wait(bar(C::kBarDQEmpty), (it - 1) & 1, ctl, kSiteDQEmpty))) break;
+            tc_fence_after();
+          }
+          issue_dq(sbase + C::ds_off(it));
+          mma_commit(bar(C::kBarDQFull));
         }
-        issue_dq(sbase + C::ds_off(it));
-        mma_commit(bar(C::kBarDQFull));
-        // With the transposed dQ the drain needs no shared memory: dQ_i was
-        // the last reader of the stage.  Otherwise the drain returns it.
+        // With the transposed dQ the drain needs no shared memory: dQ_i (or,
+        // without dQ, dK_i) was the last reader of the stage.  Otherwise the
+        // drain returns it.
         if (C::kDqTransposed) mma_commit(bar(C::kBarStEmpty + s));
       }
       mma_commit(bar(C::kBarMmaDone));
@@ -426,6 +439,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
   } else if (warp >= C::kDrainWarp0) {
     regs_set<C::kDrainRegs, C::kLaunchRegs>();
+    if constexpr (C::kDQ) {
     // ------------------------------------------------------------- dQ drain
     const int quarter = warp & 3;
     const int qr = quarter * 32 + lane;  // query row within the tile
@@ -454,6 +468,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // dQ_i^T has left tensor memory: the MMA may write the columns again.
         tc_fence_before();
         mbar_arrive(bar(C::kBarDQEmpty));
+        // (The per-key-tile store branch is not taken at d = 128 any more:
+        // the deterministic mode computes dQ with its own kernel there.  The
+        // drain without it measured 2% slower, so it stays.)
         if (det) {  // this key tile's contribution, summed later in key-tile order
 #pragma unroll
           for (int qc = 0; qc < kBlockM; ++qc)
@@ -526,6 +543,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
     }
     if (leader) bulk_wait<0>();
+    }
     }
   } else {
     regs_set<C::kComputeRegs, C::kLaunchRegs>();
@@ -634,6 +652,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::kBarDSTmem));
+      if constexpr (C::kDQ) {  // the dS copy for the dQ product
       if constexpr (C::kDsInDO) {  // dV_i must be done reading dO_i
         ok = mbar_wait(bar(C::kBarDVDone), it & 1, ctl, kSiteDVDone);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -653,6 +672,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(C::kBarDSFull));
+      }
     }
 
     // Epilogue: warpgroup 0 writes dV, warpgroup 1 dK (times the softmax
@@ -716,19 +736,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 }
 
 template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+  bwd_body<D, false>(p);
+}
+
+__global__ void __launch_bounds__(BwdCfg<128, true>::kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  bwd_body<128, true>(p);
+}
+
+template <int D, bool kNoDQ = false>
 cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, kNoDQ>;
+  void (*kernel)(BwdParams) = kNoDQ ? fa_bwd_dkdv_kernel : fa_bwd_kernel<D>;
   // The setmaxnreg split assumes the launch allocation; refuse to run a build
   // whose register count differs (an over-committed split would never finish).
   cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, fa_bwd_kernel<D>);
+  cudaError_t err = cudaFuncGetAttributes(&attr, kernel);
   if (err != cudaSuccess) return err;
   if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(p.n_kblk) * p.BH;
-  err = launch_dependent(fa_bwd_kernel<D>, dim3(static_cast<unsigned int>(blocks)), dim3(C::kThreads),
+  err = launch_dependent(kernel, dim3(static_cast<unsigned int>(blocks)), dim3(C::kThreads),
                          C::kSmemBytes, stream, p);
   if (err != cudaSuccess) return err;
   return launched(1);
@@ -740,6 +772,10 @@ cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream) {
   if (d == 128) return launch_bwd_d<128>(p, stream);
   if (d == 64) return launch_bwd_d<64>(p, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_dkdv(const BwdParams& p, cudaStream_t stream) {
+  return launch_bwd_d<128, true>(p, stream);
 }
 
 }  // namespace fa

@@ -197,6 +197,9 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* 
                            long long rows, int d, cudaStream_t stream);
 // Backward main kernel (key/value stationary).
 cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
+// The same kernel computing dK and dV only (d = 128; p.tm_dq, p.dq_acc and
+// p.dq_part unused): the deterministic mode's first pass.
+cudaError_t launch_bwd_dkdv(const BwdParams& p, cudaStream_t stream);
 // dQ = mul * dQ accumulator -> bf16 (mul: the softmax scale, which the main
 // kernels leave out of dS).
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, float mul,

@@ -55,9 +55,8 @@ def test_workspace_bytes(lib):
     assert ws(0, 1, 1, 64) == 0
     assert ws(1, 1, 1, 96) == 0  # unsupported head dim
     det = lib.fa_bwd_deterministic_workspace_bytes
-    n_kblk = (N + 127) // 128
-    assert det(B, H, N, d) == up(4 * rows) + up(4 * rows * d * n_kblk)
-    assert det(1, 1, 129, 64) == up(4 * 129) + up(4 * 129 * 64 * 2)
+    assert det(B, H, N, d) == up(4 * rows)  # d = 128: D only
+    assert det(1, 1, 129, 64) == up(4 * 129) + up(4 * 129 * 64 * 2)  # d = 64: D and parts
     assert det(0, 1, 1, 64) == 0
 
 
