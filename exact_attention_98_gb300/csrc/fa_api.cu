@@ -573,7 +573,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     p.causal = dp.causal = causal;
     p.c = dp.c = scale * 1.4426950408889634f;
     p.scale = dp.scale = scale;
-    p.inv_scale = dp.inv_scale = 1.0f / scale;
+    p.inv_scale = 1.0f / scale;
     p.log2e = 1.4426950408889634f;
     if (static_cast<long long>(n_kblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     if (launch_bwd_pre(o, dout, dsum, nullptr, rows, d, s) != cudaSuccess) return FA_ERR_CUDA;

@@ -6,12 +6,12 @@
 // Per query tile i (128 rows) the CTA keeps Q_i and dO_i in shared memory and
 // streams K_j through three slots and V_j through one (K_j is read by S_j
 // and, at the end of the tile's chain, by dQ_j, while S_{j+1} is wanted
-// early; V_j only by dP_j); with LSE_i and D_i entering
-// as rank-1 bias products (as in the key-stationary kernel):
-//   S_j  = Q_i K_j^T - LSE_i / scale      (tensor memory, lane = query)
-//   P_j  = exp2(c S_j)                     (registers only)
-//   dP_j = dO_i V_j^T - D_i                (tensor memory)
-//   dS_j = P_j dP_j -> bf16 over dP_j      (tensor memory)
+// early; V_j only by dP_j).  A thread owns one query row, so it subtracts
+// that row's LSE and D itself (in fp32):
+//   S_j  = Q_i K_j^T                       (tensor memory, lane = query)
+//   P_j  = exp2(c S_j - LSE_i log2 e)      (registers only)
+//   dP_j = dO_i V_j^T                      (tensor memory)
+//   dS_j = P_j (dP_j - D_i) -> bf16 over dP_j (tensor memory)
 //   dQ  += dS_j K_j                        (tensor memory accumulator)
 // and at the end dQ_i * scale -> bf16, written by bulk tensor stores.
 //
@@ -53,16 +53,7 @@ struct DqCfg {
   static constexpr int kDOOff = kTileBytes;
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kKSlots * kTileBytes;
-  // bias operands: A = bias rows (128 queries x 16 bf16: -LSE / scale, then
-  // -D, as hi + lo in entries 0 and 1), B = ones (128 keys x 16); K-major
-  // without swizzle: [8-row group][K half][row mod 8][16 bytes] -> LBO =
-  // 128 B, SBO = 256 B
-  static constexpr int kBiasTileBytes = 128 * 16 * 2;
-  static constexpr int kBiasLbo = 128;
-  static constexpr int kBiasSbo = 256;
-  static constexpr int kOnesOff = kVOff + kTileBytes;
-  static constexpr int kBiasOff = kOnesOff + kBiasTileBytes;  // [lse, d]
-  static constexpr int kBarOff = kBiasOff + 2 * kBiasTileBytes;
+  static constexpr int kBarOff = kVOff + kTileBytes;
   static constexpr int kBarQFull = 0;
   static constexpr int kBarKFull = 1;                    // [kKSlots]
   static constexpr int kBarKEmpty = kBarKFull + kKSlots;  // [kKSlots]
@@ -134,7 +125,7 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(bar(C::kBarQFull), 2);
+    mbar_init(bar(C::kBarQFull), 1);
     for (int s = 0; s < C::kKSlots; ++s) {
       mbar_init(bar(C::kBarKFull + s), 1);
       mbar_init(bar(C::kBarKEmpty + s), 1);
@@ -148,13 +139,6 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
     mbar_init(bar(C::kBarMmaDone), 1);
     fence_mbar_init();
   }
-  // B = ones; the A bias tiles start at zero and the loader writes only the
-  // two hi/lo entries of each row
-  for (int w = threadIdx.x; w < C::kBiasTileBytes / 4; w += C::kThreads)
-    reinterpret_cast<uint32_t*>(smem + C::kOnesOff)[w] = 0x3F803F80u;  // bf16 1.0 pairs
-  for (int w = threadIdx.x; w < 2 * C::kBiasTileBytes / 4; w += C::kThreads)
-    reinterpret_cast<uint32_t*>(smem + C::kBiasOff)[w] = 0u;
-  fence_proxy_async_smem();
   if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -180,26 +164,6 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
                       bh);
         }
       }
-      // bias rows: -LSE_q / scale (raw score units) and -D_q, as bf16 hi +
-      // lo; rows past N get -10^4 (P = 0 there) and D = 0
-      uint8_t* bias_lse = smem + C::kBiasOff;
-      uint8_t* bias_d = bias_lse + C::kBiasTileBytes;
-#pragma unroll
-      for (int r4 = 0; r4 < 4; ++r4) {
-        const int rr = r4 * 32 + lane;
-        const int q = q0 + rr;
-        const size_t gi = static_cast<size_t>(bh) * p.N + q;
-        const float vl = (q < p.N) ? -p.lse[gi] * p.inv_scale : -1.0e4f;
-        const float vd = (q < p.N) ? -p.dsum[gi] : 0.0f;
-        const int off = (rr >> 3) * C::kBiasSbo + (rr & 7) * 16;
-        const float lh = __bfloat162float(__float2bfloat16_rn(vl));
-        const float dh = __bfloat162float(__float2bfloat16_rn(vd));
-        *reinterpret_cast<uint32_t*>(bias_lse + off) = pack_bf16x2(lh, vl - lh);
-        *reinterpret_cast<uint32_t*>(bias_d + off) = pack_bf16x2(dh, vd - dh);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kBarQFull));
       // K_j into slot j mod 3 once K_{j-3} is released (after dQ_{j-3}),
       // V_j into its slot once V_{j-1} is (after dP_{j-1}); in the order
       // K_0, K_1, V_0, then K_{j+2}, V_{j+1} for j = 0, 1, ...
@@ -265,12 +229,6 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
           mma_ss(tmem_base + dcol, step(ad, off), step(bd, off), kIdescS, kk > 0 ? 1u : 0u);
         }
       };
-      // X += b ones^T: the rank-1 bias (which = 0: -LSE / scale, 1: -D)
-      auto issue_bias = [&](int which, uint32_t dcol) {
-        mma_ss(tmem_base + dcol,
-               sdesc_plain(sbase + C::kBiasOff + which * C::kBiasTileBytes, C::kBiasLbo, C::kBiasSbo),
-               sdesc_plain(sbase + C::kOnesOff, C::kBiasLbo, C::kBiasSbo), kIdescS, 1u);
-      };
       // dQ += dS_j K_j: A = dS_j (bf16, packed in the dP columns), B = K_j as
       // an MN-major operand (d contiguous): K = 128 keys, N = d.
       auto issue_dq = [&](uint32_t k0_smem, bool accumulate) {
@@ -285,7 +243,6 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
           return false;
         tc_fence_after();
         issue_nt(q_smem, k_addr(j), C::kColS);
-        issue_bias(0, C::kColS);
         mma_commit(bar(C::kBarSFull));
         return true;
       };
@@ -293,7 +250,6 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
         if (!mbar_wait(bar(C::kBarVFull), j & 1, ctl, kSiteFull)) return false;
         tc_fence_after();
         issue_nt(do_smem, sbase + C::kVOff, C::kColDP);
-        issue_bias(1, C::kColDP);
         mma_commit(bar(C::kBarDPFull));
         mma_commit(bar(C::kBarVEmpty));  // V_j: read by dP_j only
         return true;
@@ -325,6 +281,12 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
     const int row = quarter * 32 + lane;  // query row within the tile
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const f32x2 c2 = f2_pack(p.c, p.c);
+    // this row's -LSE log2(e) and -D; a row past N gets -inf (P = 0)
+    const int qrow = q0 + row;
+    const float nl = qrow < p.N ? -p.lse[static_cast<size_t>(bh) * p.N + qrow] * 1.4426950408889634f
+                                : -INFINITY;
+    const float nd = qrow < p.N ? -p.dsum[static_cast<size_t>(bh) * p.N + qrow] : 0.0f;
+    const f32x2 nl2 = f2_pack(nl, nl), nd2 = f2_pack(nd, nd);
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int kbase = j * kBlockN + wg * 64;  // first key of this warpgroup's columns
@@ -345,15 +307,15 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::kBarSFree));
-      // P = exp2(c S'), S' = S - LSE / scale by the bias product
+      // P = exp2(c S - LSE log2 e)
       float pf[64];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
         for (int e2 = 0; e2 < 16; ++e2) {
           float x0, x1;
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
-                           c2),
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
+                           c2, nl2),
                     x0, x1);
           pf[ch * 32 + 2 * e2] = ex2_mufu(x0);
           pf[ch * 32 + 2 * e2 + 1] = ex2_mufu(x1);
@@ -363,7 +325,7 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
         for (int e = 0; e < 64; ++e)
           if (e >= lim) pf[e] = 0.0f;
       }
-      // dS = P dP', dP' = dP - D by the bias product; bf16, packed over dP
+      // dS = P (dP - D); bf16, packed over dP
       ok = mbar_wait(bar(C::kBarDPFull), j & 1, ctl, kSiteDPFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -381,7 +343,9 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
           // from the P that its dV product uses
           const uint32_t pb = pack_bf16x2(pf[ch * 32 + 2 * e2], pf[ch * 32 + 2 * e2 + 1]);
           float a0, a1;
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(dr[ch][2 * e2]), __uint_as_float(dr[ch][2 * e2 + 1])),
+          f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(dr[ch][2 * e2]),
+                                          __uint_as_float(dr[ch][2 * e2 + 1])),
+                                  nd2),
                            f2_pack(__uint_as_float(pb << 16), __uint_as_float(pb & 0xFFFF0000u))),
                     a0, a1);
           w[e2] = pack_bf16x2(a0, a1);

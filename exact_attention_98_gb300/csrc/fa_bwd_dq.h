@@ -20,7 +20,6 @@ struct BwdDqParams {
   int causal;
   float c;          // scale * log2(e)
   float scale;      // dQ = scale * sum_j dS_j K_j
-  float inv_scale;  // -LSE / scale is the bias in raw score units
 };
 
 // One CTA per (head, 128-row query tile): dQ_i = scale * sum_j dS_ij K_j
