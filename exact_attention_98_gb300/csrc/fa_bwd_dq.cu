@@ -24,7 +24,8 @@
 // Warp roles (384 threads): warps 0-7 compute (two warpgroups, thread =
 // query row, warpgroup w takes key columns [64 w, 64 w + 64) of every key
 // tile; in the epilogue d columns [64 w, 64 w + 64) of dQ), warp 8 loads,
-// warp 9 allocates tensor memory and issues every MMA (lane 0).
+// warp 9 allocates tensor memory and issues every MMA (the whole warp runs
+// the loop, an elected lane issues).
 //
 // MMA order, key tile j:
 //   [compute has read S_j] S_{j+1} ; [dS_j] dQ += dS_j K_j ; dP_{j+1}
@@ -206,7 +207,9 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
           mbar_wait_drain(bar(C::kBarKFull + kt % C::kKSlots), (kt / C::kKSlots) & 1);
         if (v_issued > 0) mbar_wait_drain(bar(C::kBarVFull), (v_issued - 1) & 1);
       }
-    } else if (warp == C::kMmaWarp && lane == 0) {
+    } else if (warp == C::kMmaWarp) {
+      // The whole warp runs the issue loop (its waits warp-uniform); one
+      // lane chosen by elect.sync issues each MMA and commit.
       // ----------------------------------------------------------- MMA issue
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBlockM, kBlockN, false, false);  // S, dP
       constexpr uint32_t kIdescQ = idesc_bf16_f32(kBlockM, D, false, true);         // dQ
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          mma_ss(tmem_base + dcol, step(ad, off), step(bd, off), kIdescS, kk > 0 ? 1u : 0u);
+          mma_ss<true>(tmem_base + dcol, step(ad, off), step(bd, off), kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       // dQ += dS_j K_j: A = dS_j (bf16, packed in the dP columns), B = K_j as
@@ -235,42 +238,42 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
         const uint64_t bd = base(sdesc_sw128(k0_smem, C::kHalfBytes, 1024));
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem_base + C::kColDQ, tmem_base + C::kColDP + C::packed_col(kk),
+          mma_ts<true>(tmem_base + C::kColDQ, tmem_base + C::kColDP + C::packed_col(kk),
                  step(bd, kk * 2048), kIdescQ, (accumulate || kk > 0) ? 1u : 0u);
       };
       auto issue_s = [&](int j) -> bool {
-        if (!mbar_wait(bar(C::kBarKFull + j % C::kKSlots), (j / C::kKSlots) & 1, ctl, kSiteFull))
+        if (!mbar_wait_warp(bar(C::kBarKFull + j % C::kKSlots), (j / C::kKSlots) & 1, ctl, kSiteFull))
           return false;
         tc_fence_after();
         issue_nt(q_smem, k_addr(j), C::kColS);
-        mma_commit(bar(C::kBarSFull));
+        mma_commit<true>(bar(C::kBarSFull));
         return true;
       };
       auto issue_dp = [&](int j) -> bool {
-        if (!mbar_wait(bar(C::kBarVFull), j & 1, ctl, kSiteFull)) return false;
+        if (!mbar_wait_warp(bar(C::kBarVFull), j & 1, ctl, kSiteFull)) return false;
         tc_fence_after();
         issue_nt(do_smem, sbase + C::kVOff, C::kColDP);
-        mma_commit(bar(C::kBarDPFull));
-        mma_commit(bar(C::kBarVEmpty));  // V_j: read by dP_j only
+        mma_commit<true>(bar(C::kBarDPFull));
+        mma_commit<true>(bar(C::kBarVEmpty));  // V_j: read by dP_j only
         return true;
       };
-      bool ok = mbar_wait(bar(C::kBarQFull), 0, ctl, kSiteQFull);
+      bool ok = mbar_wait_warp(bar(C::kBarQFull), 0, ctl, kSiteQFull);
       if (ok) {
         tc_fence_after();
         ok = issue_s(0) && issue_dp(0);
       }
       for (int j = 0; ok && j < n; ++j) {
         // S_{j+1} once the compute warps have read S_j into registers
-        if (!(ok = mbar_wait(bar(C::kBarSFree), j & 1, ctl, kSiteSFree))) break;
+        if (!(ok = mbar_wait_warp(bar(C::kBarSFree), j & 1, ctl, kSiteSFree))) break;
         tc_fence_after();
         if (j + 1 < n && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(bar(C::kBarDSFull), j & 1, ctl, kSiteDSFull))) break;
+        if (!(ok = mbar_wait_warp(bar(C::kBarDSFull), j & 1, ctl, kSiteDSFull))) break;
         tc_fence_after();
         issue_dq(k_addr(j), j > 0);
-        mma_commit(bar(C::kBarKEmpty + j % C::kKSlots));  // K_j: read by S_j and dQ_j
+        mma_commit<true>(bar(C::kBarKEmpty + j % C::kKSlots));  // K_j: read by S_j and dQ_j
         if (j + 1 < n && !(ok = issue_dp(j + 1))) break;
       }
-      mma_commit(bar(C::kBarMmaDone));
+      mma_commit<true>(bar(C::kBarMmaDone));
       if (!ok) mbar_wait_drain(bar(C::kBarMmaDone), 0);
     }
   } else {
