@@ -101,6 +101,14 @@ struct BwdCfg {
   // wait for its drain) and a third stage gives the next Q tile its lead.
   // At d = 128 tensor memory is full and measured slower (8%).
   static constexpr bool kEarlyS = (D == 64) || kNoDQ;
+  // -LSE and -D: at d = 128 a rank-1 bias product each onto S^T and dP^T,
+  // so that the compute warps, on the tile's critical path, do no per-query
+  // work; at d = 64, where the products are the tighter resource, fp32 rows
+  // in shared memory that the compute warps apply themselves (two products
+  // per tile fewer: +3 to +4%; at d = 128 the same change measured 5-7%
+  // slower).  The d = 128 dK/dV-only form keeps the bias products, so that
+  // its dK and dV stay those of the full kernel bit for bit.
+  static constexpr bool kRowLse = (D == 64);
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTileBytes;
   static constexpr int kQOff = 2 * kTileBytes;                     // kStages tiles
@@ -293,6 +301,20 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
                         bar(C::kBarStFull + s), h * 64, q0, bh);
           }
         }
+        if constexpr (C::kRowLse) {
+          // fp32 rows -LSE_q log2 e and -D_q (at the start of the stage's
+          // bias space); rows past N get -inf (P = 0 there) and D = 0
+          float* row_l = reinterpret_cast<float*>(smem + C::kBiasOff) + (2 * s) * kBlockM;
+          float* row_d = row_l + kBlockM;
+#pragma unroll
+          for (int r4 = 0; r4 < 4; ++r4) {
+            const int r = r4 * 32 + lane;
+            const int q = q0 + r;
+            const size_t gi = static_cast<size_t>(bh) * p.N + q;
+            row_l[r] = (q < p.N) ? -p.lse[gi] * p.log2e : -INFINITY;
+            row_d[r] = (q < p.N) ? -p.dsum[gi] : 0.0f;
+          }
+        } else {
         // Bias rows: -LSE_q / scale (raw score units, so that c (S^T + b)
         // = S^T c - LSE_q log2 e) and -D_q, each as bf16 hi + lo.  Rows past
         // N get a bias of -10^4 (P = 0 there) and D = 0.
@@ -312,6 +334,7 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
           *reinterpret_cast<uint32_t*>(bias_d + off) = pack_bf16x2(dh, vd - dh);
         }
         fence_proxy_async_smem();
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::kBarStFull + s));
         issued = it + 1;
@@ -391,7 +414,7 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
         if (!mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull)) return false;
         tc_fence_after();
         issue_nt(k_smem, sbase + C::kQOff + s * C::kTileBytes, C::kColS);
-        issue_bias(2 * s, C::kColS);
+        if constexpr (!C::kRowLse) issue_bias(2 * s, C::kColS);
         mma_commit(bar(C::kBarSFull));
         return true;
       };
@@ -407,7 +430,7 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
           tc_fence_after();
         }
         issue_nt(v_smem, do_s, C::kColDP);
-        issue_bias(2 * s + 1, C::kColDP);
+        if constexpr (!C::kRowLse) issue_bias(2 * s + 1, C::kColDP);
         mma_commit(bar(C::kBarDPFull));
         if (!(ok = mbar_wait(bar(C::kBarPFull), it & 1, ctl, kSitePFull))) break;
         tc_fence_after();
@@ -564,6 +587,16 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
       ok = mbar_wait(bar(C::kBarSFull), it & 1, ctl, kSiteSFull);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
+      // kRowLse: S^T_i was issued after stage s landed, so this wait returns
+      // at once; it makes the loader's LSE / D rows of the stage visible
+      if constexpr (C::kRowLse) {
+        ok = mbar_wait(bar(C::kBarStFull + s), (it / C::kStages) & 1, ctl, kSiteStFull);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      }
+      // this warpgroup's 64 queries' -LSE log2 e and -D (kRowLse)
+      const float4* rl4 =
+          reinterpret_cast<const float4*>(smem + C::kBiasOff) + (2 * s) * (kBlockM / 4) + wg * 16;
+      const float4* rd4 = rl4 + kBlockM / 4;
 
       // P^T = exp2(c S'^T), S'^T = S^T - LSE / scale by the bias MMA; masked
       // entries (query < key on the diagonal tile, keys past N) are 0.
@@ -577,9 +610,17 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
       uint32_t pw[32];
       auto exp_pair = [&](int ch, int e2, float& p0, float& p1) {
         float x0, x1;
-        f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
-                         c2),
-                  x0, x1);
+        if constexpr (C::kRowLse) {
+          const float4 l4 = rl4[ch * 8 + (e2 >> 1)];
+          const f32x2 nl = (e2 & 1) ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
+                           c2, nl),
+                    x0, x1);
+        } else {
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(sr[ch][2 * e2]), __uint_as_float(sr[ch][2 * e2 + 1])),
+                           c2),
+                    x0, x1);
+        }
         p0 = ex2_mufu(x0);
         p1 = ex2_mufu(x1);
       };
@@ -637,10 +678,13 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
 #pragma unroll
         for (int e2 = 0; e2 < 16; ++e2) {
           float a0, a1;
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(dr[ch][2 * e2]),
-                                   __uint_as_float(dr[ch][2 * e2 + 1])),
-                           f2_pack(__uint_as_float(pw[ch * 16 + e2] << 16),
-                                   __uint_as_float(pw[ch * 16 + e2] & 0xFFFF0000u))),
+          f32x2 dp = f2_pack(__uint_as_float(dr[ch][2 * e2]), __uint_as_float(dr[ch][2 * e2 + 1]));
+          if constexpr (C::kRowLse) {
+            const float4 d4 = rd4[ch * 8 + (e2 >> 1)];
+            dp = f2_add(dp, (e2 & 1) ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y));
+          }
+          f2_unpack(f2_mul(dp, f2_pack(__uint_as_float(pw[ch * 16 + e2] << 16),
+                                       __uint_as_float(pw[ch * 16 + e2] & 0xFFFF0000u))),
                     a0, a1);
           dsw[ch * 16 + e2] = pack_bf16x2(a0, a1);
         }
