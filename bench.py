@@ -140,17 +140,17 @@ def loop_arm(args):
 
 # DRAM traffic of one launch of the dominant kernel (the backward main kernel)
 # on this workload: dram__bytes_read.sum + dram__bytes_write.sum from one
-# `ncu --set full` capture (cold cache) of B1 H4 N32768 d128 (214849792 +
-# 94259456 bytes), times 4 for the 16 independent heads of the headline (the
-# full-size launch is too large to capture).  It describes the kernel built
-# from the sources whose digest is recorded with it, and is reported as null
-# as soon as any of them changes.
+# `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum` capture (cold
+# cache) of B1 H4 N32768 d128 (214669824 + 95447552 bytes), times 4 for the
+# 16 independent heads of the headline (the full-size launch is too large to
+# capture).  It describes the kernel built from the sources whose digest is
+# recorded with it, and is reported as null as soon as any of them changes.
 NCU_TRAFFIC = {
     "kernel": "fa_bwd_kernel<128>",
     "workload": WORKLOAD_NAME,
-    "bytes": 4 * (214849792 + 94259456),
+    "bytes": 4 * (214669824 + 95447552),
     "captured": "B1 H4 N32768 d128, scaled by 4",
-    "sources_sha256": "9bdfc0245321907b965c0a984e04990602cac3cad2dae6dc2a478118195f225b",
+    "sources_sha256": "4ddb179edb48cc48e2c39715058473acab4254171bf57b4fbf1bdb10c8058da1",
 }
 KERNEL_SOURCES = ("fa_bwd.cu", "fa_device.cuh", "fa_kernels.h", "exp2_poly_coeffs.h")
 
