@@ -7,7 +7,9 @@ first and the last head (the largest offsets) are compared with the fp64
 oracle on sampled rows: O and LSE element by element, dQ rows by relative
 Frobenius error; dK and dV of those heads through the properties that hold
 at any size (dK rows sum to zero, dV rows sum to the dO rows).  The 2-CTA
-backward must stay within rounding of the backward on those heads, the 2-CTA
+backward must stay within rounding of the backward on those heads, the
+deterministic backward must equal it on dK and dV and stay within rounding
+on dQ, the 2-CTA
 forward must equal the forward bit for bit, and the FP8 forward must stay
 within its bounds."""
 import math
@@ -74,7 +76,17 @@ def test_forward_backward(big):
         for a, b in ((dk, dk2), (dv, dv2)):
             assert rel_fro(head64(b, h), head64(a, h)) <= 2e-3, h
         assert rel_fro(to64(dq2[0, h])[rows], to64(dq[0, h])[rows]) <= 2e-3, h
-    del dq, dk, dv, dq2, dk2, dv2
+    del dq2, dk2, dv2
+    # the deterministic backward (d = 128: dK/dV pass and query-stationary dQ
+    # kernel, 139264 CTAs each): dK and dV equal fa_bwd's bit for bit, dQ
+    # within rounding on the sampled rows
+    dq3, dk3, dv3 = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale, deterministic=True)
+    assert fa.fa_last_device_status() == fa.FA_OK
+    assert torch.equal(dk3, dk) and torch.equal(dv3, dv)
+    for h in (0, H - 1):
+        rows = sampled_rows(N, 64, 0, h, H)
+        assert rel_fro(to64(dq3[0, h])[rows], to64(dq[0, h])[rows]) <= 2e-3, h
+    del dq, dk, dv, dq3, dk3, dv3
     # the 2-CTA forward: the same products and per-row arithmetic
     o2, lse2 = fa.forward(q, k, v, causal=True, scale=scale, two_cta=True)
     assert fa.fa_last_device_status() == fa.FA_OK
