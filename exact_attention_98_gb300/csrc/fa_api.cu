@@ -475,11 +475,9 @@ size_t fa_bwd_deterministic_workspace_bytes(int B, int H, int N, int d) {
   bool empty = false;
   if (check_shape(B, H, N, d, 1.0f, &empty) != FA_OK || empty) return 0;
   const size_t rows = static_cast<size_t>(B) * H * N;
-  // d = 128: D only (dQ from the query-stationary kernel); d = 64: D and the
-  // per-key-tile dQ contributions
-  if (d == 128) return round_up(rows * sizeof(float));
-  const size_t n_kblk = (static_cast<size_t>(N) + kBlockN - 1) / kBlockN;
-  return round_up(rows * sizeof(float)) + round_up(n_kblk * rows * d * sizeof(float));
+  // D only: dQ comes from the query-stationary kernel, accumulated in
+  // tensor memory
+  return round_up(rows * sizeof(float));
 }
 
 namespace {
@@ -543,7 +541,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     return FA_OK;
   }
 
-  if (deterministic && d == 128) {
+  if (deterministic) {
     // dK, dV by the key-stationary kernel without its dQ product, then dQ by
     // query-stationary CTAs that add the key tiles in order in tensor memory
     BwdParams p;
@@ -578,8 +576,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
     if (static_cast<long long>(n_kblk) * BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     if (launch_bwd_pre(o, dout, dsum, nullptr, rows, d, s) != cudaSuccess) return FA_ERR_CUDA;
     if (timing_record(1, true, s) != cudaSuccess) return FA_ERR_CUDA;
-    if (launch_bwd_dkdv(p, s) != cudaSuccess) return FA_ERR_CUDA;
-    if (launch_bwd_dq(dp, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_bwd_dkdv(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (launch_bwd_dq(dp, d, s) != cudaSuccess) return FA_ERR_CUDA;
     if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
     return FA_OK;
   }
@@ -588,13 +586,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   if (!encode_tile_map(&p.tm_q, q, N, BH, d) || !encode_tile_map(&p.tm_k, k, N, BH, d) ||
       !encode_tile_map(&p.tm_v, v, N, BH, d) || !encode_tile_map(&p.tm_do, dout, N, BH, d) ||
       !encode_tile_map(&p.tm_dk, dk, N, BH, d) || !encode_tile_map(&p.tm_dv, dv, N, BH, d) ||
-      !encode_dq_map(&p.tm_dq, dq_buf, N,
-                     deterministic ? static_cast<long long>(n_kblk) * BH : BH, d))
+      !encode_dq_map(&p.tm_dq, dq_buf, N, BH, d))
     return FA_ERR_CUDA;
   p.lse = lse;
   p.dsum = dsum;
   p.dq_acc = dq_acc;
-  p.dq_part = deterministic ? dq_buf : nullptr;
+  p.dq_part = nullptr;
   p.dk = dk;
   p.dv = dv;
   p.status = status_ptr();
@@ -613,12 +610,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   if (timing_record(1, true, s) != cudaSuccess) return FA_ERR_CUDA;
   if (launch_bwd_main(p, d, s) != cudaSuccess) return FA_ERR_CUDA;
   if (timing_record(1, false, s) != cudaSuccess) return FA_ERR_CUDA;
-  if (deterministic) {
-    if (launch_bwd_dq_reduce(dq_buf, dq, BH, N, d, n_kblk, causal, scale, s) != cudaSuccess)
-      return FA_ERR_CUDA;
-  } else if (launch_bwd_post(dq_acc, dq, rows * d, scale, s) != cudaSuccess) {
-    return FA_ERR_CUDA;
-  }
+  if (launch_bwd_post(dq_acc, dq, rows * d, scale, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 

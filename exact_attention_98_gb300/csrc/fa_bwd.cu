@@ -1,8 +1,8 @@
 // Backward exact attention for sm_103a: key/value-stationary CTAs, all five
 // GEMMs of a tile on tcgen05 with their accumulators in tensor memory, dQ
 // added into an fp32 accumulator (fa_bwd_kernel).  fa_bwd_dkdv_kernel is the
-// same body at d = 128 without the dQ product, for the deterministic mode
-// (whose dQ comes from the query-stationary kernel of fa_bwd_dq.cu).
+// same body without the dQ product, for the deterministic mode (whose dQ
+// comes from the query-stationary kernel of fa_bwd_dq.cu).
 //
 // The pages single out the backward pass as limited by shared-memory traffic
 // and by its reductions and atomic updates ("Pourquoi l'approche standard ne
@@ -72,7 +72,6 @@ namespace {
 template <int D, bool kNoDQ = false>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(!kNoDQ || D == 128, "dK/dV-only mode: d = 128");
   // kNoDQ: dK and dV only (the deterministic mode's first pass; dQ comes
   // from the query-stationary kernel): no dQ product, no dS copy in shared
   // memory, no drain, and the next tile's S^T right after dV_i.
@@ -207,7 +206,7 @@ enum : unsigned int {
 };
 
 // The kernel body; fa_bwd_kernel<D> (all five products) and
-// fa_bwd_dkdv_kernel (d = 128, dK and dV only) below are its two entry points.
+// fa_bwd_dkdv_kernel<D> (dK and dV only) below are its two entry points.
 template <int D, bool kNoDQ>
 __device__ __forceinline__ void bwd_body(const BwdParams& p) {
   using C = BwdCfg<D, kNoDQ>;
@@ -455,7 +454,7 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
         // With the transposed dQ the drain needs no shared memory: dQ_i (or,
         // without dQ, dK_i) was the last reader of the stage.  Otherwise the
         // drain returns it.
-        if (C::kDqTransposed) mma_commit(bar(C::kBarStEmpty + s));
+        if (C::kDqTransposed || !C::kDQ) mma_commit(bar(C::kBarStEmpty + s));
       }
       mma_commit(bar(C::kBarMmaDone));
       if (!ok) mbar_wait_drain(bar(C::kBarMmaDone), 0);
@@ -491,9 +490,9 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
         // dQ_i^T has left tensor memory: the MMA may write the columns again.
         tc_fence_before();
         mbar_arrive(bar(C::kBarDQEmpty));
-        // (The per-key-tile store branch is not taken at d = 128 any more:
-        // the deterministic mode computes dQ with its own kernel there.  The
-        // drain without it measured 2% slower, so it stays.)
+        // (The per-key-tile store branch is not taken any more: the
+        // deterministic mode computes dQ with its own kernel.  The kernel
+        // measured 1-2% slower without it, so it stays; see BwdParams.)
         if (det) {  // this key tile's contribution, summed later in key-tile order
 #pragma unroll
           for (int qc = 0; qc < kBlockM; ++qc)
@@ -551,7 +550,7 @@ __device__ __forceinline__ void bwd_body(const BwdParams& p) {
       named_bar_sync(C::kDrainBarrier, kBlockM);
       if (leader) {
         const int q0 = (i_first + it) * kBlockM;
-        if (p.dq_part != nullptr) {  // this key tile's contribution (see BwdParams)
+        if (p.dq_part != nullptr) {  // not taken any more (see BwdParams)
 #pragma unroll 1
           for (int ch = 0; ch < C::kDqChunks; ++ch)
             tma_store_3d(&p.tm_dq, smem_u32(chunk_base(ch)), ch * C::kDqCols, q0, kt * p.BH + bh);
@@ -785,15 +784,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   bwd_body<D, false>(p);
 }
 
-__global__ void __launch_bounds__(BwdCfg<128, true>::kThreads, 1)
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D, true>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
-  bwd_body<128, true>(p);
+  bwd_body<D, true>(p);
 }
 
 template <int D, bool kNoDQ = false>
 cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
   using C = BwdCfg<D, kNoDQ>;
-  void (*kernel)(BwdParams) = kNoDQ ? fa_bwd_dkdv_kernel : fa_bwd_kernel<D>;
+  void (*kernel)(BwdParams) = kNoDQ ? fa_bwd_dkdv_kernel<D> : fa_bwd_kernel<D>;
   // The setmaxnreg split assumes the launch allocation; refuse to run a build
   // whose register count differs (an over-committed split would never finish).
   cudaFuncAttributes attr;
@@ -818,8 +818,10 @@ cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_dkdv(const BwdParams& p, cudaStream_t stream) {
-  return launch_bwd_d<128, true>(p, stream);
+cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream) {
+  if (d == 128) return launch_bwd_d<128, true>(p, stream);
+  if (d == 64) return launch_bwd_d<64, true>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

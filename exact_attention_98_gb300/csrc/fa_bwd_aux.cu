@@ -3,8 +3,6 @@
 //   pre : D_i = sum_t dO_it * O_it  (fp32, from the bf16 O the forward wrote)
 //         and dQacc := 0
 //   post: dQ = dQacc -> bf16  (dS already carries the softmax scale)
-//   dq_reduce (deterministic mode): dQ = sum over key tiles, in key-tile
-//         order, of the per-key-tile contributions -> bf16
 //
 // D is the row term of dS = P * (dP - D): the softmax Jacobian applied to dP
 // (chain rule of the loss sum(O * dO) through P = softmax(S)).
@@ -89,38 +87,6 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const float* __restrict__
   }
 }
 
-// One thread per 8 consecutive d of one row: the contributions of key tiles
-// 0, 1, ... are added in that order (fp32), so the result does not depend on
-// the order in which the key tiles ran.
-__global__ void __launch_bounds__(256) bwd_dq_reduce_kernel(const float* __restrict__ part,
-                                                            __nv_bfloat16* __restrict__ dq,
-                                                            int BH, int N, int d, int n_kblk,
-                                                            int causal, long long n8, float mul) {
-  grid_dependency_wait();  // the contributions of the main kernel before it
-  const int per_row = d / 8;
-  const size_t slice = static_cast<size_t>(BH) * N * d;  // one key tile's contributions
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = i / per_row;  // (bh, q)
-    const int q = static_cast<int>(row % N);
-    const int nc = causal ? min(n_kblk, q / kBlockN + 1) : n_kblk;
-    const float* src = part + static_cast<size_t>(i) * 8;
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int kt = 0; kt < nc; ++kt) {
-      const float4 x = reinterpret_cast<const float4*>(src + kt * slice)[0];
-      const float4 y = reinterpret_cast<const float4*>(src + kt * slice)[1];
-      a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
-      a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
-    }
-    uint4 w;
-    w.x = pack_bf16x2(a[0] * mul, a[1] * mul);
-    w.y = pack_bf16x2(a[2] * mul, a[3] * mul);
-    w.z = pack_bf16x2(a[4] * mul, a[5] * mul);
-    w.w = pack_bf16x2(a[6] * mul, a[7] * mul);
-    reinterpret_cast<uint4*>(dq)[i] = w;
-  }
-}
-
 int grid_for(long long work_items, int per_block) {
   long long g = (work_items + per_block - 1) / per_block;
   const long long cap = 152LL * 16;  // 16 resident 256-thread blocks per SM
@@ -150,16 +116,6 @@ cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, floa
   const long long n8 = elems / 8;  // d is a multiple of 8, so elems is too
   const cudaError_t err = launch_dependent(bwd_post_kernel, dim3(grid_for(n8, 256)), dim3(256), 0,
                                            stream, dq_acc, static_cast<__nv_bfloat16*>(dq), n8, mul);
-  if (err != cudaSuccess) return err;
-  return launched(1);
-}
-
-cudaError_t launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, int n_kblk,
-                                 int causal, float mul, cudaStream_t stream) {
-  const long long n8 = static_cast<long long>(BH) * N * d / 8;
-  const cudaError_t err = launch_dependent(bwd_dq_reduce_kernel, dim3(grid_for(n8, 256)), dim3(256),
-                                           0, stream, dq_part, static_cast<__nv_bfloat16*>(dq), BH,
-                                           N, d, n_kblk, causal, n8, mul);
   if (err != cudaSuccess) return err;
   return launched(1);
 }

@@ -1,4 +1,4 @@
-// dQ of the backward pass by query-stationary CTAs (d = 128), for the
+// dQ of the backward pass by query-stationary CTAs (d = 64 or 128), for the
 // deterministic mode: dQ_i = scale * sum over key tiles j (in order) of
 // dS_ij K_j, accumulated in tensor memory, with no reductions in global
 // memory and no per-key-tile partial sums.
@@ -19,11 +19,12 @@
 //     [  0,128)  S_j (fp32)
 //     [128,256)  dP_j (fp32) -> dS_j (bf16, each warpgroup packs its 64 key
 //                columns into the first 32 of them)
-//     [256,384)  dQ accumulator (fp32)
+//     [256,256+d)  dQ accumulator (fp32)
 //
 // Warp roles (384 threads): warps 0-7 compute (two warpgroups, thread =
 // query row, warpgroup w takes key columns [64 w, 64 w + 64) of every key
-// tile; in the epilogue d columns [64 w, 64 w + 64) of dQ), warp 8 loads,
+// tile; in the epilogue d columns [64 w, 64 w + 64) of dQ, at d = 64 only
+// warpgroup 0), warp 8 loads,
 // warp 9 allocates tensor memory and issues every MMA (the whole warp runs
 // the loop, an elected lane issues).
 //
@@ -37,8 +38,10 @@
 namespace fa {
 namespace {
 
+template <int kD>
 struct DqCfg {
-  static constexpr int D = 128;
+  static constexpr int D = kD;
+  static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kThreads = 384;
   static constexpr int kLaunchRegs = 168;
   static constexpr int kComputeRegs = 200;  // 2 x 128 threads
@@ -97,9 +100,10 @@ enum : unsigned int {
   kSiteMmaDone = 0x228,
 };
 
-__global__ void __launch_bounds__(DqCfg::kThreads, 1)
+template <int kD>
+__global__ void __launch_bounds__(DqCfg<kD>::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ BwdDqParams p) {
-  using C = DqCfg;
+  using C = DqCfg<kD>;
   constexpr int D = C::D;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
         tma_prefetch_desc(&p.tm_v);
         tma_prefetch_desc(&p.tm_do);
         mbar_arrive_expect_tx(bar(C::kBarQFull), 2 * C::kTileBytes);
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < D / 64; ++h) {
           tma_load_3d(sbase + C::kQOff + h * C::kHalfBytes, &p.tm_q, bar(C::kBarQFull), h * 64, q0, bh);
           tma_load_3d(sbase + C::kDOOff + h * C::kHalfBytes, &p.tm_do, bar(C::kBarQFull), h * 64, q0,
                       bh);
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
       auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int kt) {
         if (lane == 0) {
           mbar_arrive_expect_tx(full, C::kTileBytes);
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < D / 64; ++h)
             tma_load_3d(dst + h * C::kHalfBytes, map, full, h * 64, kt * kBlockN, bh);
         }
       };
@@ -361,15 +365,16 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
       if (lane == 0) mbar_arrive(bar(C::kBarDSFull));
     }
 
-    // Epilogue: dQ * scale -> bf16, warpgroup w's 64 d columns staged as one
-    // 128B-swizzle box in the dead Q (w = 0) or dO (w = 1) tile and written
-    // by a bulk tensor store (rows past N dropped by the TMA unit).
+    // Epilogue: dQ * scale -> bf16, warpgroup w's 64 d columns (at d = 64
+    // warpgroup 0's only) staged as one 128B-swizzle box in the dead Q (w = 0)
+    // or dO (w = 1) tile and written by a bulk tensor store (rows past N
+    // dropped by the TMA unit).
     if (ok) {
       ok = mbar_wait(bar(C::kBarMmaDone), 0, ctl, kSiteMmaDone);
       ok = __all_sync(0xffffffffu, ok);
     }
     ok = named_bar_and(C::kEpiBarrier0 + wg, 128, ok);
-    if (ok) {
+    if (ok && wg * 64 < D) {
       tc_fence_after();
       const int stage_off = wg == 0 ? C::kQOff : C::kDOOff;
       uint8_t* stage = smem + stage_off + row * 128;
@@ -408,20 +413,27 @@ __global__ void __launch_bounds__(DqCfg::kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd_dq(const BwdDqParams& p, cudaStream_t stream) {
-  using C = DqCfg;
+template <int D>
+static cudaError_t launch_bwd_dq_d(const BwdDqParams& p, cudaStream_t stream) {
+  using C = DqCfg<D>;
   cudaFuncAttributes attr;
-  cudaError_t err = cudaFuncGetAttributes(&attr, fa_bwd_dq_kernel);
+  cudaError_t err = cudaFuncGetAttributes(&attr, fa_bwd_dq_kernel<D>);
   if (err != cudaSuccess) return err;
   if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
-  err = cudaFuncSetAttribute(fa_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  err = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
   if (err != cudaSuccess) return err;
   const long long blocks = static_cast<long long>(p.n_qtiles) * p.BH;
-  err = launch_dependent(fa_bwd_dq_kernel, dim3(static_cast<unsigned int>(blocks)), dim3(C::kThreads),
-                         C::kSmemBytes, stream, p);
+  err = launch_dependent(fa_bwd_dq_kernel<D>, dim3(static_cast<unsigned int>(blocks)),
+                         dim3(C::kThreads), C::kSmemBytes, stream, p);
   if (err != cudaSuccess) return err;
   return launched(1);
+}
+
+cudaError_t launch_bwd_dq(const BwdDqParams& p, int d, cudaStream_t stream) {
+  if (d == 128) return launch_bwd_dq_d<128>(p, stream);
+  if (d == 64) return launch_bwd_dq_d<64>(p, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

@@ -1,4 +1,4 @@
-// dQ of the backward pass by query-stationary CTAs (deterministic mode, d = 128).
+// dQ of the backward pass by query-stationary CTAs (deterministic mode, d = 64 or 128).
 #pragma once
 
 #include "fa_kernels.h"
@@ -24,6 +24,6 @@ struct BwdDqParams {
 
 // One CTA per (head, 128-row query tile): dQ_i = scale * sum_j dS_ij K_j
 // accumulated in tensor memory over the key tiles in order, written as bf16.
-cudaError_t launch_bwd_dq(const BwdDqParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const BwdDqParams& p, int d, cudaStream_t stream);
 
 }  // namespace fa

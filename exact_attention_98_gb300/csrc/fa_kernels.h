@@ -82,7 +82,7 @@ struct BwdParams {
   CUtensorMap tm_v;
   CUtensorMap tm_do;
   // fp32 dQ target, box {16, 128, 1}, 64B swizzle: the accumulator
-  // [BH, N, d], or in deterministic mode the partial sums [n_kblk * BH, N, d]
+  // [BH, N, d] (or, with dq_part, the per-key-tile slices [n_kblk * BH, N, d])
   CUtensorMap tm_dq;
   // bf16 dK and dV [BH, N, d], box {64, 128, 1}, 128B swizzle (bulk stores)
   CUtensorMap tm_dk;
@@ -90,9 +90,11 @@ struct BwdParams {
   const float* lse;   // fp32 [BH, N]
   const float* dsum;  // fp32 [BH, N]: D = rowsum(dO * O)
   float* dq_acc;      // fp32 [BH, N, d], zeroed before the main kernel (atomic mode)
-  // Deterministic mode (dq_part != nullptr): key tile kt of head bh writes
-  // its dQ contribution to dq_part[kt * BH + bh] (plain stores, no atomics);
-  // a second kernel adds the contributions in key-tile order.
+  // Per-key-tile dQ contributions (key tile kt of head bh would write
+  // dq_part[kt * BH + bh] with plain stores instead of reducing): no entry
+  // point sets it any more (nullptr; the deterministic mode has its own dQ
+  // kernel).  The drains' store branches that read it stay because the
+  // kernel measured 1-2% slower without them (code layout).
   float* dq_part;     // fp32 [n_kblk * BH, N, d]
   void* dk;           // bf16 [BH, N, d]
   void* dv;           // bf16 [BH, N, d]
@@ -197,17 +199,12 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dsum, float* 
                            long long rows, int d, cudaStream_t stream);
 // Backward main kernel (key/value stationary).
 cudaError_t launch_bwd_main(const BwdParams& p, int d, cudaStream_t stream);
-// The same kernel computing dK and dV only (d = 128; p.tm_dq, p.dq_acc and
-// p.dq_part unused): the deterministic mode's first pass.
-cudaError_t launch_bwd_dkdv(const BwdParams& p, cudaStream_t stream);
+// The same kernel computing dK and dV only (p.tm_dq, p.dq_acc and p.dq_part
+// unused): the deterministic mode's first pass.
+cudaError_t launch_bwd_dkdv(const BwdParams& p, int d, cudaStream_t stream);
 // dQ = mul * dQ accumulator -> bf16 (mul: the softmax scale, which the main
 // kernels leave out of dS).
 cudaError_t launch_bwd_post(const float* dq_acc, void* dq, long long elems, float mul,
                             cudaStream_t stream);
-// Deterministic mode: dQ = mul * sum over key tiles kt = 0, 1, ... (in that
-// order) of dq_part[kt] -> bf16.  Causal: query tile i has contributions
-// from kt <= i only.
-cudaError_t launch_bwd_dq_reduce(const float* dq_part, void* dq, int BH, int N, int d, int n_kblk,
-                                 int causal, float mul, cudaStream_t stream);
 
 }  // namespace fa

@@ -224,9 +224,7 @@ int fa_bwd_2cta(const void* q, const void* k, const void* v, const void* o, cons
 
 /*
  * Bytes of device workspace fa_bwd_deterministic needs: fp32 D [B, H, N]
- * (256-byte aligned); at d = 64 also one fp32 dQ contribution per key tile,
- * ceil(N / 128) x [B, H, N, d] (at B2 H16 N4096 d64 about 1.1 GB).  Returns 0
- * for empty or unsupported shapes.
+ * (256-byte aligned).  Returns 0 for empty or unsupported shapes.
  */
 size_t fa_bwd_deterministic_workspace_bytes(int B, int H, int N, int d);
 
@@ -234,19 +232,16 @@ size_t fa_bwd_deterministic_workspace_bytes(int B, int H, int N, int d);
  * Backward with results that are bit-identical from run to run.  The pages
  * single out the backward's dQ reduction (fp32 atomic adds from every key
  * tile, whose order varies between runs) as a cost ("FlashAttention-3 и
- * FlashAttention-4", section "Режим 2-CTA MMA").  At d = 128, dK and dV come
- * from fa_bwd's key-stationary kernel without its dQ product, and dQ from a
+ * FlashAttention-4", section "Режим 2-CTA MMA").  Here dK and dV come from
+ * fa_bwd's key-stationary kernel without its dQ product, and dQ from a
  * second, query-stationary kernel that recomputes P and dS for its query
  * tile and adds dS K over the key tiles in order (causal: key tiles 0..i for
- * query tile i) in tensor memory; at d = 64 each key tile writes its dQ
- * contribution with plain stores and a second kernel adds the contributions
- * in key-tile order.  dK and dV are deterministic in both entry points (each
- * key tile owns its rows and accumulates them in a fixed order) and equal
- * to fa_bwd's bit for bit.
+ * query tile i) in tensor memory.  dK and dV are deterministic in both entry
+ * points (each key tile owns its rows and accumulates them in a fixed order)
+ * and equal to fa_bwd's bit for bit.
  * Same arguments, results and errors as fa_bwd; the workspace must hold
- * fa_bwd_deterministic_workspace_bytes(B, H, N, d) bytes.  Slower than fa_bwd:
- * at d = 128 by the recomputed S and dP products, at d = 64 by the memory
- * traffic of the contributions.
+ * fa_bwd_deterministic_workspace_bytes(B, H, N, d) bytes.  Slower than fa_bwd
+ * by the recomputed S and dP products.
  */
 int fa_bwd_deterministic(const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,

@@ -55,8 +55,8 @@ def test_workspace_bytes(lib):
     assert ws(0, 1, 1, 64) == 0
     assert ws(1, 1, 1, 96) == 0  # unsupported head dim
     det = lib.fa_bwd_deterministic_workspace_bytes
-    assert det(B, H, N, d) == up(4 * rows)  # d = 128: D only
-    assert det(1, 1, 129, 64) == up(4 * 129) + up(4 * 129 * 64 * 2)  # d = 64: D and parts
+    assert det(B, H, N, d) == up(4 * rows)  # D only: dQ accumulates in tensor memory
+    assert det(1, 1, 129, 64) == up(4 * 129)
     assert det(0, 1, 1, 64) == 0
 
 
@@ -149,8 +149,6 @@ def test_bwd_deterministic_validation(lib):
         a, a, a, a, a, a, a, a, a, 1, 1, 256, d, 0.125, 0, P(ws), nbytes, None)
     assert call(0, need) == lib.FA_ERR_WORKSPACE
     assert call(0x10000, need - 1) == lib.FA_ERR_WORKSPACE
-    # the atomic backward's smaller workspace is not enough
-    assert call(0x10000, lib.fa_bwd_workspace_bytes(1, 1, 256, 64)) == lib.FA_ERR_WORKSPACE
     assert call(0x10000, need, d=96) == lib.FA_ERR_UNSUPPORTED
 
 

@@ -1,9 +1,8 @@
-"""The deterministic backward (fa_bwd_deterministic): at d = 128 dK and dV
-from the key-stationary kernel without its dQ product and dQ from a
-query-stationary kernel adding the key tiles in order in tensor memory; at
-d = 64 per-key-tile dQ contributions added in key-tile order.  No fp32
-atomics either way.  Same bounds against the fp64 oracle as fa_bwd, and
-bit-identical results from run to run."""
+"""The deterministic backward (fa_bwd_deterministic): dK and dV from the
+key-stationary kernel without its dQ product and dQ from a query-stationary
+kernel adding the key tiles in order in tensor memory, with no fp32 atomics.
+Same bounds against the fp64 oracle as fa_bwd, and bit-identical results
+from run to run."""
 import numpy as np
 import pytest
 import torch
